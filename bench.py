@@ -1,0 +1,357 @@
+"""Benchmark of the HC gated residual on GB300 (one JSON line on rank 0).
+
+Workload (one "step"): the decode sweep -- one forward call at each of
+M = 2, 4, 8, 16, 32 tokens, HC=4, HS=2560 (K=10240), r=320, bf16, seeded
+synthetic inputs (weights ~ N(0, 1/sqrt(fan-in)), Wnorm ~ N(0, 0.1), R and y
+~ N(0, 1), inj ~ N(0, 2)).  value = tokens per second over K timed steps.
+
+Timing: the device-side number replays one CUDA graph per step (the five
+calls), rotating over NSETS distinct weight+activation sets whose total
+footprint exceeds twice the L2, so weights stream from HBM on every call.
+The e2e number calls the public API eagerly with pinned host inputs copied in
+and every output copied back inside the timed region.  Also reported: the
+per-M latency table, the roofline of the decode kernel against the measured
+HBM peak, SM clocks sampled during the timed region, and the fp64 CPU oracle
+timed on a bounded sample (cpu_baseline).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+SWEEP = (2, 4, 8, 16, 32)
+HC, HS, R_LOW = 4, 2560, 320
+K_DIM = HC * HS
+METRIC = "HC gated-residual µs/call & tokens/s vs M (HC4,HS2560,r320 bf16); % roofline"
+WEIGHT_BYTES = 2 * (R_LOW + HC) * K_DIM + 2 * K_DIM * R_LOW + 2 * K_DIM     # Wd, Wi, Wu, Wnorm
+ACT_BYTES_PER_TOKEN = (2 * K_DIM + 2 * HS + 4 * HC + 2 * K_DIM + 4 * HC + 4 * HC
+                       + 4 * R_LOW + 2 * HS)                                   # R y inj R2 rrms inj_next lora x
+FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clock and throttle reasons during a region."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- CPU baseline
+def cpu_baseline(seconds: float = 12.0, max_steps: int | None = None, warmup: int = 0) -> dict:
+    """The fp64 oracle, single-threaded BLAS, on the sweep's token mix.
+
+    Runs in a child process with one BLAS thread so the core count is exact
+    and no CUDA state is touched.  Repeats whole sweeps until `seconds` of
+    CPU work (or max_steps sweeps) and returns tokens/s.
+    """
+    code = f"""
+import sys, time, json
+sys.path.insert(0, {ROOT!r})
+import oracle
+from hyper_connection_gated_gb300 import inputs
+w = {{k: inputs.bf16_bits_to_f64(v) for k, v in inputs.weights().items()}}
+a = inputs.activations(32)
+R = inputs.bf16_bits_to_f64(a['R']); y = inputs.bf16_bits_to_f64(a['y']); inj = a['inj'].astype('f8')
+sweep = {list(SWEEP)!r}
+for _ in range({warmup}):
+    for M in sweep:
+        oracle.forward(R=R[:M], y=y[:M], inj=inj[:M], Wnorm=w['Wnorm'], Wd=w['Wd'], Wi=w['Wi'],
+                       Wu=w['Wu'], eps=1e-6)
+t0 = time.perf_counter(); n = 0; tok = 0
+while True:
+    for M in sweep:
+        oracle.forward(R=R[:M], y=y[:M], inj=inj[:M], Wnorm=w['Wnorm'], Wd=w['Wd'], Wi=w['Wi'],
+                       Wu=w['Wu'], eps=1e-6)
+        tok += M
+    n += 1
+    el = time.perf_counter() - t0
+    if el >= {seconds} or ({max_steps!r} is not None and n >= ({max_steps!r} or 0)):
+        break
+print(json.dumps({{"tokens": tok, "seconds": el, "sweeps": n}}))
+"""
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=600)
+    if res.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                "error": res.stderr[-500:]}
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": f"{d['sweeps']} sweeps of M={list(SWEEP)} ({d['tokens']} tokens), fp64 numpy, "
+                      f"1 BLAS thread, {d['seconds']:.1f} s"}
+
+
+# ---------------------------------------------------------------- main arm
+def run_ours(args, rank, world):
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import HcGatedResidual, _native, inputs
+
+    dev = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 126 * 1024 * 1024)
+    per_set = WEIGHT_BYTES + sum(SWEEP) * ACT_BYTES_PER_TOKEN
+    nsets = max(4, int(np.ceil(2.0 * l2 / per_set)) + 1)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = inputs.weights()
+    a = inputs.activations(max(SWEEP))
+    base = {k: bf(v) for k, v in w.items()}
+    base.update(R=bf(a["R"]), y=bf(a["y"]), inj=torch.from_numpy(a["inj"]).cuda())
+    sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
+    op = HcGatedResidual(max_M=max(SWEEP))
+    outs = {M: [op.forward(s["R"][:M], s["y"][:M], s["inj"][:M], s["Wnorm"], s["Wu"],
+                           Wd=s["Wd"], Wi=s["Wi"]) for s in sets] for M in SWEEP}
+    op.check()
+
+    def prepared(M, j):
+        s, o = sets[j], outs[M][j]
+        ar = _native.Args()
+        ar.M, ar.HC, ar.HS, ar.r, ar.eps = M, HC, HS, R_LOW, 1e-6
+        ar.R, ar.y, ar.inj, ar.ld_inj = s["R"].data_ptr(), s["y"].data_ptr(), s["inj"].data_ptr(), HC
+        ar.Wnorm, ar.Wd, ar.Wi, ar.Wu = (s["Wnorm"].data_ptr(), s["Wd"].data_ptr(),
+                                         s["Wi"].data_ptr(), s["Wu"].data_ptr())
+        ar.R2, ar.rrms, ar.inj_next = o["R2"].data_ptr(), o["rrms"].data_ptr(), o["inj_next"].data_ptr()
+        ar.x, ar.lora = o["x"].data_ptr(), o["lora"].data_ptr()
+        return ar
+
+    args_tab = {(M, j): prepared(M, j) for M in SWEEP for j in range(nsets)}
+    stream = torch.cuda.Stream()
+
+    def capture(calls):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for ar in calls:
+                st = op.forward_raw(ar, torch.cuda.current_stream().cuda_stream)
+                assert st == 0, st
+        return g
+
+    step_graphs = [capture([args_tab[(M, j)] for M in SWEEP]) for j in range(nsets)]
+    per_m_graphs = {M: capture([args_tab[(M, j)] for j in range(nsets)]) for M in SWEEP}
+    torch.cuda.synchronize()
+
+    # per-M latency (graph replay, nsets calls per replay)
+    per_m = {}
+    with torch.cuda.stream(stream):
+        for M in SWEEP:
+            for _ in range(3):
+                per_m_graphs[M].replay()
+            samples = []
+            for _ in range(5):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for _ in range(4):
+                    per_m_graphs[M].replay()
+                e1.record(stream)
+                e1.synchronize()
+                samples.append(e0.elapsed_time(e1) * 1e3 / (4 * nsets))
+            per_m[M] = statistics.median(samples)
+
+    # timed steps
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            step_graphs[i % nsets].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(dev) as clk:
+        time.sleep(0.3)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for i in range(args.steps):
+                step_graphs[i % nsets].replay()
+            e1.record(stream)
+        e1.synchronize()
+        time.sleep(0.2)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        torch.distributed.barrier()
+        t = torch.tensor([ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    op.check(stream)
+    tokens_per_step = sum(SWEEP)
+    value = tokens_per_step * args.steps * world / (ms / 1e3)
+
+    # e2e through the public API: pinned host inputs in, all outputs back
+    host_in = {M: {k: v[:M].cpu().pin_memory() for k, v in (("R", base["R"]), ("y", base["y"]),
+                                                             ("inj", base["inj"]))}
+               for M in SWEEP}
+    dev_in = {M: {k: torch.empty_like(v, device="cuda") for k, v in host_in[M].items()} for M in SWEEP}
+    host_out = {M: {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs[M][0].items()}
+                for M in SWEEP}
+    h2d = sum(t.numel() * t.element_size() for M in SWEEP for t in host_in[M].values())
+    d2h = sum(t.numel() * t.element_size() for M in SWEEP for t in host_out[M].values())
+
+    def e2e_step(j):
+        s = sets[j]
+        for M in SWEEP:
+            for k, v in host_in[M].items():
+                dev_in[M][k].copy_(v, non_blocking=True)
+            o = op.forward(dev_in[M]["R"], dev_in[M]["y"], dev_in[M]["inj"], s["Wnorm"], s["Wu"],
+                           Wd=s["Wd"], Wi=s["Wi"], out=outs[M][j])
+            for k, v in o.items():
+                host_out[M][k].copy_(v, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    with torch.cuda.stream(stream):
+        for i in range(args.warmup):
+            e2e_step(i % nsets)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            e2e_step(i % nsets)
+        e2e_s = time.perf_counter() - t0
+    e2e_value = tokens_per_step * args.steps * world / e2e_s
+
+    hbm, bf16_peak, peak_src = peaks()
+    alg_bytes = sum(WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN for M in SWEEP)
+    kernel_us = sum(per_m[M] for M in SWEEP)
+    achieved = alg_bytes / (kernel_us * 1e-6) / 1e9
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/sqrt(fan-in)) weights)",
+        "config": {"workload": "decode sweep M={2,4,8,16,32}, HC=4 HS=2560 r=320 bf16, "
+                               "unfolded Wd/Wi", "tokens_per_step": tokens_per_step,
+                   "l2": f"rotating {nsets} weight+input sets ({nsets * per_set / 1e6:.0f} MB > 2x L2)",
+                   "timing": "CUDA graph replay, CUDA events on the launching stream",
+                   "parallelism": f"replicas x{world}"},
+        "clocks": clocks,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": len(SWEEP) * args.steps,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                     "frac": achieved / hbm, "traffic": None,
+                     "kernel": "decode_kernel (per launch: weights + activations)",
+                     "peak_source": peak_src},
+        "per_M_us": {str(M): per_m[M] for M in SWEEP},
+        "per_M_roofline_frac": {str(M): (WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN) / hbm / 1e3
+                                / per_m[M] for M in SWEEP},
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        # The reference arm is the fp64 CPU oracle on the host cores; rank 0 only.
+        if rank != 0:
+            return
+        steps = args.steps
+        res = cpu_baseline(seconds=1e9, max_steps=steps, warmup=args.warmup)
+        line = {"impl": "reference", "metric": METRIC, "value": res["value"], "unit": "tokens/s",
+                "n_gpus": 1, "steps": steps, "warmup": args.warmup,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": "decode sweep M={2,4,8,16,32}, HC=4 "
+                                                            "HS=2560 r=320 (fp64 oracle)"},
+                "cpu_baseline": {k: res.get(k) for k in ("value", "unit", "cores", "kind", "sample")},
+                "e2e": {"value": res["value"], "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline()
+        print(json.dumps(line))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

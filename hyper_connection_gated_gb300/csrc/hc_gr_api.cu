@@ -1,0 +1,281 @@
+// C ABI of the HC gated residual: argument validation, the handle's
+// workspace, the M-based dispatch between the decode and prefill paths, and
+// device status reporting.  The operation and the layouts are documented in
+// include/hc_gr.h.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "hc_gr_internal.cuh"
+
+struct hc_gr_ctx {
+  hcgr::Device dev;
+  hcgr::Workspace ws;
+  int64_t max_M = 0;
+  int K_max = 0;
+  int n_out_max = 0;
+  int HC_max = 0;
+  int r_max = 0;
+  char last_cuda[256] = {0};
+};
+
+namespace {
+
+using hcgr::bf16_t;
+
+struct DeviceGuard {
+  int prev = -1;
+  explicit DeviceGuard(int id) {
+    if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
+    if (prev != id) cudaSetDevice(id);
+  }
+  ~DeviceGuard() {
+    if (prev >= 0) cudaSetDevice(prev);
+  }
+};
+
+int cuda_fail(hc_gr_ctx* h, cudaError_t e) {
+  if (h) std::snprintf(h->last_cuda, sizeof(h->last_cuda), "%s", cudaGetErrorString(e));
+  return HC_GR_ERR_CUDA;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range span(const void* p, int64_t bytes) {
+  const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+  return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+bool overlap(const Range& a, const Range& b) {
+  return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo;
+}
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+}  // namespace
+
+extern "C" {
+
+const char* hc_gr_strerror(int status) {
+  switch (status) {
+    case HC_GR_OK: return "ok";
+    case HC_GR_ERR_INVALID_ARG: return "invalid argument";
+    case HC_GR_ERR_UNSUPPORTED: return "unsupported shape or device";
+    case HC_GR_ERR_ALIAS: return "an output overlaps another output or an input";
+    case HC_GR_ERR_CUDA: return "CUDA error";
+    case HC_GR_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+const char* hc_gr_last_cuda_error(hc_gr_handle h) { return h ? h->last_cuda : ""; }
+
+int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, int r) {
+  if (!out) return HC_GR_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (max_M < 1 || HC < 1 || HS < 1 || r < 1 || device < 0) return HC_GR_ERR_INVALID_ARG;
+  if (HS % 8 != 0 || r % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
+  hc_gr_ctx* h = new (std::nothrow) hc_gr_ctx();
+  if (!h) return HC_GR_ERR_CUDA;
+  DeviceGuard guard(device);
+  cudaDeviceProp prop;
+  cudaError_t e = cudaGetDeviceProperties(&prop, device);
+  if (e != cudaSuccess) {
+    delete h;
+    return HC_GR_ERR_CUDA;
+  }
+  if (!(prop.major == 10 && prop.minor == 3)) {
+    delete h;
+    return HC_GR_ERR_UNSUPPORTED;
+  }
+  h->dev.id = device;
+  h->dev.sms = prop.multiProcessorCount;
+  h->dev.smem_optin = static_cast<int>(prop.sharedMemPerBlockOptin);
+  h->dev.l2_bytes = prop.l2CacheSize;
+  h->max_M = max_M;
+  h->K_max = HC * HS;
+  h->HC_max = HC;
+  h->r_max = r;
+  h->n_out_max = r + HC;
+
+  // one allocation: [bar/err | part | sumsq | lora | prefill]
+  const size_t part_f = hcgr::decode_ws_part_floats(h->dev, h->K_max, h->n_out_max);
+  const size_t sumsq_f = static_cast<size_t>(h->dev.sms) * hcgr::DECODE_MAX_M;
+  const size_t lora_f = static_cast<size_t>(max_M) * r;
+  size_t off = 0;
+  const size_t off_ctl = off;    off += 256;
+  const size_t off_part = off;   off = align_up(off + part_f * 4, 256);
+  const size_t off_sumsq = off;  off = align_up(off + sumsq_f * 4, 256);
+  const size_t off_lora = off;   off = align_up(off + lora_f * 4, 256);
+  const size_t off_pre = off;    off = align_up(off + hcgr::prefill_ws_bytes(max_M, HC, HS, r), 256);
+  void* base = nullptr;
+  e = cudaMalloc(&base, off);
+  if (e != cudaSuccess) {
+    delete h;
+    return HC_GR_ERR_CUDA;
+  }
+  e = cudaMemset(base, 0, 256);
+  if (e != cudaSuccess) {
+    cudaFree(base);
+    delete h;
+    return HC_GR_ERR_CUDA;
+  }
+  unsigned char* b = static_cast<unsigned char*>(base);
+  h->ws.base = base;
+  h->ws.bytes = off;
+  h->ws.bar = reinterpret_cast<unsigned*>(b + off_ctl);
+  h->ws.err = reinterpret_cast<int*>(b + off_ctl + 64);
+  h->ws.part = reinterpret_cast<float*>(b + off_part);
+  h->ws.sumsq = reinterpret_cast<float*>(b + off_sumsq);
+  h->ws.lora = reinterpret_cast<float*>(b + off_lora);
+  h->ws.k1_part = reinterpret_cast<float*>(b + off_pre);
+  *out = h;
+  return HC_GR_OK;
+}
+
+int hc_gr_destroy(hc_gr_handle h) {
+  if (!h) return HC_GR_OK;
+  int st = HC_GR_OK;
+  {
+    DeviceGuard guard(h->dev.id);
+    cudaDeviceSynchronize();
+    if (h->ws.base && cudaFree(h->ws.base) != cudaSuccess) st = HC_GR_ERR_CUDA;
+  }
+  delete h;
+  return st;
+}
+
+int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* stream) {
+  if (!h || !a) return HC_GR_ERR_INVALID_ARG;
+  const int64_t M = a->M;
+  const int HC = a->HC, HS = a->HS, r = a->r;
+  if (M < 1 || HC < 1 || HS < 1 || r < 1) return HC_GR_ERR_INVALID_ARG;
+  if (!(std::isfinite(a->eps) && a->eps > 0.0f)) return HC_GR_ERR_INVALID_ARG;
+  if (a->force_path < HC_GR_PATH_AUTO || a->force_path > HC_GR_PATH_PREFILL)
+    return HC_GR_ERR_INVALID_ARG;
+  const int64_t ld_inj = a->ld_inj == 0 ? HC : a->ld_inj;
+  if (ld_inj < HC) return HC_GR_ERR_INVALID_ARG;
+  const bool merged = a->Wdi != nullptr;
+  if (!a->R || !a->y || !a->inj || !a->Wnorm || !a->Wu || !a->R2 || !a->rrms ||
+      !a->inj_next || !a->x)
+    return HC_GR_ERR_INVALID_ARG;
+  if (!merged && (!a->Wd || !a->Wi)) return HC_GR_ERR_INVALID_ARG;
+  const void* p16[] = {a->R, a->y, a->Wnorm, a->Wu, a->R2, a->x,
+                       merged ? a->Wdi : a->Wd, merged ? a->Wdi : a->Wi};
+  for (const void* p : p16)
+    if (!aligned(p, 16)) return HC_GR_ERR_INVALID_ARG;
+  const void* p4[] = {a->inj, a->rrms, a->inj_next, a->lora};
+  for (const void* p : p4)
+    if (!aligned(p, 4)) return HC_GR_ERR_INVALID_ARG;
+  if (HS % 8 != 0 || r % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
+  const int64_t K = static_cast<int64_t>(HC) * HS;
+  if (M > h->max_M || K > h->K_max || r + HC > h->n_out_max) return HC_GR_ERR_UNSUPPORTED;
+  if (merged && a->n_pad < r + HC) return HC_GR_ERR_UNSUPPORTED;
+  if (a->force_path == HC_GR_PATH_DECODE && M > hcgr::DECODE_MAX_M) return HC_GR_ERR_UNSUPPORTED;
+
+  // outputs must not overlap each other or any input
+  const Range outs[] = {span(a->R2, M * K * 2), span(a->rrms, M * HC * 4),
+                        span(a->inj_next, M * HC * 4), span(a->x, M * HS * 2),
+                        a->lora ? span(a->lora, M * r * 4) : Range{0, 0}};
+  const Range ins[] = {span(a->R, M * K * 2), span(a->y, M * HS * 2),
+                       span(a->inj, ((M - 1) * ld_inj + HC) * 4), span(a->Wnorm, K * 2),
+                       span(a->Wu, K * r * 2),
+                       merged ? span(a->Wdi, static_cast<int64_t>(a->n_pad) * K * 2)
+                              : span(a->Wd, static_cast<int64_t>(r) * K * 2),
+                       merged ? Range{0, 0} : span(a->Wi, static_cast<int64_t>(HC) * K * 2)};
+  const int nouts = sizeof(outs) / sizeof(outs[0]);
+  for (int i = 0; i < nouts; ++i) {
+    for (int j = i + 1; j < nouts; ++j)
+      if (overlap(outs[i], outs[j])) return HC_GR_ERR_ALIAS;
+    for (const Range& in : ins)
+      if (overlap(outs[i], in)) return HC_GR_ERR_ALIAS;
+  }
+
+  hcgr::Call c;
+  c.M = M;
+  c.HC = HC;
+  c.HS = HS;
+  c.r = r;
+  c.K = static_cast<int>(K);
+  c.n_out = r + HC;
+  c.eps = a->eps;
+  c.R = static_cast<const bf16_t*>(a->R);
+  c.y = static_cast<const bf16_t*>(a->y);
+  c.inj = a->inj;
+  c.ld_inj = ld_inj;
+  c.Wnorm = static_cast<const bf16_t*>(a->Wnorm);
+  if (merged) {
+    c.Wd = static_cast<const bf16_t*>(a->Wdi);
+    c.Wi = c.Wd + static_cast<int64_t>(r) * K;
+  } else {
+    c.Wd = static_cast<const bf16_t*>(a->Wd);
+    c.Wi = static_cast<const bf16_t*>(a->Wi);
+  }
+  c.fold = a->fold_w ? 1 : 0;
+  c.Wu = static_cast<const bf16_t*>(a->Wu);
+  c.R2 = static_cast<bf16_t*>(a->R2);
+  c.rrms = a->rrms;
+  c.inj_next = a->inj_next;
+  c.x = static_cast<bf16_t*>(a->x);
+  c.lora = a->lora ? a->lora : h->ws.lora;
+  c.debug_fault = a->debug_fault;
+
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  DeviceGuard guard(h->dev.id);
+  int path = a->force_path;
+  if (path == HC_GR_PATH_AUTO) path = M <= hcgr::DECODE_MAX_M ? HC_GR_PATH_DECODE : HC_GR_PATH_PREFILL;
+  cudaError_t e = path == HC_GR_PATH_DECODE ? hcgr::launch_decode(c, h->ws, h->dev, s)
+                                            : hcgr::launch_prefill(c, h->ws, h->dev, s);
+  if (e == cudaErrorNotSupported) return HC_GR_ERR_UNSUPPORTED;
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return HC_GR_OK;
+}
+
+int hc_gr_forward(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps, const void* R,
+                  const void* y, const float* inj, const void* Wnorm, const void* Wd,
+                  const void* Wi, const void* Wu, void* R2, float* rrms, float* inj_next,
+                  void* x, float* lora, struct CUstream_st* stream) {
+  hc_gr_args a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = M;
+  a.HC = HC;
+  a.HS = HS;
+  a.r = r;
+  a.eps = eps;
+  a.R = R;
+  a.y = y;
+  a.inj = inj;
+  a.Wnorm = Wnorm;
+  a.Wd = Wd;
+  a.Wi = Wi;
+  a.Wu = Wu;
+  a.R2 = R2;
+  a.rrms = rrms;
+  a.inj_next = inj_next;
+  a.x = x;
+  a.lora = lora;
+  return hc_gr_forward_ex(h, &a, stream);
+}
+
+int hc_gr_check(hc_gr_handle h, struct CUstream_st* stream) {
+  if (!h) return HC_GR_ERR_INVALID_ARG;
+  DeviceGuard guard(h->dev.id);
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  int dev_status = 0;
+  e = cudaMemcpy(&dev_status, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  if (dev_status == hcgr::DEV_OK) return HC_GR_OK;
+  // clear the status and the barrier words so the handle can be used again
+  e = cudaMemset(h->ws.base, 0, 256);
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return HC_GR_ERR_TIMEOUT;
+}
+
+}  // extern "C"

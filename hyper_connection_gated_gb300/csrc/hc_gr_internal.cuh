@@ -1,0 +1,219 @@
+// Internal declarations shared by the HC-GR CUDA sources (not part of the ABI).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/hc_gr.h"
+
+namespace hcgr {
+
+using bf16_t = uint16_t;
+
+// Device status word values (the handle's err word).
+constexpr int DEV_OK = 0;
+constexpr int DEV_TIMEOUT = 1;
+
+// Workspace of a handle: all device memory the library owns.
+struct Workspace {
+  float* part = nullptr;      // decode: per-CTA split-K partial products
+  float* sumsq = nullptr;     // decode: per-CTA partial sums of R2^2
+  float* lora = nullptr;      // lora when the caller passes lora == NULL
+  unsigned* bar = nullptr;    // grid barrier: [0] arrivals, [1] generation
+  int* err = nullptr;         // device status word
+  void* base = nullptr;       // single allocation holding everything above
+  size_t bytes = 0;
+  // prefill workspace
+  float* k1_part = nullptr;   // [HC][M][NP] per-stream products, rrms applied
+  bf16_t* h = nullptr;        // [M][r] bf16 SiLU(lora / HC), the up-GEMM operand
+  float* wfold = nullptr;     // unused placeholder for future folded weights
+};
+
+// Everything one forward call needs after validation.
+struct Call {
+  int64_t M;
+  int HC, HS, r, K, n_out;
+  float eps;
+  const bf16_t* R;
+  const bf16_t* y;
+  const float* inj;
+  int64_t ld_inj;
+  const bf16_t* Wnorm;
+  const bf16_t* Wd;   // row n < r of the projection weight: Wd + n * K
+  const bf16_t* Wi;   // row j < HC of the inject weight:   Wi + j * K
+  int fold;
+  const bf16_t* Wu;
+  bf16_t* R2;
+  float* rrms;
+  float* inj_next;
+  bf16_t* x;
+  float* lora;        // never NULL here (workspace substitute)
+  int debug_fault;
+};
+
+struct Device {
+  int id = 0;
+  int sms = 0;
+  int smem_optin = 0;
+  int l2_bytes = 0;
+};
+
+// Decode path (M <= DECODE_MAX_M): one cooperative persistent kernel.
+constexpr int DECODE_MAX_M = 32;
+int decode_grid(const Device& dev, int HC, int HS);
+size_t decode_ws_part_floats(const Device& dev, int HC_times_HS_max, int n_out_max);
+cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
+                          cudaStream_t stream);
+
+// Prefill path: tcgen05 tensor-core kernels.
+cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev,
+                           cudaStream_t stream);
+size_t prefill_ws_bytes(int64_t max_M, int HC, int HS, int r);
+
+// ------------------------------------------------------------ device helpers
+#if defined(__CUDACC__)
+
+__device__ __forceinline__ float bf16_to_f32(bf16_t v) {
+  return __uint_as_float(static_cast<uint32_t>(v) << 16);
+}
+
+// Round-to-nearest-even float -> bf16 (NaN kept quiet).
+__device__ __forceinline__ bf16_t f32_to_bf16(float f) {
+  uint32_t u = __float_as_uint(f);
+  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<bf16_t>((u >> 16) | 0x40u);
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<bf16_t>(u >> 16);
+}
+
+__device__ __forceinline__ void unpack8(const uint4 v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  return static_cast<uint32_t>(f32_to_bf16(a)) | (static_cast<uint32_t>(f32_to_bf16(b)) << 16);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// --- mbarrier
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+               ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+  return ok != 0;
+}
+
+// Bounded wait on an mbarrier phase.  On expiry it records DEV_TIMEOUT in the
+// status word and returns false; the caller then skips the dependent work.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 15u) == 0) {
+      if (globaltimer_ns() - t0 > limit_ns) {
+        atomicCAS(err, DEV_OK, DEV_TIMEOUT);
+        return false;
+      }
+      if (*((volatile int*)err) != DEV_OK) return false;
+    }
+  }
+}
+
+// 1-D bulk async copy global -> shared, completion counted on an mbarrier.
+// src, dst 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Grid-wide barrier for a cooperative launch.  bar[0] counts arrivals and is
+// reset by the last arriver, which then bumps the generation bar[1]; waiters
+// spin on the generation with a time limit.  Every call starts from
+// bar[0] == 0, so calls with different grid sizes or shapes cannot alias a
+// phase.  Returns false (all threads of the CTA) when the wait expired or
+// another CTA reported an error; the CTA must then leave.
+__device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err,
+                                             uint64_t limit_ns, int* s_flag) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    const unsigned gen = ld_acquire_u32(bar + 1);
+    __threadfence();
+    const unsigned prev = atomicAdd(bar, 1u);
+    if (prev == nblocks - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      st_release_u32(bar + 1, gen + 1);
+    } else {
+      const uint64_t t0 = globaltimer_ns();
+      uint32_t it = 0;
+      while (ld_acquire_u32(bar + 1) == gen) {
+        if ((++it & 31u) == 0) {
+          if (*((volatile int*)err) != DEV_OK) { ok = 0; break; }
+          if (globaltimer_ns() - t0 > limit_ns) {
+            atomicCAS(err, DEV_OK, DEV_TIMEOUT);
+            ok = 0;
+            break;
+          }
+        }
+      }
+    }
+    __threadfence();
+    *s_flag = ok;
+  }
+  __syncthreads();
+  return *s_flag != 0;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float sigmoidf_dev(float v) { return 1.0f / (1.0f + expf(-v)); }
+
+#endif  // __CUDACC__
+
+}  // namespace hcgr

@@ -1,0 +1,147 @@
+/*
+ * hc_gr.h -- C ABI of the Hyper-Connection gated residual (HC-GR) for one
+ * GB300 GPU (sm_103a).
+ *
+ * The operation (aiter PR #5913, "Two-stage Hyper-Connection Gated Residual
+ * kernel", section "Technical Details"), per token, with HC residual streams
+ * of width HS, K = HC * HS and low rank r:
+ *
+ *   (COMBINE) iw[s] = 2 * sigmoid(inj[s] / HC)
+ *             R2[s, c] = R[s, c] + y[c] * iw[s]              -> stored in bf16
+ *   (N)       rrms[s] = 1 / sqrt(mean_c R2[s, c]^2 + eps)
+ *             xn[s, c] = R2[s, c] * rrms[s] * (1 + Wnorm[s * HS + c])
+ *   (G1)      lora = xn . Wd^T            (r values, stored before SiLU)
+ *             h = SiLU(lora / HC)
+ *   (INJ)     inj_next = xn . Wi^T        (HC values, the next layer's logits)
+ *   (G2)      G = sigmoid(h . Wu^T)       (K values, never stored)
+ *   (MIX)     x[c] = (1 / HC) * sum_s G[s * HS + c] * xn[s * HS + c]
+ *
+ * R2 is rounded to bf16 before rrms and everything after it are computed, the
+ * way the page's second kernel rebuilds xn from the stored R2 and rrms.
+ *
+ * Types and layouts (all row-major, contiguous unless a leading dimension is
+ * given; M tokens):
+ *   R, R2      [M, HC, HS] bf16        y, x      [M, HS] bf16
+ *   inj        [M, HC] fp32 (row stride ld_inj >= HC in hc_gr_forward_ex)
+ *   rrms, inj_next [M, HC] fp32        lora      [M, r] fp32
+ *   Wnorm      [K] bf16                Wd        [r, K] bf16
+ *   Wi         [HC, K] bf16            Wu        [K, r] bf16
+ *   Wdi        [n_pad, K] bf16 merged down/inject weight: rows 0..r-1 = Wd,
+ *              rows r..r+HC-1 = Wi, rows r+HC..n_pad-1 are never read.  With
+ *              fold_w = 1 every column k already carries the factor
+ *              (1 + Wnorm[k]) (the "(1+w) folded in" weight of the page's
+ *              Performance setup); Wnorm is then still read for the mix.
+ * bf16 is passed as raw 16-bit storage (const void*).  Every pointer is a
+ * device pointer, 16-byte aligned, owned by the caller; the library never
+ * frees or retains it past the call.  HS must be a multiple of 8 and r a
+ * multiple of 8.
+ *
+ * Streams and concurrency: hc_gr_forward* only enqueues work on `stream`
+ * (a cudaStream_t; NULL is the legacy default stream) and returns.  A handle
+ * owns one workspace (cross-CTA partial sums, a grid-barrier word pair and
+ * a device status word); calls on one handle must be ordered on one stream.
+ * Use one handle per concurrent stream.
+ *
+ * Errors: every entry point returns an hc_gr_status.  Argument errors are
+ * detected on the host before anything is enqueued and leave outputs
+ * untouched.  A device-side failure (a bounded wait that expired) is
+ * recorded in the handle and reported by hc_gr_check.
+ */
+#ifndef HC_GR_H_
+#define HC_GR_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
+
+typedef struct hc_gr_ctx* hc_gr_handle;
+
+typedef enum hc_gr_status {
+  HC_GR_OK = 0,
+  HC_GR_ERR_INVALID_ARG = 1, /* NULL pointer, M < 1, eps <= 0 or not finite,
+                                misaligned pointer, ld_inj < HC, bad path */
+  HC_GR_ERR_UNSUPPORTED = 2, /* shape outside what the handle was created for,
+                                HS or r not a multiple of 8, n_pad < r + HC */
+  HC_GR_ERR_ALIAS = 3,       /* an output overlaps another output or an input */
+  HC_GR_ERR_CUDA = 4,        /* a CUDA call failed (launch, allocation, copy) */
+  HC_GR_ERR_TIMEOUT = 5      /* a device-side bounded wait expired */
+} hc_gr_status;
+
+typedef enum hc_gr_path {
+  HC_GR_PATH_AUTO = 0,    /* M <= 32: decode kernel, otherwise prefill kernels */
+  HC_GR_PATH_DECODE = 1,  /* weight-streaming persistent kernel, M <= 32 */
+  HC_GR_PATH_PREFILL = 2  /* tensor-core (tcgen05) two-stage kernels */
+} hc_gr_path;
+
+/* Full argument set of hc_gr_forward_ex.  Zero-initialise, then fill. */
+typedef struct hc_gr_args {
+  int64_t M;
+  int32_t HC, HS, r;
+  float eps;
+  const void* R;
+  const void* y;
+  const float* inj;
+  int64_t ld_inj;      /* row stride of inj in floats; 0 means HC */
+  const void* Wnorm;
+  const void* Wd;      /* separate down weight [r, K]; used when Wdi == NULL */
+  const void* Wi;      /* separate inject weight [HC, K] */
+  const void* Wdi;     /* merged [n_pad, K] weight, or NULL */
+  int32_t n_pad;       /* rows of Wdi (>= r + HC); ignored without Wdi */
+  int32_t fold_w;      /* 1: the projection weight carries (1 + Wnorm) */
+  const void* Wu;
+  void* R2;
+  float* rrms;
+  float* inj_next;
+  void* x;
+  float* lora;         /* may be NULL: lora is then kept in the workspace */
+  int32_t force_path;  /* hc_gr_path */
+  int32_t debug_fault; /* tests only: 1 = one CTA of the decode kernel leaves
+                          before the first grid barrier, so the others' bounded
+                          wait expires and hc_gr_check reports TIMEOUT */
+} hc_gr_args;
+
+/* Creates a handle bound to `device` and allocates its workspace for calls
+ * with M <= max_M, HC * HS <= the given HC * HS and r + HC <= the given
+ * r + HC.  Queries the device (SM count, shared memory) once.
+ * Returns INVALID_ARG for out == NULL or non-positive sizes, UNSUPPORTED for
+ * a device that is not sm_103, CUDA when allocation fails (*out is then
+ * NULL). */
+int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, int r);
+
+/* The whole forward pass for one batch of M tokens with separate, unfolded
+ * Wd and Wi (see the layouts above).  lora may be NULL.  Asynchronous on
+ * `stream`. */
+int hc_gr_forward(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps,
+                  const void* R, const void* y, const float* inj, const void* Wnorm,
+                  const void* Wd, const void* Wi, const void* Wu,
+                  void* R2, float* rrms, float* inj_next, void* x, float* lora,
+                  struct CUstream_st* stream);
+
+/* Same operation with every option: a merged (optionally folded) weight, a
+ * strided inj and a forced path. */
+int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* stream);
+
+/* Waits for `stream`, then returns the device status recorded by the
+ * handle's kernels since the last check (HC_GR_OK or HC_GR_ERR_TIMEOUT) and
+ * clears it, resetting the grid-barrier words so the handle is usable again.
+ * Returns HC_GR_ERR_CUDA if the stream reports a CUDA error. */
+int hc_gr_check(hc_gr_handle h, struct CUstream_st* stream);
+
+/* Releases the workspace.  Waits for the device first.  NULL is a no-op. */
+int hc_gr_destroy(hc_gr_handle h);
+
+/* Static text for a status code. */
+const char* hc_gr_strerror(int status);
+
+/* Text of the last CUDA error seen by this handle (static storage). */
+const char* hc_gr_last_cuda_error(hc_gr_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HC_GR_H_ */
