@@ -313,8 +313,38 @@ def run_ours(args, rank, world):
     return line
 
 
+def run_case(args):
+    """A few plain forward calls of one shape (for ncu captures)."""
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import HcGatedResidual, inputs
+
+    shape = inputs.WIDE if args.wide else inputs.DEFAULT
+    M = args.M
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = {k: bf(v) for k, v in inputs.weights(shape).items()}
+    a = inputs.activations(M, shape, distinct_rows=4096)
+    R, y, inj = bf(a["R"]), bf(a["y"]), torch.from_numpy(a["inj"]).cuda()
+    op = HcGatedResidual(max_M=M, HC=shape.HC, HS=shape.HS, r=shape.r)
+    path = {"auto": 0, "decode": 1, "prefill": 2}[args.case]
+    for _ in range(args.calls):
+        op.forward(R, y, inj, w["Wnorm"], w["Wu"], Wd=w["Wd"], Wi=w["Wi"], force_path=path)
+    op.check()
+    torch.cuda.synchronize()
+    print(f"case ok: {args.case} M={M} calls={args.calls}")
+
+
 def main():
     ap = argparse.ArgumentParser()
+    ap.add_argument("--case", choices=["auto", "decode", "prefill"], default=None,
+                    help="only run --calls forward calls of one shape (for profiling)")
+    ap.add_argument("--M", type=int, default=32)
+    ap.add_argument("--calls", type=int, default=3)
+    ap.add_argument("--wide", action="store_true")
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
@@ -323,6 +353,9 @@ def main():
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
+    if args.case is not None:
+        run_case(args)
+        return
 
     if args.impl == "reference":
         # The reference arm is the fp64 CPU oracle on the host cores; rank 0 only.

@@ -132,6 +132,7 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   h->ws.sumsq = reinterpret_cast<float*>(b + off_sumsq);
   h->ws.lora = reinterpret_cast<float*>(b + off_lora);
   h->ws.k1_part = reinterpret_cast<float*>(b + off_pre);
+  h->ws.prefill_bytes = hcgr::prefill_ws_bytes(max_M, HC, HS, r);
   *out = h;
   return HC_GR_OK;
 }
