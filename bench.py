@@ -338,6 +338,99 @@ def run_case(args):
     print(f"case ok: {args.case} M={M} calls={args.calls}")
 
 
+PREFILL_MS = (512, 1024, 2048, 4096, 8192, 16384, 32768, 65536)
+
+
+def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
+    """Per-M latency of the prefill path (graph replay, L2 defeated).
+
+    Token rows repeat the generator's first 4096 rows.  Small M rotate over
+    enough weight+activation copies to exceed twice the L2; from M=4096 on a
+    single call's inputs already exceed the L2.  Mid-batch M also run the
+    merged 336-row weight, unfolded and with (1 + Wnorm) folded in (the fold
+    is input preparation, done once here with torch on the device).
+    """
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import HcGatedResidual, inputs
+
+    dev = torch.cuda.current_device()
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = {k: bf(v) for k, v in inputs.weights().items()}
+    base_rows = 4096
+    a = inputs.activations(base_rows)
+    R0, y0, inj0 = bf(a["R"]), bf(a["y"]), torch.from_numpy(a["inj"]).cuda()
+    Wdi = torch.zeros((336, K_DIM), dtype=torch.bfloat16, device="cuda")
+    Wdi[:R_LOW] = w["Wd"]
+    Wdi[R_LOW:R_LOW + HC] = w["Wi"]
+    Wdi_f = (Wdi.float() * (1.0 + w["Wnorm"].float())[None, :]).to(torch.bfloat16)
+    hbm, _, _ = peaks()
+    res = {}
+    stream = torch.cuda.Stream()
+    for M in Ms:
+        per_set = WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN
+        nsets = 1 if M >= 4096 else int(min(8, max(1, np.ceil(2.0 * l2 / per_set))))
+        reps_rows = (M + base_rows - 1) // base_rows
+        R = R0.repeat(reps_rows, 1, 1)[:M].contiguous()
+        y = y0.repeat(reps_rows, 1)[:M].contiguous()
+        inj = inj0.repeat(reps_rows, 1)[:M].contiguous()
+        variants = [("unfolded", None, False)]
+        if M <= 2048:
+            variants += [("merged336", Wdi, False), ("merged336_folded", Wdi_f, True)]
+        op = HcGatedResidual(max_M=M)
+        for name, Wm, fold in variants:
+            sets = [(R, y, inj, w) if j == 0 else
+                    (R.clone(), y.clone(), inj.clone(), {k: v.clone() for k, v in w.items()})
+                    for j in range(nsets)]
+            mats = [Wm if (Wm is None or j == 0) else Wm.clone() for j in range(nsets)]
+            outs = [{"R2": torch.empty_like(R), "rrms": torch.empty((M, HC), device="cuda"),
+                     "inj_next": torch.empty((M, HC), device="cuda"),
+                     "x": torch.empty((M, HS), dtype=torch.bfloat16, device="cuda"),
+                     "lora": torch.empty((M, R_LOW), device="cuda")} for _ in range(nsets)]
+
+            def call(j):
+                Rj, yj, ij, wj = sets[j]
+                kw = dict(Wdi=mats[j], fold_w=fold) if mats[j] is not None else dict(Wd=wj["Wd"], Wi=wj["Wi"])
+                op.forward(Rj, yj, ij, wj["Wnorm"], wj["Wu"], out=outs[j], **kw)
+
+            for j in range(nsets):
+                call(j)
+            op.check()
+            g = torch.cuda.CUDAGraph()
+            calls = max(nsets, 2)
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(calls):
+                    call(j % nsets)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    g.replay()
+                samples = []
+                for _ in range(reps):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    samples.append(e0.elapsed_time(e1) * 1e3 / calls)
+            us = statistics.median(samples)
+            roof_us = per_set / hbm / 1e3
+            res.setdefault(str(M), {})[name] = {
+                "us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us,
+                "roofline_frac": roof_us / us, "spread": (max(samples) - min(samples)) / us,
+                "l2": f"{nsets} rotating sets" if nsets > 1 else "inputs > L2"}
+            del sets, outs
+        op.close()
+        del R, y, inj
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["auto", "decode", "prefill"], default=None,
@@ -350,6 +443,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-prefill-sweep", action="store_true",
+                    help="skip the per-M table of the prefill path")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -378,6 +473,8 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl")
     line = run_ours(args, rank, world)
+    if rank == 0 and not args.no_prefill_sweep:
+        line["prefill_sweep_us"] = prefill_sweep()
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline()
         print(json.dumps(line))

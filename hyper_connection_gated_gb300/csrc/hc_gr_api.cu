@@ -104,12 +104,13 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   // one allocation: [bar/err | part | sumsq | lora | prefill]
   const size_t part_f = hcgr::decode_ws_part_floats(h->dev, h->K_max, h->n_out_max);
   const size_t sumsq_f = static_cast<size_t>(h->dev.sms) * hcgr::DECODE_MAX_M;
-  const size_t lora_f = static_cast<size_t>(max_M) * r;
+  const size_t lora_f = static_cast<size_t>(max_M) * (r + HC);
   size_t off = 0;
-  const size_t off_ctl = off;    off += 256;
+  const size_t off_ctl = off;    off += hcgr::CTL_BYTES;
   const size_t off_part = off;   off = align_up(off + part_f * 4, 256);
   const size_t off_sumsq = off;  off = align_up(off + sumsq_f * 4, 256);
   const size_t off_lora = off;   off = align_up(off + lora_f * 4, 256);
+  const size_t off_hdec = off;   off = align_up(off + static_cast<size_t>(hcgr::DECODE_MAX_M) * (r + HC) * 2, 256);
   const size_t off_pre = off;    off = align_up(off + hcgr::prefill_ws_bytes(max_M, HC, HS, r), 256);
   void* base = nullptr;
   e = cudaMalloc(&base, off);
@@ -117,7 +118,7 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
     delete h;
     return HC_GR_ERR_CUDA;
   }
-  e = cudaMemset(base, 0, 256);
+  e = cudaMemset(base, 0, hcgr::CTL_BYTES);
   if (e != cudaSuccess) {
     cudaFree(base);
     delete h;
@@ -126,11 +127,12 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   unsigned char* b = static_cast<unsigned char*>(base);
   h->ws.base = base;
   h->ws.bytes = off;
-  h->ws.bar = reinterpret_cast<unsigned*>(b + off_ctl);
-  h->ws.err = reinterpret_cast<int*>(b + off_ctl + 64);
+  h->ws.bar = reinterpret_cast<unsigned long long*>(b + off_ctl);
+  h->ws.err = reinterpret_cast<int*>(b + off_ctl + hcgr::MAX_GRID * 8);
   h->ws.part = reinterpret_cast<float*>(b + off_part);
   h->ws.sumsq = reinterpret_cast<float*>(b + off_sumsq);
   h->ws.lora = reinterpret_cast<float*>(b + off_lora);
+  h->ws.hdec = reinterpret_cast<hcgr::bf16_t*>(b + off_hdec);
   h->ws.k1_part = reinterpret_cast<float*>(b + off_pre);
   h->ws.prefill_bytes = hcgr::prefill_ws_bytes(max_M, HC, HS, r);
   *out = h;
@@ -164,11 +166,11 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
       !a->inj_next || !a->x)
     return HC_GR_ERR_INVALID_ARG;
   if (!merged && (!a->Wd || !a->Wi)) return HC_GR_ERR_INVALID_ARG;
-  const void* p16[] = {a->R, a->y, a->Wnorm, a->Wu, a->R2, a->x,
+  const void* p16[] = {a->R, a->y, a->Wnorm, a->Wu, a->R2, a->x, a->lora,
                        merged ? a->Wdi : a->Wd, merged ? a->Wdi : a->Wi};
   for (const void* p : p16)
     if (!aligned(p, 16)) return HC_GR_ERR_INVALID_ARG;
-  const void* p4[] = {a->inj, a->rrms, a->inj_next, a->lora};
+  const void* p4[] = {a->inj, a->rrms, a->inj_next};
   for (const void* p : p4)
     if (!aligned(p, 4)) return HC_GR_ERR_INVALID_ARG;
   if (HS % 8 != 0 || r % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
@@ -226,10 +228,18 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   DeviceGuard guard(h->dev.id);
-  int path = a->force_path;
-  if (path == HC_GR_PATH_AUTO) path = M <= hcgr::DECODE_MAX_M ? HC_GR_PATH_DECODE : HC_GR_PATH_PREFILL;
-  cudaError_t e = path == HC_GR_PATH_DECODE ? hcgr::launch_decode(c, h->ws, h->dev, s)
-                                            : hcgr::launch_prefill(c, h->ws, h->dev, s);
+  // M-based dispatch: the weight-streaming decode kernel for M <= 32, the
+  // tensor-core prefill kernels otherwise (and for shapes the decode
+  // kernel's shared-memory plan cannot hold).
+  cudaError_t e;
+  if (a->force_path == HC_GR_PATH_DECODE) {
+    e = hcgr::launch_decode(c, h->ws, h->dev, s);
+  } else if (a->force_path == HC_GR_PATH_PREFILL || M > hcgr::DECODE_MAX_M) {
+    e = hcgr::launch_prefill(c, h->ws, h->dev, s);
+  } else {
+    e = hcgr::launch_decode(c, h->ws, h->dev, s);
+    if (e == cudaErrorNotSupported) e = hcgr::launch_prefill(c, h->ws, h->dev, s);
+  }
   if (e == cudaErrorNotSupported) return HC_GR_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return cuda_fail(h, e);
   return HC_GR_OK;
@@ -271,8 +281,8 @@ int hc_gr_check(hc_gr_handle h, struct CUstream_st* stream) {
   e = cudaMemcpy(&dev_status, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (dev_status == hcgr::DEV_OK) return HC_GR_OK;
-  // clear the status and the barrier words so the handle can be used again
-  e = cudaMemset(h->ws.base, 0, 256);
+  // clear the status and the barrier counters so the handle can be used again
+  e = cudaMemset(h->ws.base, 0, hcgr::CTL_BYTES);
   if (e != cudaSuccess) return cuda_fail(h, e);
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(h, e);

@@ -20,7 +20,8 @@ struct Workspace {
   float* part = nullptr;      // decode: per-CTA split-K partial products
   float* sumsq = nullptr;     // decode: per-CTA partial sums of R2^2
   float* lora = nullptr;      // lora when the caller passes lora == NULL
-  unsigned* bar = nullptr;    // grid barrier: [0] arrivals, [1] generation
+  bf16_t* hdec = nullptr;     // decode: h = bf16(SiLU(lora / HC)) [DECODE_MAX_M][r_max]
+  unsigned long long* bar = nullptr;  // grid-barrier counters, one per grid size
   int* err = nullptr;         // device status word
   void* base = nullptr;       // single allocation holding everything above
   size_t bytes = 0;
@@ -60,6 +61,8 @@ struct Device {
 
 // Decode path (M <= DECODE_MAX_M): one cooperative persistent kernel.
 constexpr int DECODE_MAX_M = 32;
+constexpr int MAX_GRID = 256;            // grid-barrier counters in the workspace
+constexpr int CTL_BYTES = MAX_GRID * 8 + 256;   // counters, then the status word
 size_t decode_ws_part_floats(const Device& dev, int HC_times_HS_max, int n_out_max);
 cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
                           cudaStream_t stream);
@@ -76,12 +79,11 @@ __device__ __forceinline__ float bf16_to_f32(bf16_t v) {
   return __uint_as_float(static_cast<uint32_t>(v) << 16);
 }
 
-// Round-to-nearest-even float -> bf16 (NaN kept quiet).
+// Round-to-nearest-even float -> bf16 (the cvt.rn conversion instructions).
 __device__ __forceinline__ bf16_t f32_to_bf16(float f) {
-  uint32_t u = __float_as_uint(f);
-  if ((u & 0x7fffffffu) > 0x7f800000u) return static_cast<bf16_t>((u >> 16) | 0x40u);
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return static_cast<bf16_t>(u >> 16);
+  unsigned short r;
+  asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(f));
+  return r;
 }
 
 __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
@@ -93,9 +95,14 @@ __device__ __forceinline__ void unpack8(const uint4 v, float* f) {
   }
 }
 
+// Two floats -> packed bf16x2 (a in the low half), round-to-nearest-even.
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-  return static_cast<uint32_t>(f32_to_bf16(a)) | (static_cast<uint32_t>(f32_to_bf16(b)) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
 }
+__device__ __forceinline__ float lo_bf16(uint32_t p) { return __uint_as_float(p << 16); }
+__device__ __forceinline__ float hi_bf16(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
@@ -130,16 +137,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// Time limits of the bounded waits are counted in SM clock cycles (clock64,
+// cheap to read); limit_ns is converted at 2 cycles per ns, the upper end of
+// the SM clock range, so a limit never expires early.
+__device__ __forceinline__ long long wait_limit_cycles(uint64_t limit_ns) {
+  return static_cast<long long>(limit_ns) * 2;
+}
+
 // Bounded wait on an mbarrier phase.  On expiry it records DEV_TIMEOUT in the
 // status word and returns false; the caller then skips the dependent work.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity, int* err,
                                                   uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
+  const long long t0 = clock64();
   for (uint32_t it = 1;; ++it) {
     if (mbar_try_wait(bar, parity)) return true;
     if ((it & 15u) == 0) {
-      if (globaltimer_ns() - t0 > limit_ns) {
+      if (clock64() - t0 > wait_limit_cycles(limit_ns)) {
         atomicCAS(err, DEV_OK, DEV_TIMEOUT);
         return false;
       }
@@ -219,6 +233,13 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* v) {
         "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
 }
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* v) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7])
+      : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -261,43 +282,96 @@ __device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
-// Grid-wide barrier for a cooperative launch.  bar[0] counts arrivals and is
-// reset by the last arriver, which then bumps the generation bar[1]; waiters
-// spin on the generation with a time limit.  Every call starts from
-// bar[0] == 0, so calls with different grid sizes or shapes cannot alias a
-// phase.  Returns false (all threads of the CTA) when the wait expired or
-// another CTA reported an error; the CTA must then leave.
-__device__ __forceinline__ bool grid_barrier(unsigned* bar, unsigned nblocks, int* err,
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
+  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ unsigned atom_add_acq_rel_u32(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p,
+                                                                  unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
+               : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void prefetch_tmap(const void* tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_gpu() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
+// Grid-wide barrier for a cooperative launch of `nblocks` CTAs.  `cnt` is a
+// 64-bit counter used only by grids of exactly this size, so it is a multiple
+// of nblocks whenever a barrier begins: an arriving CTA adds 1 (release, so
+// everything the CTA wrote before the CTA barrier is published), derives the
+// barrier's target from the value it saw, polls with relaxed loads and ends
+// with one acquire fence.  Returns false (all threads of the CTA) when the
+// wait expired or another CTA reported an error; the CTA must then leave.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* cnt, unsigned nblocks, int* err,
                                              uint64_t limit_ns, int* s_flag) {
   __syncthreads();
   if (threadIdx.x == 0) {
     int ok = 1;
-    const unsigned gen = ld_acquire_u32(bar + 1);
-    __threadfence();
-    const unsigned prev = atomicAdd(bar, 1u);
-    if (prev == nblocks - 1) {
-      atomicExch(bar, 0u);
-      __threadfence();
-      st_release_u32(bar + 1, gen + 1);
-    } else {
-      const uint64_t t0 = globaltimer_ns();
-      uint32_t it = 0;
-      while (ld_acquire_u32(bar + 1) == gen) {
-        if ((++it & 31u) == 0) {
-          if (*((volatile int*)err) != DEV_OK) { ok = 0; break; }
-          if (globaltimer_ns() - t0 > limit_ns) {
-            atomicCAS(err, DEV_OK, DEV_TIMEOUT);
-            ok = 0;
-            break;
-          }
+    const unsigned long long old = atom_add_release_u64(cnt, 1ull);
+    const unsigned long long target = (old / nblocks + 1) * nblocks;
+    const long long t0 = clock64();
+    uint32_t it = 0;
+    while (ld_relaxed_u64(cnt) < target) {
+      if ((++it & 31u) == 0) {
+        if (*((volatile int*)err) != DEV_OK) { ok = 0; break; }
+        if (clock64() - t0 > wait_limit_cycles(limit_ns)) {
+          atomicCAS(err, DEV_OK, DEV_TIMEOUT);
+          ok = 0;
+          break;
         }
       }
     }
-    __threadfence();
+    fence_acq_rel_gpu();
     *s_flag = ok;
   }
   __syncthreads();
   return *s_flag != 0;
+}
+
+// Warp-level bf16 MMA (D += A * B, fp32 accumulate).  Fragment layouts (g =
+// lane / 4, t = lane % 4): A rows g and g+8, column pairs 2t and 2t+8; B
+// column g, row pairs 2t and 2t+8; D rows g, g+8 and columns 2t, 2t+1.
+__device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
+                                          uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+      " {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_1688(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6},"
+      " {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Orders this thread's earlier generic-proxy accesses (and those it has
+// acquired) before its later async-proxy (TMA / bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

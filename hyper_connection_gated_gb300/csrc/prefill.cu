@@ -171,60 +171,50 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       mbar_wait_bounded(accb, 0, p.err, p.limit_ns);
     }
   } else {
-    // ---------------- converters: warps 0-7, 4 row passes of 32 rows each
-    const int ch = lane & 7;
-    const int rbase = warp * 4 + (lane >> 3);
-    float iw[4], ss[4], ij[4][8];
-    bool valid[4];
+    // ---------------- converters: warps 0-7.  Thread t owns row t / 2 of the
+    // tile and channel chunks 4 * (t & 1) .. +3 (8 channels each) of every
+    // K block, so its row's partial sums stay in registers.  In the 128-byte
+    // swizzled tile chunk c of row i sits at i * 128 + ((c ^ (i & 7)) << 4);
+    // any 8 consecutive threads touch 8 distinct chunk positions, so the
+    // shared-memory accesses are free of bank conflicts.
+    const int row = tid >> 1, cbase = (tid & 1) * 4;
+    const int m = m0 + row;
+    const bool valid = m < p.M;
+    const float iw =
+        valid ? 2.0f * sigmoidf_dev(p.inj[m * p.ld_inj + s] / static_cast<float>(HC)) : 0.f;
+    float ss = 0.f, ij[8];
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-      const int m = m0 + rbase + 32 * pp;
-      valid[pp] = m < p.M;
-      iw[pp] = valid[pp] ? 2.0f * sigmoidf_dev(p.inj[m * p.ld_inj + s] / static_cast<float>(HC)) : 0.f;
-      ss[pp] = 0.f;
-#pragma unroll
-      for (int j = 0; j < 8; ++j) ij[pp][j] = 0.f;
-    }
+    for (int j = 0; j < 8; ++j) ij[j] = 0.f;
+    bf16_t* r2row = p.R2 + static_cast<int64_t>(valid ? m : 0) * p.K + static_cast<int64_t>(s) * HS;
     bool ok = true;
     for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % K1_NST;
       ok = mbar_wait_bounded(full(st), (kb / K1_NST) & 1, p.err, p.limit_ns);
       if (!ok) break;
       unsigned char* sb = smem + st * p.stage_bytes;
-      const int col = kb * BK + ch * 8;           // channel within the stream
-      const int64_t k = static_cast<int64_t>(s) * HS + col;
-      float wn[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(p.Wnorm + k)), wn);
-      float wi[8][8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < HC) unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wi + j * 128 + ch * 16), wi[j]);
-#pragma unroll
-      for (int pp = 0; pp < 4; ++pp) {
-        const int row = rbase + 32 * pp;
+      for (int i = 0; i < 4; ++i) {
+        const int ch = cbase + i;
+        const int col = kb * BK + ch * 8;           // channel within the stream
         const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-        float rv[8], yv[8], a[8];
+        float rv[8], yv[8], wn[8], a[8];
         unpack8(*reinterpret_cast<const uint4*>(sb + off), rv);
         unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(p.Wnorm + static_cast<int64_t>(s) * HS + col)), wn);
         uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float r2 = bf16_to_f32(f32_to_bf16(fmaf(yv[e], iw[pp], rv[e])));
-          ss[pp] = fmaf(r2, r2, ss[pp]);
-          a[e] = p.fold ? r2 : r2 * (1.0f + wn[e]);
-          rv[e] = r2;
-        }
-#pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pr[e] = pack2(rv[2 * e], rv[2 * e + 1]);
-          const float h0 = bf16_to_f32(f32_to_bf16(a[2 * e]));
-          const float h1 = bf16_to_f32(f32_to_bf16(a[2 * e + 1]));
-          ph[e] = pack2(h0, h1);
-          pl[e] = pack2(a[2 * e] - h0, a[2 * e + 1] - h1);
+          pr[e] = pack2(fmaf(yv[2 * e], iw, rv[2 * e]), fmaf(yv[2 * e + 1], iw, rv[2 * e + 1]));
+          const float r0 = lo_bf16(pr[e]), r1 = hi_bf16(pr[e]);
+          ss = fmaf(r0, r0, ss);
+          ss = fmaf(r1, r1, ss);
+          a[2 * e] = p.fold ? r0 : r0 * (1.0f + wn[2 * e]);
+          a[2 * e + 1] = p.fold ? r1 : r1 * (1.0f + wn[2 * e + 1]);
+          ph[e] = pack2(a[2 * e], a[2 * e + 1]);
+          pl[e] = pack2(a[2 * e] - lo_bf16(ph[e]), a[2 * e + 1] - hi_bf16(ph[e]));
         }
-        if (valid[pp])
-          *reinterpret_cast<uint4*>(p.R2 + static_cast<int64_t>(m0 + row) * p.K + k) =
-              make_uint4(pr[0], pr[1], pr[2], pr[3]);
+        if (valid)
+          *reinterpret_cast<uint4*>(r2row + col) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
         if (p.fold) {
           *reinterpret_cast<uint4*>(sb + off) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
         } else {
@@ -234,10 +224,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
           if (j < HC) {
-            float t = ij[pp][j];
+            float wi[8];
+            unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wi + j * 128 + ch * 16), wi);
+            float t = ij[j];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t = fmaf(a[e], wi[j][e], t);
-            ij[pp][j] = t;
+            for (int e = 0; e < 8; ++e) t = fmaf(a[e], wi[e], t);
+            ij[j] = t;
           }
         }
       }
@@ -245,38 +237,33 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(conv(st));
     }
-    // per-row totals: the 8 lanes sharing a row hold the 8 channel chunks
+    // per-row totals: the two threads of a row are lanes 2i and 2i+1
+    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
+    for (int j = 0; j < 8; ++j) ij[j] += __shfl_xor_sync(0xffffffffu, ij[j], 1);
+    if ((tid & 1) == 0) {
+      rowss[row] = ss;
 #pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        ss[pp] += __shfl_xor_sync(0xffffffffu, ss[pp], o);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) ij[pp][j] += __shfl_xor_sync(0xffffffffu, ij[pp][j], o);
-      }
-      if (ch == 0) {
-        const int row = rbase + 32 * pp;
-        rowss[row] = ss[pp];
-        for (int j = 0; j < HC; ++j) rowinj[row * HC + j] = ij[pp][j];
-      }
+      for (int j = 0; j < 8; ++j)
+        if (j < HC) rowinj[row * HC + j] = ij[j];
     }
     named_bar_sync(1, K1_CONV_WARPS * 32);
     // ---------------- epilogue: rrms_s, inj partial, lora partial
     if (ok) ok = mbar_wait_bounded(accb, 0, p.err, p.limit_ns);
     tc_fence_after();
     const int q = warp & 3, half = warp >> 2;
-    const int row = 32 * q + lane;
-    const int m = m0 + row;
-    const bool v = m < p.M;
-    const float rr = 1.0f / sqrtf(rowss[row] / static_cast<float>(HS) + p.eps);
+    const int erow = 32 * q + lane;
+    const int em = m0 + erow;
+    const bool v = em < p.M;
+    const float rr = 1.0f / sqrtf(rowss[erow] / static_cast<float>(HS) + p.eps);
     if (v && half == 0) {
-      p.rrms[static_cast<int64_t>(m) * HC + s] = rr;
+      p.rrms[static_cast<int64_t>(em) * HC + s] = rr;
       for (int j = 0; j < HC; ++j)
-        p.inj_part[(static_cast<int64_t>(s) * p.M + m) * HC + j] = rr * rowinj[row * HC + j];
+        p.inj_part[(static_cast<int64_t>(s) * p.M + em) * HC + j] = rr * rowinj[erow * HC + j];
     }
     if (ok) {
       const int cols = r / 2;
-      float* dst = p.part + (static_cast<int64_t>(s) * p.M + m) * r + half * cols;
+      float* dst = p.part + (static_cast<int64_t>(s) * p.M + (v ? em : 0)) * r + half * cols;
       for (int c0 = 0; c0 < cols; c0 += 16) {
         uint32_t acc[16];
         tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + half * cols + c0, acc);
@@ -345,19 +332,23 @@ struct K2Params {
   bf16_t* x;
   int M, HC, HS, K, r;
   int nkb, ncb, n_units, nst, nacc, ncols_acc;
-  uint32_t stage_bytes, tmem_cols;
+  uint32_t stage_bytes, tmem_cols, wn_bytes;
   int* err;
   uint64_t limit_ns;
 };
 
+template <int HCT>
 __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant__ K2Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int HC = p.HC, HS = p.HS, nkb = p.nkb, nst = p.nst, nacc = p.nacc;
+  constexpr int HC = HCT;
+  const int HS = p.HS, nkb = p.nkb, nst = p.nst, nacc = p.nacc;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + nst * p.stage_bytes;
+  const uint32_t wnbar = bar + 160u;
+  const bf16_t* s_wn = reinterpret_cast<const bf16_t*>(smem + nst * p.stage_bytes + 256);
   auto full = [&](int st) { return bar + 8u * st; };
   auto freeb = [&](int st) { return bar + 64u + 8u * st; };
   auto accfull = [&](int a) { return bar + 128u + 8u * a; };
@@ -373,6 +364,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
       mbar_init(accfull(a), 1);
       mbar_init(accfree(a), K2_EPI_WARPS);
     }
+    mbar_init(wnbar, 1);
     fence_mbar_init();
   }
   if (warp == K2_ALLOC_WARP) {
@@ -388,6 +380,9 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
 
   if (warp == K2_TMA_WARP) {
     if (lane == 0) {
+      // Wnorm, staged once for the epilogue
+      mbar_arrive_expect_tx(wnbar, p.wn_bytes);
+      bulk_g2s(smem_u32(s_wn), p.Wnorm, p.wn_bytes, wnbar);
       int g = 0;
       bool ok = true;
       int last_g[8];
@@ -410,6 +405,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
       }
       for (int st = 0; st < nst; ++st)
         if (last_g[st] >= 0) mbar_wait_bounded(full(st), (last_g[st] / nst) & 1, p.err, p.limit_ns);
+      mbar_wait_bounded(wnbar, 0, p.err, p.limit_ns);
     }
   } else if (warp == K2_MMA_WARP) {
     if (lane == 0) {
@@ -451,57 +447,75 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
       }
     }
   } else if (warp >= K2_EPI_WARP0) {
+    // Epilogue: thread = one token row (TMEM lane), 32 channels of the unit
+    // (warps 4-7 the first half, 8-11 the second).  Channels go in chunks of
+    // CC; the R2 values of chunk q+1 are loaded while chunk q is computed, and
+    // those of chunk 0 (and rrms) before waiting for the accumulator.
+    constexpr int CC = HC <= 4 ? 16 : 8;
+    constexpr int NCH = 32 / CC;
+    constexpr int V = CC / 8;
     const int ew = warp - K2_EPI_WARP0;
-    const int q = warp & 3, half = ew >> 2;
+    const int q4 = warp & 3, half = ew >> 2;
     const float inv_hc = 1.0f / static_cast<float>(HC);
-    for (int i = 0; i < n_local; ++i) {
+    bool wn_ready = mbar_wait_bounded(wnbar, 0, p.err, p.limit_ns);
+    for (int i = 0; i < n_local && wn_ready; ++i) {
       const int u = blockIdx.x + i * gridDim.x;
       const int t = u / p.ncb, cb = u % p.ncb;
       const int ab = i % nacc;
-      if (!mbar_wait_bounded(accfull(ab), (i / nacc) & 1, p.err, p.limit_ns)) break;
-      tc_fence_after();
-      const int row = 32 * q + lane;
+      const int row = 32 * q4 + lane;
       const int64_t m = static_cast<int64_t>(t) * BM + row;
       const bool v = m < p.M;
-      float rr[8];
+      const int cbase = cb * NC + half * 32;          // first channel of this thread
+      const bf16_t* r2p = p.R2 + (v ? m : 0) * p.K + cbase;
+      float rr[HC];
+      uint4 bufA[HC][V], bufB[HC][V];
 #pragma unroll
-      for (int ss = 0; ss < 8; ++ss) rr[ss] = (v && ss < HC) ? __ldg(p.rrms + m * HC + ss) : 0.f;
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16) + ab * p.ncols_acc;
-#pragma unroll 1
-      for (int c16 = 0; c16 < 2; ++c16) {
-        const int cl = half * 32 + c16 * 16;          // channel within the unit
-        const int c = cb * NC + cl;                   // channel within the stream
-        float acc[16];
+      for (int ss = 0; ss < HC; ++ss) rr[ss] = v ? __ldg(p.rrms + m * HC + ss) : 0.f;
+      auto load = [&](int q, uint4 (&buf)[HC][V]) {
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        for (int ss = 0; ss < HC; ++ss)
+#pragma unroll
+          for (int j = 0; j < V; ++j)
+            buf[ss][j] = v ? __ldg(reinterpret_cast<const uint4*>(r2p + ss * HS + q * CC + j * 8))
+                           : make_uint4(0, 0, 0, 0);
+      };
+      load(0, bufA);
+      if (!mbar_wait_bounded(accfull(ab), (i / nacc) & 1, p.err, p.limit_ns)) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q4) << 16) + ab * p.ncols_acc;
+#pragma unroll
+      for (int q = 0; q < NCH; ++q) {
+        uint4 (&cur)[HC][V] = (q & 1) ? bufB : bufA;
+        uint4 (&nxt)[HC][V] = (q & 1) ? bufA : bufB;
+        if (q + 1 < NCH) load(q + 1, nxt);
+        float acc[CC];
+#pragma unroll
+        for (int e = 0; e < CC; ++e) acc[e] = 0.f;
+#pragma unroll
         for (int ss = 0; ss < HC; ++ss) {
-          uint32_t gv[16];
-          tmem_ld16(tbase + ss * NC + cl, gv);
+          uint32_t gv[CC];
+          if constexpr (CC == 16) tmem_ld16(tbase + ss * NC + half * 32 + q * CC, gv);
+          else tmem_ld8(tbase + ss * NC + half * 32 + q * CC, gv);
           tmem_ld_wait();
-          if (v) {
-            const int64_t k = static_cast<int64_t>(ss) * HS + c;
-            float r2[16], wn[16];
-            const uint4* rp = reinterpret_cast<const uint4*>(p.R2 + m * p.K + k);
-            const uint4* wp = reinterpret_cast<const uint4*>(p.Wnorm + k);
-            unpack8(__ldg(rp), r2);
-            unpack8(__ldg(rp + 1), r2 + 8);
-            unpack8(__ldg(wp), wn);
-            unpack8(__ldg(wp + 1), wn + 8);
+          float r2[CC], wn[CC];
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const float G = sigmoid_tanh(__uint_as_float(gv[e]));
-              const float xn = r2[e] * rr[ss] * (1.0f + wn[e]);
-              acc[e] = fmaf(G, xn, acc[e]);
-            }
+          for (int j = 0; j < V; ++j) {
+            unpack8(cur[ss][j], r2 + 8 * j);
+            unpack8(*reinterpret_cast<const uint4*>(s_wn + ss * HS + cbase + q * CC + j * 8), wn + 8 * j);
+          }
+#pragma unroll
+          for (int e = 0; e < CC; ++e) {
+            const float G = sigmoid_tanh(__uint_as_float(gv[e]));
+            acc[e] = fmaf(G, r2[e] * rr[ss] * (1.0f + wn[e]), acc[e]);
           }
         }
         if (v) {
-          uint32_t o[8];
+          uint32_t o[CC / 2];
 #pragma unroll
-          for (int e = 0; e < 8; ++e) o[e] = pack2(acc[2 * e] * inv_hc, acc[2 * e + 1] * inv_hc);
-          uint4* xp = reinterpret_cast<uint4*>(p.x + m * HS + c);
-          xp[0] = make_uint4(o[0], o[1], o[2], o[3]);
-          xp[1] = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int e = 0; e < CC / 2; ++e) o[e] = pack2(acc[2 * e] * inv_hc, acc[2 * e + 1] * inv_hc);
+          uint4* xp = reinterpret_cast<uint4*>(p.x + m * HS + cbase + q * CC);
+#pragma unroll
+          for (int j = 0; j < V; ++j) xp[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
         }
       }
       tc_fence_before();
@@ -521,6 +535,20 @@ uint32_t pow2_cols(int n) {
   uint32_t c = 32;
   while (c < static_cast<uint32_t>(n)) c <<= 1;
   return c;
+}
+
+template <int HCT>
+cudaError_t launch_k2(const K2Params& p, int grid, size_t smem, const Device& dev,
+                      cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k2_kernel<HCT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k2_kernel<HCT><<<grid, K2_THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 bool prefill_supported(const Call& c) {
@@ -551,7 +579,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
       reinterpret_cast<unsigned char*>(inj_part) + ((static_cast<size_t>(c.HC) * M * c.HC * 4 + 255) / 256) * 256);
 
   // ---------------- K1
-  static bool k1_attr = false, k2_attr = false;
+  static bool k1_attr = false;
   {
     K1Params p;
     const uint64_t dR[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(M)};
@@ -635,7 +663,8 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.ncb = c.HS / NC;
     p.n_units = n_mt * p.ncb;
     p.stage_bytes = TILE_BYTES + c.HC * NC * 128;
-    const int budget = dev.smem_optin - 1024 - 256;
+    p.wn_bytes = static_cast<uint32_t>(c.K) * 2;
+    const int budget = dev.smem_optin - 1024 - 256 - static_cast<int>(p.wn_bytes);
     p.nst = std::min(4, budget / static_cast<int>(p.stage_bytes));
     if (p.nst < 2) return cudaErrorNotSupported;
     p.ncols_acc = c.HC * NC;
@@ -643,16 +672,19 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.tmem_cols = pow2_cols(p.nacc * p.ncols_acc);
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
-    const size_t smem = static_cast<size_t>(p.nst) * p.stage_bytes + 256 + 1024;
-    if (!k2_attr) {
-      cudaError_t e = cudaFuncSetAttribute(k2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           dev.smem_optin);
-      if (e != cudaSuccess) return e;
-      k2_attr = true;
-    }
+    const size_t smem = static_cast<size_t>(p.nst) * p.stage_bytes + 256 + p.wn_bytes + 1024;
     const int grid = std::min(p.n_units, dev.sms);
-    k2_kernel<<<grid, K2_THREADS, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = cudaSuccess;
+    switch (c.HC) {
+      case 1: e = launch_k2<1>(p, grid, smem, dev, stream); break;
+      case 2: e = launch_k2<2>(p, grid, smem, dev, stream); break;
+      case 3: e = launch_k2<3>(p, grid, smem, dev, stream); break;
+      case 4: e = launch_k2<4>(p, grid, smem, dev, stream); break;
+      case 5: e = launch_k2<5>(p, grid, smem, dev, stream); break;
+      case 6: e = launch_k2<6>(p, grid, smem, dev, stream); break;
+      case 7: e = launch_k2<7>(p, grid, smem, dev, stream); break;
+      default: e = launch_k2<8>(p, grid, smem, dev, stream); break;
+    }
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -26,11 +26,11 @@ inline EncodeTiledFn encode_tiled_fn() {
   return fn;
 }
 
-// bf16 tensor of `rank` dims (dims[0] innermost, elements); strides[i] is
-// the byte stride of dim i+1.  Out-of-range box elements read as zero.
-inline bool make_tmap_bf16(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
-                           const uint64_t* strides, const uint32_t* box,
-                           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+// Tensor of `rank` dims (dims[0] innermost, elements); strides[i] is the
+// byte stride of dim i+1.  Out-of-range box elements read as zero.
+inline bool make_tmap(CUtensorMap* tm, CUtensorMapDataType dtype, const void* base, int rank,
+                      const uint64_t* dims, const uint64_t* strides, const uint32_t* box,
+                      CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
   EncodeTiledFn fn = encode_tiled_fn();
   if (!fn) return false;
   cuuint64_t d[5], s[4];
@@ -41,9 +41,15 @@ inline bool make_tmap_bf16(CUtensorMap* tm, const void* base, int rank, const ui
     e[i] = 1;
     if (i + 1 < rank) s[i] = strides[i];
   }
-  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), d, s, b, e,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  return fn(tm, dtype, rank, const_cast<void*>(base), d, s, b, e, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+inline bool make_tmap_bf16(CUtensorMap* tm, const void* base, int rank, const uint64_t* dims,
+                           const uint64_t* strides, const uint32_t* box,
+                           CUtensorMapSwizzle swz = CU_TENSOR_MAP_SWIZZLE_NONE) {
+  return make_tmap(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, rank, dims, strides, box, swz);
 }
 
 }  // namespace hcgr

@@ -32,9 +32,12 @@
  *              (1 + Wnorm[k]) (the "(1+w) folded in" weight of the page's
  *              Performance setup); Wnorm is then still read for the mix.
  * bf16 is passed as raw 16-bit storage (const void*).  Every pointer is a
- * device pointer, 16-byte aligned, owned by the caller; the library never
- * frees or retains it past the call.  HS must be a multiple of 8 and r a
- * multiple of 8.
+ * device pointer owned by the caller; the library never frees or retains it
+ * past the call.  bf16 tensors and lora are 16-byte aligned; inj, rrms and
+ * inj_next need only 4-byte alignment.  HS and r are multiples of 8.  The
+ * prefill kernels additionally need HS and r multiples of 64, r <= 512 and
+ * HC <= 8; other shapes run on the decode kernel (M <= 32) or are rejected
+ * with HC_GR_ERR_UNSUPPORTED.
  *
  * Streams and concurrency: hc_gr_forward* only enqueues work on `stream`
  * (a cudaStream_t; NULL is the legacy default stream) and returns.  A handle
