@@ -16,7 +16,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT = range(6
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = range(3)
 
 EXPORTS = ("hc_gr_create", "hc_gr_forward", "hc_gr_forward_ex", "hc_gr_check",
-           "hc_gr_destroy", "hc_gr_strerror", "hc_gr_last_cuda_error")
+           "hc_gr_destroy", "hc_gr_strerror", "hc_gr_last_cuda_error", "hc_gr_forward_noalloc")
 
 _vp = ctypes.c_void_p
 _fp = ctypes.c_void_p   # float* passed as an address
@@ -65,6 +65,9 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_gr_strerror.restype = ctypes.c_char_p
     lib.hc_gr_last_cuda_error.argtypes = [_vp]
     lib.hc_gr_last_cuda_error.restype = ctypes.c_char_p
+    lib.hc_gr_forward_noalloc.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          ctypes.c_float] + [_vp] * 12 + [_vp]
+    lib.hc_gr_forward_noalloc.restype = ctypes.c_int
     return lib
 
 

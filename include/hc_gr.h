@@ -143,6 +143,33 @@ const char* hc_gr_strerror(int status);
 /* Text of the last CUDA error seen by this handle (static storage). */
 const char* hc_gr_last_cuda_error(hc_gr_handle h);
 
+/* hc_gr_forward without a handle and without any device allocation.  The
+ * pages have no counterpart: this entry point exists for callers that may not
+ * call cudaMalloc on their call path, for instance an engine whose memory
+ * manager owns all device memory, or code that must not risk the implicit
+ * device synchronisation of an allocation.  It runs the decode kernel with
+ * its scratch memory (cross-CTA partial sums, h, lora when lora is NULL, the
+ * grid-barrier counters and the status word) in one fixed 2 MiB device array
+ * inside the library, which every GPU that loads the library holds until the
+ * process exits.
+ *   - Limits: M <= 8 tokens and r + HC <= 336; larger sizes return
+ *     HC_GR_ERR_UNSUPPORTED.  Other arguments, layouts and alignment as for
+ *     hc_gr_forward; the current device is used.
+ *   - The first call on a device queries the device and resolves the device
+ *     address of the scratch array; make that first call before any stream
+ *     capture.
+ *   - Every call shares the one array: calls that overlap on the GPU (on
+ *     different streams, or on several host threads) race and corrupt each
+ *     other.  Each call clears the barrier counters and the status word
+ *     first; a device-side timeout ends the kernel but is not reported here.
+ *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ *     routine.  Asynchronous on `stream`. */
+int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps,
+                          const void* R, const void* y, const float* inj, const void* Wnorm,
+                          const void* Wd, const void* Wi, const void* Wu,
+                          void* R2, float* rrms, float* inj_next, void* x, float* lora,
+                          struct CUstream_st* stream);
+
 #ifdef __cplusplus
 }
 #endif
