@@ -47,36 +47,41 @@ constexpr int K1_THREADS = (K1_CONV_WARPS + 2) * 32;
 constexpr int K1_TMA_WARP = K1_CONV_WARPS;
 constexpr int K1_MMA_WARP = K1_CONV_WARPS + 1;
 constexpr int K1_NST = 2;
+constexpr int WI_ROWS = 16;   // inject rows in the MMA's B tile (HC real, rest zero-filled)
 
 struct K1Params {
   CUtensorMap tm_R;    // [M][K], box {64, 128}, 128B swizzle
   CUtensorMap tm_y;    // [M][HS], box {64, 128}, 128B swizzle
   CUtensorMap tm_w;    // Wd [r][K], box {64, wbox_rows}, 128B swizzle
-  CUtensorMap tm_wi;   // Wi [HC][K], box {64, HC}
+  CUtensorMap tm_wi;   // Wi [HC][K], box {64, 16} (128B swizzle) or {64, HC} (plain)
   const float* inj;
   int64_t ld_inj;
-  const bf16_t* Wnorm;
   bf16_t* R2;
+  const bf16_t* Wnorm;
   float* rrms;
   float* part;        // [HC][M][r]
   float* inj_part;    // [HC][M][HC]
-  int M, HC, HS, K, r, fold;
+  int M, HS, K, r, fold;
   float eps;
-  int nkb, wbox_rows, nwbox, mma_n, n_mma;
+  int nkb, wbox_rows, nwbox, n1, n2;   // MMA column blocks: [0, n1) and [n1, n1 + n2)
   uint32_t stage_bytes, tmem_cols;
   int* err;
   uint64_t limit_ns;
 };
 
 struct K1Smem {
-  uint32_t off_b, off_wi, off_bar, off_rowss, off_rowinj, total;
+  uint32_t off_b, off_wi, off_wn, off_bar, off_rowss, off_rowinj, total;
 };
 
-__host__ __device__ inline K1Smem k1_smem(int r, int HC) {
+// Stage: R tile, y tile, B tile (r rows of Wd, then the inject rows), the K
+// block's 64 Wnorm values.
+__host__ __device__ inline K1Smem k1_smem(int r, int HC, bool inj_mma) {
   K1Smem s;
   s.off_b = 2 * TILE_BYTES;
   s.off_wi = s.off_b + r * 128;
-  const uint32_t stage = s.off_wi + ((HC * 128 + 1023) / 1024) * 1024;
+  const uint32_t wi_bytes = (inj_mma ? WI_ROWS : HC) * 128;
+  s.off_wn = s.off_wi + wi_bytes;
+  const uint32_t stage = ((s.off_wn + 128) + 1023) / 1024 * 1024;
   s.off_bar = K1_NST * stage;
   s.off_rowss = s.off_bar + 128;
   s.off_rowinj = s.off_rowss + BM * 4;
@@ -84,15 +89,17 @@ __host__ __device__ inline K1Smem k1_smem(int r, int HC) {
   return s;
 }
 
+template <int HCT, bool INJ_MMA>
 __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant__ K1Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const K1Smem L = k1_smem(p.r, p.HC);
+  constexpr int HC = HCT;
+  const K1Smem L = k1_smem(p.r, HC, INJ_MMA);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = blockIdx.x % p.HC;
-  const int m0 = (blockIdx.x / p.HC) * BM;
-  const int HC = p.HC, HS = p.HS, r = p.r, nkb = p.nkb;
+  const int s = blockIdx.x % HC;
+  const int m0 = (blockIdx.x / HC) * BM;
+  const int HS = p.HS, r = p.r, nkb = p.nkb;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + L.off_bar;
   auto full = [&](int st) { return bar + 8u * st; };
@@ -104,6 +111,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   float* rowinj = reinterpret_cast<float*>(smem + L.off_rowinj);
 
   if (tid == 0) {
+    prefetch_tmap(&p.tm_R);
+    prefetch_tmap(&p.tm_y);
+    prefetch_tmap(&p.tm_w);
+    prefetch_tmap(&p.tm_wi);
     for (int i = 0; i < K1_NST; ++i) {
       mbar_init(full(i), 1);
       mbar_init(conv(i), K1_CONV_WARPS);
@@ -125,19 +136,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     if (lane == 0) {
       int last_issued[K1_NST] = {-1, -1};
       bool ok = true;
+      const uint32_t wi_tx = (INJ_MMA ? WI_ROWS : HC) * 128;
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int st = kb % K1_NST;
         if (kb >= K1_NST)
           ok = mbar_wait_bounded(freeb(st), ((kb / K1_NST) - 1) & 1, p.err, p.limit_ns);
         if (!ok) break;
         const uint32_t sb = sbase + st * p.stage_bytes;
-        mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES + r * 128 + HC * 128);
+        mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES + r * 128 + wi_tx + 128);
         tma_load_2d(sb, &p.tm_R, s * HS + kb * BK, m0, full(st));
         tma_load_2d(sb + TILE_BYTES, &p.tm_y, kb * BK, m0, full(st));
         for (int bx = 0; bx < p.nwbox; ++bx)
           tma_load_2d(sb + L.off_b + bx * p.wbox_rows * 128, &p.tm_w, s * HS + kb * BK,
                       bx * p.wbox_rows, full(st));
         tma_load_2d(sb + L.off_wi, &p.tm_wi, s * HS + kb * BK, 0, full(st));
+        bulk_g2s(sb + L.off_wn, p.Wnorm + static_cast<int64_t>(s) * HS + kb * BK, 128, full(st));
         last_issued[st] = kb;
       }
       // outstanding copies land before the CTA can leave
@@ -147,7 +160,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     }
   } else if (warp == K1_MMA_WARP) {
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, p.mma_n);
+      const uint32_t id1 = idesc_bf16(BM, p.n1);
+      const uint32_t id2 = idesc_bf16(BM, p.n2 > 0 ? p.n2 : 16);
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
         const int st = kb % K1_NST;
@@ -159,10 +173,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
         for (int ks = 0; ks < BK / 16; ++ks) {
           const uint64_t a_hi = desc_sw128(sb + ks * 32);
           const uint64_t a_lo = desc_sw128(sb + TILE_BYTES + ks * 32);
-          for (int nn = 0; nn < p.n_mma; ++nn) {
-            const uint64_t bd = desc_sw128(sb + L.off_b + nn * p.mma_n * 128 + ks * 32);
-            umma_bf16(tmem + nn * p.mma_n, a_hi, bd, idesc, (kb | ks) != 0);
-            if (!p.fold) umma_bf16(tmem + nn * p.mma_n, a_lo, bd, idesc, 1);
+          const uint64_t b1 = desc_sw128(sb + L.off_b + ks * 32);
+          umma_bf16(tmem, a_hi, b1, id1, (kb | ks) != 0);
+          if (!p.fold) umma_bf16(tmem, a_lo, b1, id1, 1);
+          if (p.n2 > 0) {
+            const uint64_t b2 = desc_sw128(sb + L.off_b + p.n1 * 128 + ks * 32);
+            umma_bf16(tmem + p.n1, a_hi, b2, id2, (kb | ks) != 0);
+            if (!p.fold) umma_bf16(tmem + p.n1, a_lo, b2, id2, 1);
           }
         }
         umma_commit(freeb(st));
@@ -171,65 +188,79 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       mbar_wait_bounded(accb, 0, p.err, p.limit_ns);
     }
   } else {
-    // ---------------- converters: warps 0-7.  Thread t owns row t / 2 of the
-    // tile and channel chunks 4 * (t & 1) .. +3 (8 channels each) of every
-    // K block, so its row's partial sums stay in registers.  In the 128-byte
-    // swizzled tile chunk c of row i sits at i * 128 + ((c ^ (i & 7)) << 4);
-    // any 8 consecutive threads touch 8 distinct chunk positions, so the
-    // shared-memory accesses are free of bank conflicts.
-    const int row = tid >> 1, cbase = (tid & 1) * 4;
-    const int m = m0 + row;
-    const bool valid = m < p.M;
-    const float iw =
-        valid ? 2.0f * sigmoidf_dev(p.inj[m * p.ld_inj + s] / static_cast<float>(HC)) : 0.f;
-    float ss = 0.f, ij[8];
+    // ---------------- converters: warps 0-7.  Thread (warp w, lane l) owns
+    // channel chunk l & 7 (8 channels) of every K block and the four rows
+    // 4w + (l >> 3) + 32 pp, pp < 4.  In the 128-byte swizzled tile chunk c of
+    // row i sits at i * 128 + ((c ^ (i & 7)) << 4): the 8 lanes of a row read
+    // 8 distinct chunk positions, so there are no bank conflicts; the Wnorm
+    // factor (1 + w) of the chunk is formed once and reused for four rows.
+    const int ch = lane & 7;
+    const int rbase = warp * 4 + (lane >> 3);
+    float iw[4], ss[4];
+    bool valid[4];
+    float ij[4][HC];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ij[j] = 0.f;
-    bf16_t* r2row = p.R2 + static_cast<int64_t>(valid ? m : 0) * p.K + static_cast<int64_t>(s) * HS;
+    for (int pp = 0; pp < 4; ++pp) {
+      const int m = m0 + rbase + 32 * pp;
+      valid[pp] = m < p.M;
+      iw[pp] = valid[pp] ? 2.0f * sigmoidf_dev(p.inj[m * p.ld_inj + s] / static_cast<float>(HC)) : 0.f;
+      ss[pp] = 0.f;
+#pragma unroll
+      for (int j = 0; j < HC; ++j) ij[pp][j] = 0.f;
+    }
     bool ok = true;
     for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % K1_NST;
       ok = mbar_wait_bounded(full(st), (kb / K1_NST) & 1, p.err, p.limit_ns);
       if (!ok) break;
       unsigned char* sb = smem + st * p.stage_bytes;
+      const int col = kb * BK + ch * 8;           // channel within the stream
+      float f[8];
+      unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wn + ch * 16), f);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int ch = cbase + i;
-        const int col = kb * BK + ch * 8;           // channel within the stream
+      for (int e = 0; e < 8; ++e) f[e] += 1.0f;
+      float wi[INJ_MMA ? 1 : HC][8];
+      if constexpr (!INJ_MMA) {
+#pragma unroll
+        for (int j = 0; j < HC; ++j)
+          unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wi + j * 128 + ch * 16), wi[j]);
+      }
+#pragma unroll
+      for (int pp = 0; pp < 4; ++pp) {
+        const int row = rbase + 32 * pp;
         const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-        float rv[8], yv[8], wn[8], a[8];
+        float rv[8], yv[8], a[8];
         unpack8(*reinterpret_cast<const uint4*>(sb + off), rv);
         unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(p.Wnorm + static_cast<int64_t>(s) * HS + col)), wn);
         uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pr[e] = pack2(fmaf(yv[2 * e], iw, rv[2 * e]), fmaf(yv[2 * e + 1], iw, rv[2 * e + 1]));
+          pr[e] = pack2(fmaf(yv[2 * e], iw[pp], rv[2 * e]), fmaf(yv[2 * e + 1], iw[pp], rv[2 * e + 1]));
           const float r0 = lo_bf16(pr[e]), r1 = hi_bf16(pr[e]);
-          ss = fmaf(r0, r0, ss);
-          ss = fmaf(r1, r1, ss);
-          a[2 * e] = p.fold ? r0 : r0 * (1.0f + wn[2 * e]);
-          a[2 * e + 1] = p.fold ? r1 : r1 * (1.0f + wn[2 * e + 1]);
+          ss[pp] = fmaf(r0, r0, ss[pp]);
+          ss[pp] = fmaf(r1, r1, ss[pp]);
+          a[2 * e] = p.fold ? r0 : r0 * f[2 * e];
+          a[2 * e + 1] = p.fold ? r1 : r1 * f[2 * e + 1];
           ph[e] = pack2(a[2 * e], a[2 * e + 1]);
           pl[e] = pack2(a[2 * e] - lo_bf16(ph[e]), a[2 * e + 1] - hi_bf16(ph[e]));
         }
-        if (valid)
-          *reinterpret_cast<uint4*>(r2row + col) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+        if (valid[pp])
+          *reinterpret_cast<uint4*>(p.R2 + static_cast<int64_t>(m0 + row) * p.K +
+                                    static_cast<int64_t>(s) * HS + col) =
+              make_uint4(pr[0], pr[1], pr[2], pr[3]);
         if (p.fold) {
           *reinterpret_cast<uint4*>(sb + off) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
         } else {
           *reinterpret_cast<uint4*>(sb + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
           *reinterpret_cast<uint4*>(sb + TILE_BYTES + off) = make_uint4(pl[0], pl[1], pl[2], pl[3]);
         }
+        if constexpr (!INJ_MMA) {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (j < HC) {
-            float wi[8];
-            unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wi + j * 128 + ch * 16), wi);
-            float t = ij[j];
+          for (int j = 0; j < HC; ++j) {
+            float t = ij[pp][j];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) t = fmaf(a[e], wi[e], t);
-            ij[j] = t;
+            for (int e = 0; e < 8; ++e) t = fmaf(a[e], wi[j][e], t);
+            ij[pp][j] = t;
           }
         }
       }
@@ -237,15 +268,25 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(conv(st));
     }
-    // per-row totals: the two threads of a row are lanes 2i and 2i+1
-    ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+    // per-row totals: the 8 lanes of a row hold its 8 channel chunks
 #pragma unroll
-    for (int j = 0; j < 8; ++j) ij[j] += __shfl_xor_sync(0xffffffffu, ij[j], 1);
-    if ((tid & 1) == 0) {
-      rowss[row] = ss;
+    for (int pp = 0; pp < 4; ++pp) {
 #pragma unroll
-      for (int j = 0; j < 8; ++j)
-        if (j < HC) rowinj[row * HC + j] = ij[j];
+      for (int o = 1; o < 8; o <<= 1) {
+        ss[pp] += __shfl_xor_sync(0xffffffffu, ss[pp], o);
+        if constexpr (!INJ_MMA) {
+#pragma unroll
+          for (int j = 0; j < HC; ++j) ij[pp][j] += __shfl_xor_sync(0xffffffffu, ij[pp][j], o);
+        }
+      }
+      if (ch == 0) {
+        const int row = rbase + 32 * pp;
+        rowss[row] = ss[pp];
+        if constexpr (!INJ_MMA) {
+#pragma unroll
+          for (int j = 0; j < HC; ++j) rowinj[row * HC + j] = ij[pp][j];
+        }
+      }
     }
     named_bar_sync(1, K1_CONV_WARPS * 32);
     // ---------------- epilogue: rrms_s, inj partial, lora partial
@@ -256,17 +297,32 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     const int em = m0 + erow;
     const bool v = em < p.M;
     const float rr = 1.0f / sqrtf(rowss[erow] / static_cast<float>(HS) + p.eps);
-    if (v && half == 0) {
-      p.rrms[static_cast<int64_t>(em) * HC + s] = rr;
-      for (int j = 0; j < HC; ++j)
-        p.inj_part[(static_cast<int64_t>(s) * p.M + em) * HC + j] = rr * rowinj[erow * HC + j];
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    if (ok && half == 0) {
+      float injv[HC];
+      if constexpr (INJ_MMA) {
+        uint32_t acc[16];
+        tmem_ld16(tl + r, acc);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < HC; ++j) injv[j] = __uint_as_float(acc[j]);
+      } else {
+#pragma unroll
+        for (int j = 0; j < HC; ++j) injv[j] = rowinj[erow * HC + j];
+      }
+      if (v) {
+        p.rrms[static_cast<int64_t>(em) * HC + s] = rr;
+#pragma unroll
+        for (int j = 0; j < HC; ++j)
+          p.inj_part[(static_cast<int64_t>(s) * p.M + em) * HC + j] = rr * injv[j];
+      }
     }
     if (ok) {
       const int cols = r / 2;
       float* dst = p.part + (static_cast<int64_t>(s) * p.M + (v ? em : 0)) * r + half * cols;
       for (int c0 = 0; c0 < cols; c0 += 16) {
         uint32_t acc[16];
-        tmem_ld16(tmem + (static_cast<uint32_t>(32 * q) << 16) + half * cols + c0, acc);
+        tmem_ld16(tl + half * cols + c0, acc);
         tmem_ld_wait();
         if (v) {
 #pragma unroll
@@ -315,219 +371,278 @@ __global__ void k1_reduce_kernel(const float* __restrict__ part, const float* __
 }
 
 // ===================================================================== K2
+// Unit = (128-token tile t, NCU-channel block cb); the MMA N dimension holds
+// the HC streams of those channels (N = HC * NCU rows of Wu).  Warp roles:
+//   warp 0  TMA: the h tile (resident per token tile when it fits) and the Wu
+//           K blocks;
+//   warp 1  one thread issues tcgen05.mma into a double-buffered accumulator;
+//   warp 2  tensor-memory allocation;
+//   warp 3  TMA: the unit's R2 tile (HC boxes, 64- or 32-byte swizzle) and
+//           its Wnorm slice into a two-slot ring;
+//   warps 4-11  epilogue: one token row per thread, NCU/2 channels each.
+// The epilogue writes x into a swizzled staging tile that leaves by TMA store.
 constexpr int K2_THREADS = 384;
 constexpr int K2_TMA_WARP = 0;
 constexpr int K2_MMA_WARP = 1;
 constexpr int K2_ALLOC_WARP = 2;
+constexpr int K2_R2_WARP = 3;
 constexpr int K2_EPI_WARP0 = 4;
 constexpr int K2_EPI_WARPS = 8;
-constexpr int NC = 64;   // channels per unit
+
+__host__ __device__ constexpr int k2_ncu(int hc) { return hc <= 4 ? 32 : 16; }
 
 struct K2Params {
   CUtensorMap tm_h;    // h [M][r], box {64, 128}, 128B swizzle
-  CUtensorMap tm_wu;   // Wu [K][r], box {64, 64}, 128B swizzle
-  const bf16_t* R2;
+  CUtensorMap tm_wu;   // Wu [K][r], box {64, NCU}, 128B swizzle
+  CUtensorMap tm_r2;   // R2 [M][K], box {NCU, 128}, NCU*2-byte swizzle
+  CUtensorMap tm_wn;   // Wnorm as [HC][HS], box {NCU, HC}
+  CUtensorMap tm_x;    // x [M][HS], box {NCU, 128}, same swizzle (store)
   const float* rrms;
-  const bf16_t* Wnorm;
-  bf16_t* x;
-  int M, HC, HS, K, r;
-  int nkb, ncb, n_units, nst, nacc, ncols_acc;
-  uint32_t stage_bytes, tmem_cols, wn_bytes;
+  int M, HS, K, r;
+  int nkb, ncb, n_units, nst, a_res;
+  uint32_t b_bytes, stage_bytes, r2_slot, x_slot;
+  uint32_t off_st, off_r2, off_x, off_bar;
   int* err;
   uint64_t limit_ns;
 };
+
+// Byte offset of 16-byte chunk `chunk` of row `row` in a box whose rows are
+// ROWB bytes and that TMA wrote with the ROWB-byte swizzle (the chunk index
+// is XORed with address bits 7.. of the row start).
+template <int ROWB>
+__device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
+  if constexpr (ROWB == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+  else return row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4);
+}
 
 template <int HCT>
 __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant__ K2Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   constexpr int HC = HCT;
-  const int HS = p.HS, nkb = p.nkb, nst = p.nst, nacc = p.nacc;
+  constexpr int NCU = k2_ncu(HCT);
+  constexpr int N = HC * NCU;
+  constexpr uint32_t BOXB = BM * NCU * 2;        // one stream's R2 box
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int HS = p.HS, nkb = p.nkb, nst = p.nst;
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar = sbase + nst * p.stage_bytes;
-  const uint32_t wnbar = bar + 160u;
-  const bf16_t* s_wn = reinterpret_cast<const bf16_t*>(smem + nst * p.stage_bytes + 256);
-  auto full = [&](int st) { return bar + 8u * st; };
-  auto freeb = [&](int st) { return bar + 64u + 8u * st; };
+  const uint32_t bar = sbase + p.off_bar;
+  auto full = [&](int st) { return bar + 8u * st; };           // 0..7
+  auto freeb = [&](int st) { return bar + 64u + 8u * st; };    // 8..15
   auto accfull = [&](int a) { return bar + 128u + 8u * a; };
   auto accfree = [&](int a) { return bar + 144u + 8u * a; };
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + nst * p.stage_bytes + 192);
+  auto r2full = [&](int a) { return bar + 160u + 8u * a; };
+  auto r2free = [&](int a) { return bar + 176u + 8u * a; };
+  const uint32_t afull = bar + 192u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 224);
+
+  const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.n_units / gridDim.x);
+  const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.n_units / gridDim.x);
+  const int n_local = u1 - u0;
 
   if (tid == 0) {
+    prefetch_tmap(&p.tm_h);
+    prefetch_tmap(&p.tm_wu);
+    prefetch_tmap(&p.tm_r2);
+    prefetch_tmap(&p.tm_wn);
+    prefetch_tmap(&p.tm_x);
     for (int i = 0; i < nst; ++i) {
       mbar_init(full(i), 1);
       mbar_init(freeb(i), 1);
     }
-    for (int a = 0; a < nacc; ++a) {
+    for (int a = 0; a < 2; ++a) {
       mbar_init(accfull(a), 1);
       mbar_init(accfree(a), K2_EPI_WARPS);
+      mbar_init(r2full(a), 1);
+      mbar_init(r2free(a), K2_EPI_WARPS);
     }
-    mbar_init(wnbar, 1);
+    mbar_init(afull, 1);
     fence_mbar_init();
   }
   if (warp == K2_ALLOC_WARP) {
-    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_alloc(smem_u32(tmem_slot), 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256)));
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const int n_local = p.n_units > static_cast<int>(blockIdx.x)
-                          ? (p.n_units - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const uint32_t tmem_cols = 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256));
 
   if (warp == K2_TMA_WARP) {
     if (lane == 0) {
-      // Wnorm, staged once for the epilogue
-      mbar_arrive_expect_tx(wnbar, p.wn_bytes);
-      bulk_g2s(smem_u32(s_wn), p.Wnorm, p.wn_bytes, wnbar);
-      int g = 0;
       bool ok = true;
+      int g = 0, cur_t = -1;
       int last_g[8];
       for (int i = 0; i < 8; ++i) last_g[i] = -1;
+      int a_loads = 0;
       for (int i = 0; i < n_local && ok; ++i) {
-        const int u = blockIdx.x + i * gridDim.x;
-        const int t = u / p.ncb, cb = u % p.ncb;
+        const int u = u0 + i, t = u / p.ncb, cb = u % p.ncb;
+        if (p.a_res && t != cur_t) {
+          // the previous token tile's MMAs are done with the resident h tile
+          if (i > 0) ok = mbar_wait_bounded(accfull((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, p.limit_ns);
+          if (!ok) break;
+          mbar_arrive_expect_tx(afull, nkb * TILE_BYTES);
+          for (int kb = 0; kb < nkb; ++kb)
+            tma_load_2d(sbase + kb * TILE_BYTES, &p.tm_h, kb * BK, t * BM, afull);
+          cur_t = t;
+          ++a_loads;
+        }
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int st = g % nst;
           if (g >= nst) ok = mbar_wait_bounded(freeb(st), ((g / nst) - 1) & 1, p.err, p.limit_ns);
           if (!ok) break;
-          const uint32_t sb = sbase + st * p.stage_bytes;
-          mbar_arrive_expect_tx(full(st), TILE_BYTES + HC * NC * 128);
-          tma_load_2d(sb, &p.tm_h, kb * BK, t * BM, full(st));
+          const uint32_t sb = sbase + p.off_st + st * p.stage_bytes;
+          mbar_arrive_expect_tx(full(st), p.stage_bytes);
+          uint32_t bb = sb;
+          if (!p.a_res) {
+            tma_load_2d(sb, &p.tm_h, kb * BK, t * BM, full(st));
+            bb += TILE_BYTES;
+          }
           for (int ss = 0; ss < HC; ++ss)
-            tma_load_2d(sb + TILE_BYTES + ss * NC * 128, &p.tm_wu, kb * BK, ss * HS + cb * NC,
-                        full(st));
+            tma_load_2d(bb + ss * NCU * 128, &p.tm_wu, kb * BK, ss * HS + cb * NCU, full(st));
           last_g[st] = g;
         }
       }
       for (int st = 0; st < nst; ++st)
         if (last_g[st] >= 0) mbar_wait_bounded(full(st), (last_g[st] / nst) & 1, p.err, p.limit_ns);
-      mbar_wait_bounded(wnbar, 0, p.err, p.limit_ns);
+      if (a_loads > 0) mbar_wait_bounded(afull, (a_loads - 1) & 1, p.err, p.limit_ns);
     }
-  } else if (warp == K2_MMA_WARP) {
+  } else if (warp == K2_R2_WARP) {
     if (lane == 0) {
-      const int N = HC * NC;
-      int g = 0;
       bool ok = true;
       int issued = 0;
       for (int i = 0; i < n_local && ok; ++i) {
-        const int ab = i % nacc;
-        if (i >= nacc) ok = mbar_wait_bounded(accfree(ab), ((i / nacc) - 1) & 1, p.err, p.limit_ns);
+        const int u = u0 + i, t = u / p.ncb, cb = u % p.ncb;
+        const int slot = i & 1;
+        if (i >= 2) ok = mbar_wait_bounded(r2free(slot), ((i >> 1) - 1) & 1, p.err, p.limit_ns);
+        if (!ok) break;
+        const uint32_t rb = sbase + p.off_r2 + slot * p.r2_slot;
+        mbar_arrive_expect_tx(r2full(slot), HC * BOXB + HC * NCU * 2);
+        for (int ss = 0; ss < HC; ++ss)
+          tma_load_2d(rb + ss * BOXB, &p.tm_r2, ss * HS + cb * NCU, t * BM, r2full(slot));
+        tma_load_2d(rb + HC * BOXB, &p.tm_wn, cb * NCU, 0, r2full(slot));
+        ++issued;
+      }
+      for (int i = max(0, issued - 2); i < issued; ++i)
+        mbar_wait_bounded(r2full(i & 1), (i >> 1) & 1, p.err, p.limit_ns);
+    }
+  } else if (warp == K2_MMA_WARP) {
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(BM, N);
+      bool ok = true;
+      int g = 0, cur_t = -1, a_ph = 0, issued = 0;
+      for (int i = 0; i < n_local && ok; ++i) {
+        const int u = u0 + i, t = u / p.ncb;
+        const int ab = i & 1;
+        if (i >= 2) ok = mbar_wait_bounded(accfree(ab), ((i >> 1) - 1) & 1, p.err, p.limit_ns);
+        if (ok && p.a_res && t != cur_t) {
+          ok = mbar_wait_bounded(afull, a_ph & 1, p.err, p.limit_ns);
+          ++a_ph;
+          cur_t = t;
+        }
         if (!ok) break;
         tc_fence_after();
-        const uint32_t dcol = tmem + ab * p.ncols_acc;
+        const uint32_t dcol = tmem + ab * N;
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int st = g % nst;
           ok = mbar_wait_bounded(full(st), (g / nst) & 1, p.err, p.limit_ns);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t sb = sbase + st * p.stage_bytes;
+          const uint32_t sb = sbase + p.off_st + st * p.stage_bytes;
+          const uint32_t a_base = p.a_res ? sbase + kb * TILE_BYTES : sb;
+          const uint32_t b_base = p.a_res ? sb : sb + TILE_BYTES;
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
-            const uint64_t ad = desc_sw128(sb + ks * 32);
-            for (int n0 = 0; n0 < N; n0 += 256) {
-              const int nn = min(256, N - n0);
-              const uint64_t bd = desc_sw128(sb + TILE_BYTES + n0 * 128 + ks * 32);
-              umma_bf16(dcol + n0, ad, bd, idesc_bf16(BM, nn), (kb | ks) != 0);
-            }
-          }
+          for (int ks = 0; ks < BK / 16; ++ks)
+            umma_bf16(dcol, desc_sw128(a_base + ks * 32), desc_sw128(b_base + ks * 32), idesc,
+                      (kb | ks) != 0);
           umma_commit(freeb(st));
         }
         if (!ok) break;
         umma_commit(accfull(ab));
         ++issued;
       }
-      // all issued MMAs finish before tensor memory is released
-      if (issued > 0) {
-        const int last = issued - 1;
-        mbar_wait_bounded(accfull(last % nacc), (last / nacc) & 1, p.err, p.limit_ns);
-      }
+      if (issued > 0) mbar_wait_bounded(accfull((issued - 1) & 1), ((issued - 1) >> 1) & 1, p.err, p.limit_ns);
     }
   } else if (warp >= K2_EPI_WARP0) {
-    // Epilogue: thread = one token row (TMEM lane), 32 channels of the unit
-    // (warps 4-7 the first half, 8-11 the second).  Channels go in chunks of
-    // CC; the R2 values of chunk q+1 are loaded while chunk q is computed, and
-    // those of chunk 0 (and rrms) before waiting for the accumulator.
-    constexpr int CC = HC <= 4 ? 16 : 8;
-    constexpr int NCH = 32 / CC;
-    constexpr int V = CC / 8;
+    constexpr int CPT = NCU / 2;          // channels per thread
+    constexpr int V = CPT / 8;            // 16-byte chunks per thread and stream
     const int ew = warp - K2_EPI_WARP0;
     const int q4 = warp & 3, half = ew >> 2;
+    const int row = 32 * q4 + lane;
+    const bool leader = (ew == 0 && lane == 0);
     const float inv_hc = 1.0f / static_cast<float>(HC);
-    bool wn_ready = mbar_wait_bounded(wnbar, 0, p.err, p.limit_ns);
-    for (int i = 0; i < n_local && wn_ready; ++i) {
-      const int u = blockIdx.x + i * gridDim.x;
-      const int t = u / p.ncb, cb = u % p.ncb;
-      const int ab = i % nacc;
-      const int row = 32 * q4 + lane;
+    for (int i = 0; i < n_local; ++i) {
+      const int u = u0 + i, t = u / p.ncb, cb = u % p.ncb;
+      const int ab = i & 1, slot = i & 1;
       const int64_t m = static_cast<int64_t>(t) * BM + row;
       const bool v = m < p.M;
-      const int cbase = cb * NC + half * 32;          // first channel of this thread
-      const bf16_t* r2p = p.R2 + (v ? m : 0) * p.K + cbase;
       float rr[HC];
-      uint4 bufA[HC][V], bufB[HC][V];
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss) rr[ss] = v ? __ldg(p.rrms + m * HC + ss) : 0.f;
-      auto load = [&](int q, uint4 (&buf)[HC][V]) {
-#pragma unroll
-        for (int ss = 0; ss < HC; ++ss)
-#pragma unroll
-          for (int j = 0; j < V; ++j)
-            buf[ss][j] = v ? __ldg(reinterpret_cast<const uint4*>(r2p + ss * HS + q * CC + j * 8))
-                           : make_uint4(0, 0, 0, 0);
-      };
-      load(0, bufA);
-      if (!mbar_wait_bounded(accfull(ab), (i / nacc) & 1, p.err, p.limit_ns)) break;
+      bool got = mbar_wait_bounded(accfull(ab), (i >> 1) & 1, p.err, p.limit_ns);
+      got = got && mbar_wait_bounded(r2full(slot), (i >> 1) & 1, p.err, p.limit_ns);
+      // all eight epilogue warps take the same branch (they meet at named
+      // barriers below)
+      if (!named_bar_and(1, K2_EPI_WARPS * 32, got)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q4) << 16) + ab * p.ncols_acc;
+      const unsigned char* rb = smem + p.off_r2 + slot * p.r2_slot;
+      const bf16_t* wns = reinterpret_cast<const bf16_t*>(rb + HC * BOXB);
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q4) << 16) + ab * N + half * CPT;
+      float acc[CPT];
 #pragma unroll
-      for (int q = 0; q < NCH; ++q) {
-        uint4 (&cur)[HC][V] = (q & 1) ? bufB : bufA;
-        uint4 (&nxt)[HC][V] = (q & 1) ? bufA : bufB;
-        if (q + 1 < NCH) load(q + 1, nxt);
-        float acc[CC];
+      for (int e = 0; e < CPT; ++e) acc[e] = 0.f;
 #pragma unroll
-        for (int e = 0; e < CC; ++e) acc[e] = 0.f;
+      for (int ss = 0; ss < HC; ++ss) {
+        uint32_t gv[CPT];
+        if constexpr (CPT == 16) tmem_ld16(tbase + ss * NCU, gv);
+        else tmem_ld8(tbase + ss * NCU, gv);
+        tmem_ld_wait();
+        float r2[CPT], wn[CPT];
 #pragma unroll
-        for (int ss = 0; ss < HC; ++ss) {
-          uint32_t gv[CC];
-          if constexpr (CC == 16) tmem_ld16(tbase + ss * NC + half * 32 + q * CC, gv);
-          else tmem_ld8(tbase + ss * NC + half * 32 + q * CC, gv);
-          tmem_ld_wait();
-          float r2[CC], wn[CC];
-#pragma unroll
-          for (int j = 0; j < V; ++j) {
-            unpack8(cur[ss][j], r2 + 8 * j);
-            unpack8(*reinterpret_cast<const uint4*>(s_wn + ss * HS + cbase + q * CC + j * 8), wn + 8 * j);
-          }
-#pragma unroll
-          for (int e = 0; e < CC; ++e) {
-            const float G = sigmoid_tanh(__uint_as_float(gv[e]));
-            acc[e] = fmaf(G, r2[e] * rr[ss] * (1.0f + wn[e]), acc[e]);
-          }
+        for (int j = 0; j < V; ++j) {
+          unpack8(*reinterpret_cast<const uint4*>(rb + ss * BOXB + swz_off<NCU * 2>(row, half * V + j)),
+                  r2 + 8 * j);
+          unpack8(*reinterpret_cast<const uint4*>(wns + ss * NCU + half * CPT + 8 * j), wn + 8 * j);
         }
-        if (v) {
-          uint32_t o[CC / 2];
 #pragma unroll
-          for (int e = 0; e < CC / 2; ++e) o[e] = pack2(acc[2 * e] * inv_hc, acc[2 * e + 1] * inv_hc);
-          uint4* xp = reinterpret_cast<uint4*>(p.x + m * HS + cbase + q * CC);
-#pragma unroll
-          for (int j = 0; j < V; ++j) xp[j] = make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-        }
+        for (int e = 0; e < CPT; ++e)
+          acc[e] = fmaf(sigmoid_tanh(__uint_as_float(gv[e])), r2[e] * rr[ss] * (1.0f + wn[e]), acc[e]);
       }
+      // R2 slot and accumulator buffer are free again
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(accfree(ab));
+      if (lane == 0) {
+        mbar_arrive(r2free(slot));
+        mbar_arrive(accfree(ab));
+      }
+      // x staging buffer i % 2: the store issued two units ago has read it
+      if (leader) bulk_wait_read<1>();
+      named_bar_sync(1, K2_EPI_WARPS * 32);
+      unsigned char* xs = smem + p.off_x + (i & 1) * p.x_slot;
+#pragma unroll
+      for (int j = 0; j < V; ++j) {
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          o[e] = pack2(acc[8 * j + 2 * e] * inv_hc, acc[8 * j + 2 * e + 1] * inv_hc);
+        *reinterpret_cast<uint4*>(xs + swz_off<NCU * 2>(row, half * V + j)) = make_uint4(o[0], o[1], o[2], o[3]);
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(1, K2_EPI_WARPS * 32);
+      if (leader) {
+        tma_store_2d(&p.tm_x, cb * NCU, t * BM, smem_u32(xs));
+        bulk_commit();
+      }
     }
+    if (leader) bulk_wait<0>();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == K2_ALLOC_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, p.tmem_cols);
+    tmem_dealloc(tmem, tmem_cols);
   }
 }
 
@@ -535,6 +650,20 @@ uint32_t pow2_cols(int n) {
   uint32_t c = 32;
   while (c < static_cast<uint32_t>(n)) c <<= 1;
   return c;
+}
+
+template <int HCT, bool INJ_MMA>
+cudaError_t launch_k1(const K1Params& p, int grid, size_t smem, const Device& dev,
+                      cudaStream_t stream) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t e = cudaFuncSetAttribute(k1_kernel<HCT, INJ_MMA>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
+    if (e != cudaSuccess) return e;
+    attr = true;
+  }
+  k1_kernel<HCT, INJ_MMA><<<grid, K1_THREADS, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
 template <int HCT>
@@ -554,6 +683,7 @@ cudaError_t launch_k2(const K2Params& p, int grid, size_t smem, const Device& de
 bool prefill_supported(const Call& c) {
   return c.HS % 64 == 0 && c.r % 64 == 0 && c.r <= 512 && c.HC >= 1 && c.HC <= 8;
 }
+static_assert(k2_ncu(4) * 4 == 128 && k2_ncu(8) * 8 == 128, "K2 N = 128 for the workloads");
 
 }  // namespace
 
@@ -579,9 +709,9 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
       reinterpret_cast<unsigned char*>(inj_part) + ((static_cast<size_t>(c.HC) * M * c.HC * 4 + 255) / 256) * 256);
 
   // ---------------- K1
-  static bool k1_attr = false;
   {
     K1Params p;
+    const bool inj_mma = c.r + WI_ROWS <= 512;
     const uint64_t dR[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(M)};
     const uint64_t sR[1] = {static_cast<uint64_t>(c.K) * 2};
     const uint32_t bT[2] = {BK, BM};
@@ -595,40 +725,53 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const uint32_t bw[2] = {BK, static_cast<uint32_t>(p.wbox_rows)};
     if (!make_tmap_bf16(&p.tm_w, c.Wd, 2, dw, sR, bw, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     const uint64_t di[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(c.HC)};
-    const uint32_t bi[2] = {BK, static_cast<uint32_t>(c.HC)};
-    if (!make_tmap_bf16(&p.tm_wi, c.Wi, 2, di, sR, bi)) return cudaErrorInvalidValue;
+    const uint32_t bi[2] = {BK, static_cast<uint32_t>(inj_mma ? WI_ROWS : c.HC)};
+    if (!make_tmap_bf16(&p.tm_wi, c.Wi, 2, di, sR, bi,
+                        inj_mma ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE))
+      return cudaErrorInvalidValue;
     p.inj = c.inj;
     p.ld_inj = c.ld_inj;
-    p.Wnorm = c.Wnorm;
     p.R2 = c.R2;
+    p.Wnorm = c.Wnorm;
     p.rrms = c.rrms;
     p.part = part;
     p.inj_part = inj_part;
     p.M = M;
-    p.HC = c.HC;
     p.HS = c.HS;
     p.K = c.K;
     p.r = c.r;
     p.fold = c.fold;
     p.eps = c.eps;
     p.nkb = c.HS / BK;
-    p.n_mma = c.r > 256 ? 2 : 1;
-    p.mma_n = c.r / p.n_mma;
-    const K1Smem L = k1_smem(c.r, c.HC);
+    // MMA column blocks over the B tile (r rows of Wd, then 16 inject rows)
+    const int ntot = c.r + (inj_mma ? WI_ROWS : 0);
+    if (ntot <= 256) {
+      p.n1 = ntot;
+      p.n2 = 0;
+    } else {
+      p.n1 = ((ntot / 2) + 15) / 16 * 16;
+      p.n2 = ntot - p.n1;
+    }
+    const K1Smem L = k1_smem(c.r, c.HC, inj_mma);
     p.stage_bytes = L.off_bar / K1_NST;
-    p.tmem_cols = pow2_cols(c.r);
+    p.tmem_cols = pow2_cols(ntot);
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
     const size_t smem = L.total + 1024;
     if (smem > static_cast<size_t>(dev.smem_optin)) return cudaErrorNotSupported;
-    if (!k1_attr) {
-      cudaError_t e = cudaFuncSetAttribute(k1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           dev.smem_optin);
-      if (e != cudaSuccess) return e;
-      k1_attr = true;
+    cudaError_t e = cudaSuccess;
+    const int grid = n_mt * c.HC;
+#define HCGR_K1(HCV)                                                                        \
+  case HCV:                                                                                 \
+    e = inj_mma ? launch_k1<HCV, true>(p, grid, smem, dev, stream)                          \
+                : launch_k1<HCV, false>(p, grid, smem, dev, stream);                         \
+    break;
+    switch (c.HC) {
+      HCGR_K1(1) HCGR_K1(2) HCGR_K1(3) HCGR_K1(4) HCGR_K1(5) HCGR_K1(6) HCGR_K1(7)
+      default: e = inj_mma ? launch_k1<8, true>(p, grid, smem, dev, stream)
+                           : launch_k1<8, false>(p, grid, smem, dev, stream);
     }
-    k1_kernel<<<n_mt * c.HC, K1_THREADS, smem, stream>>>(p);
-    cudaError_t e = cudaGetLastError();
+#undef HCGR_K1
     if (e != cudaSuccess) return e;
   }
   // ---------------- reduce
@@ -643,36 +786,52 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   // ---------------- K2
   {
     K2Params p;
+    const int ncu = k2_ncu(c.HC);
     const uint64_t dh[2] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(M)};
     const uint64_t sh[1] = {static_cast<uint64_t>(c.r) * 2};
     const uint32_t bh[2] = {BK, BM};
-    if (!make_tmap_bf16(&p.tm_h, h, 2, dh, sh, bh, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     const uint64_t du[2] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(c.K)};
-    const uint32_t bu[2] = {BK, NC};
-    if (!make_tmap_bf16(&p.tm_wu, c.Wu, 2, du, sh, bu, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    p.R2 = c.R2;
+    const uint32_t bu[2] = {BK, static_cast<uint32_t>(ncu)};
+    const uint64_t dr[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(M)};
+    const uint64_t sr[1] = {static_cast<uint64_t>(c.K) * 2};
+    const uint32_t br[2] = {static_cast<uint32_t>(ncu), BM};
+    const uint64_t dn[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(c.HC)};
+    const uint64_t sn[1] = {static_cast<uint64_t>(c.HS) * 2};
+    const uint32_t bn[2] = {static_cast<uint32_t>(ncu), static_cast<uint32_t>(c.HC)};
+    const uint64_t dx[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(M)};
+    const CUtensorMapSwizzle sw = ncu == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    if (!make_tmap_bf16(&p.tm_h, h, 2, dh, sh, bh, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_bf16(&p.tm_wu, c.Wu, 2, du, sh, bu, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_bf16(&p.tm_r2, c.R2, 2, dr, sr, br, sw) ||
+        !make_tmap_bf16(&p.tm_wn, c.Wnorm, 2, dn, sn, bn) ||
+        !make_tmap_bf16(&p.tm_x, c.x, 2, dx, sn, br, sw))
+      return cudaErrorInvalidValue;
     p.rrms = c.rrms;
-    p.Wnorm = c.Wnorm;
-    p.x = c.x;
     p.M = M;
-    p.HC = c.HC;
     p.HS = c.HS;
     p.K = c.K;
     p.r = c.r;
     p.nkb = c.r / BK;
-    p.ncb = c.HS / NC;
+    p.ncb = c.HS / ncu;
     p.n_units = n_mt * p.ncb;
-    p.stage_bytes = TILE_BYTES + c.HC * NC * 128;
-    p.wn_bytes = static_cast<uint32_t>(c.K) * 2;
-    const int budget = dev.smem_optin - 1024 - 256 - static_cast<int>(p.wn_bytes);
-    p.nst = std::min(4, budget / static_cast<int>(p.stage_bytes));
+    p.b_bytes = static_cast<uint32_t>(c.HC * ncu * 128);
+    p.r2_slot = static_cast<uint32_t>(((c.HC * BM * ncu * 2 + c.HC * ncu * 2) + 1023) / 1024 * 1024);
+    p.x_slot = static_cast<uint32_t>(BM * ncu * 2);
+    const int fixed = 2 * static_cast<int>(p.r2_slot) + 2 * static_cast<int>(p.x_slot) + 256 + 1024;
+    const int a_bytes = p.nkb * static_cast<int>(TILE_BYTES);
+    // keep the h tile resident when that still leaves three Wu stages
+    p.a_res = (dev.smem_optin - fixed - a_bytes) / static_cast<int>(p.b_bytes) >= 3 ? 1 : 0;
+    p.stage_bytes = p.b_bytes + (p.a_res ? 0 : TILE_BYTES);
+    p.nst = std::min(8, (dev.smem_optin - fixed - (p.a_res ? a_bytes : 0)) /
+                            static_cast<int>(p.stage_bytes));
     if (p.nst < 2) return cudaErrorNotSupported;
-    p.ncols_acc = c.HC * NC;
-    p.nacc = 2 * p.ncols_acc <= 512 ? 2 : 1;
-    p.tmem_cols = pow2_cols(p.nacc * p.ncols_acc);
+    p.off_st = p.a_res ? static_cast<uint32_t>(a_bytes) : 0u;
+    p.off_r2 = p.off_st + p.nst * p.stage_bytes;
+    p.off_x = p.off_r2 + 2 * p.r2_slot;
+    p.off_bar = p.off_x + 2 * p.x_slot;
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
-    const size_t smem = static_cast<size_t>(p.nst) * p.stage_bytes + 256 + p.wn_bytes + 1024;
+    const size_t smem = p.off_bar + 256 + 1024;
     const int grid = std::min(p.n_units, dev.sms);
     cudaError_t e = cudaSuccess;
     switch (c.HC) {
