@@ -46,7 +46,7 @@ constexpr int K1_CONV_WARPS = 8;
 constexpr int K1_THREADS = (K1_CONV_WARPS + 2) * 32;
 constexpr int K1_TMA_WARP = K1_CONV_WARPS;
 constexpr int K1_MMA_WARP = K1_CONV_WARPS + 1;
-constexpr int K1_NST = 2;
+constexpr int K1_MAXST = 4;
 constexpr int WI_ROWS = 16;   // inject rows in the MMA's B tile (HC real, rest zero-filled)
 
 struct K1Params {
@@ -64,28 +64,29 @@ struct K1Params {
   int M, HS, K, r, fold;
   float eps;
   int nkb, wbox_rows, nwbox, n1, n2;   // MMA column blocks: [0, n1) and [n1, n1 + n2)
+  int nst;                             // pipeline stages (2 or 3)
   uint32_t stage_bytes, tmem_cols;
   int* err;
   uint64_t limit_ns;
 };
 
 struct K1Smem {
-  uint32_t off_b, off_wi, off_wn, off_bar, off_rowss, off_rowinj, total;
+  uint32_t stage, off_b, off_wi, off_wn, off_bar, off_rowss, off_rowinj, total;
 };
 
-// Stage: R tile, y tile, B tile (r rows of Wd, then the inject rows), the K
-// block's 64 Wnorm values.
-__host__ __device__ inline K1Smem k1_smem(int r, int HC, bool inj_mma) {
+// Stage: R tile, y tile, B tile (r rows of Wd, then the inject rows).  The K
+// blocks' Wnorm values (128 bytes each) sit in a small ring of their own.
+__host__ __device__ inline K1Smem k1_smem(int r, int HC, bool inj_mma, int nst) {
   K1Smem s;
   s.off_b = 2 * TILE_BYTES;
   s.off_wi = s.off_b + r * 128;
   const uint32_t wi_bytes = (inj_mma ? WI_ROWS : HC) * 128;
-  s.off_wn = s.off_wi + wi_bytes;
-  const uint32_t stage = ((s.off_wn + 128) + 1023) / 1024 * 1024;
-  s.off_bar = K1_NST * stage;
+  s.stage = (s.off_wi + wi_bytes + 1023) / 1024 * 1024;
+  s.off_wn = nst * s.stage;
+  s.off_bar = s.off_wn + K1_MAXST * 128;
   s.off_rowss = s.off_bar + 128;
   s.off_rowinj = s.off_rowss + BM * 4;
-  s.total = s.off_rowinj + BM * HC * 4;
+  s.total = s.off_rowinj + (inj_mma ? 0 : BM * HC * 4);
   return s;
 }
 
@@ -95,7 +96,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int HC = HCT;
-  const K1Smem L = k1_smem(p.r, HC, INJ_MMA);
+  const K1Smem L = k1_smem(p.r, HC, INJ_MMA, p.nst);
+  const int NST = p.nst;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int s = blockIdx.x % HC;
   const int m0 = (blockIdx.x / HC) * BM;
@@ -103,10 +105,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + L.off_bar;
   auto full = [&](int st) { return bar + 8u * st; };
-  auto conv = [&](int st) { return bar + 16u + 8u * st; };
-  auto freeb = [&](int st) { return bar + 32u + 8u * st; };
-  const uint32_t accb = bar + 48u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 64);
+  auto conv = [&](int st) { return bar + 32u + 8u * st; };
+  auto freeb = [&](int st) { return bar + 64u + 8u * st; };
+  const uint32_t accb = bar + 96u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 104);
   float* rowss = reinterpret_cast<float*>(smem + L.off_rowss);
   float* rowinj = reinterpret_cast<float*>(smem + L.off_rowinj);
 
@@ -115,7 +117,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     prefetch_tmap(&p.tm_y);
     prefetch_tmap(&p.tm_w);
     prefetch_tmap(&p.tm_wi);
-    for (int i = 0; i < K1_NST; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(full(i), 1);
       mbar_init(conv(i), K1_CONV_WARPS);
       mbar_init(freeb(i), 1);
@@ -134,15 +136,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 
   if (warp == K1_TMA_WARP) {
     if (lane == 0) {
-      int last_issued[K1_NST] = {-1, -1};
+      int last_issued[K1_MAXST] = {-1, -1, -1, -1};
       bool ok = true;
       const uint32_t wi_tx = (INJ_MMA ? WI_ROWS : HC) * 128;
       for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int st = kb % K1_NST;
-        if (kb >= K1_NST)
-          ok = mbar_wait_bounded(freeb(st), ((kb / K1_NST) - 1) & 1, p.err, p.limit_ns);
+        const int st = kb % NST;
+        if (kb >= NST)
+          ok = mbar_wait_bounded(freeb(st), ((kb / NST) - 1) & 1, p.err, p.limit_ns);
         if (!ok) break;
-        const uint32_t sb = sbase + st * p.stage_bytes;
+        const uint32_t sb = sbase + st * L.stage;
         mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES + r * 128 + wi_tx + 128);
         tma_load_2d(sb, &p.tm_R, s * HS + kb * BK, m0, full(st));
         tma_load_2d(sb + TILE_BYTES, &p.tm_y, kb * BK, m0, full(st));
@@ -150,13 +152,14 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
           tma_load_2d(sb + L.off_b + bx * p.wbox_rows * 128, &p.tm_w, s * HS + kb * BK,
                       bx * p.wbox_rows, full(st));
         tma_load_2d(sb + L.off_wi, &p.tm_wi, s * HS + kb * BK, 0, full(st));
-        bulk_g2s(sb + L.off_wn, p.Wnorm + static_cast<int64_t>(s) * HS + kb * BK, 128, full(st));
+        bulk_g2s(sbase + L.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kb * BK, 128,
+                 full(st));
         last_issued[st] = kb;
       }
       // outstanding copies land before the CTA can leave
-      for (int st = 0; st < K1_NST; ++st)
+      for (int st = 0; st < NST; ++st)
         if (last_issued[st] >= 0)
-          mbar_wait_bounded(full(st), (last_issued[st] / K1_NST) & 1, p.err, p.limit_ns);
+          mbar_wait_bounded(full(st), (last_issued[st] / NST) & 1, p.err, p.limit_ns);
     }
   } else if (warp == K1_MMA_WARP) {
     if (lane == 0) {
@@ -164,11 +167,11 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       const uint32_t id2 = idesc_bf16(BM, p.n2 > 0 ? p.n2 : 16);
       bool ok = true;
       for (int kb = 0; kb < nkb; ++kb) {
-        const int st = kb % K1_NST;
-        ok = mbar_wait_bounded(conv(st), (kb / K1_NST) & 1, p.err, p.limit_ns);
+        const int st = kb % NST;
+        ok = mbar_wait_bounded(conv(st), (kb / NST) & 1, p.err, p.limit_ns);
         if (!ok) break;
         tc_fence_after();
-        const uint32_t sb = sbase + st * p.stage_bytes;
+        const uint32_t sb = sbase + st * L.stage;
 #pragma unroll
         for (int ks = 0; ks < BK / 16; ++ks) {
           const uint64_t a_hi = desc_sw128(sb + ks * 32);
@@ -210,13 +213,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     }
     bool ok = true;
     for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb % K1_NST;
-      ok = mbar_wait_bounded(full(st), (kb / K1_NST) & 1, p.err, p.limit_ns);
+      const int st = kb % NST;
+      ok = mbar_wait_bounded(full(st), (kb / NST) & 1, p.err, p.limit_ns);
       if (!ok) break;
-      unsigned char* sb = smem + st * p.stage_bytes;
+      unsigned char* sb = smem + st * L.stage;
       const int col = kb * BK + ch * 8;           // channel within the stream
       float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wn + ch * 16), f);
+      unpack8(*reinterpret_cast<const uint4*>(smem + L.off_wn + st * 128 + ch * 16), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] += 1.0f;
       float wi[INJ_MMA ? 1 : HC][8];
@@ -752,8 +755,11 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
       p.n1 = ((ntot / 2) + 15) / 16 * 16;
       p.n2 = ntot - p.n1;
     }
-    const K1Smem L = k1_smem(c.r, c.HC, inj_mma);
-    p.stage_bytes = L.off_bar / K1_NST;
+    p.nst = 3;
+    while (p.nst > 2 && k1_smem(c.r, c.HC, inj_mma, p.nst).total + 1024 > static_cast<uint32_t>(dev.smem_optin))
+      --p.nst;
+    const K1Smem L = k1_smem(c.r, c.HC, inj_mma, p.nst);
+    p.stage_bytes = L.stage;
     p.tmem_cols = pow2_cols(ntot);
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
@@ -819,8 +825,10 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.x_slot = static_cast<uint32_t>(BM * ncu * 2);
     const int fixed = 2 * static_cast<int>(p.r2_slot) + 2 * static_cast<int>(p.x_slot) + 256 + 1024;
     const int a_bytes = p.nkb * static_cast<int>(TILE_BYTES);
-    // keep the h tile resident when that still leaves three Wu stages
-    p.a_res = (dev.smem_optin - fixed - a_bytes) / static_cast<int>(p.b_bytes) >= 3 ? 1 : 0;
+    // The h tile stays resident only when that still leaves five Wu stages;
+    // otherwise it is streamed with each Wu K block (an L2 re-read, cheap),
+    // which keeps more bytes in flight per SM.
+    p.a_res = (dev.smem_optin - fixed - a_bytes) / static_cast<int>(p.b_bytes) >= 5 ? 1 : 0;
     p.stage_bytes = p.b_bytes + (p.a_res ? 0 : TILE_BYTES);
     p.nst = std::min(8, (dev.smem_optin - fixed - (p.a_res ? a_bytes : 0)) /
                             static_cast<int>(p.stage_bytes));
