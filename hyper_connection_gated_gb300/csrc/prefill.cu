@@ -7,28 +7,32 @@
 // R2 * rrms * (1 + Wnorm), so xn and the gate never reach HBM), re-designed
 // for sm_103a:
 //
-// K1, one CTA per (128-token tile, stream s).  Because rrms_s is constant over
-//   stream s, lora = sum_s rrms_s * (R2_s . W_s^T): the CTA owns the whole
-//   K-range of its stream, so it knows rrms_s at the end of its K-loop and
-//   scales its partial product there.  Warp roles:
+// K1, one CTA per (128-token tile, stream s, K chunk of that stream).  Because
+//   rrms_s is constant over stream s, lora = sum_s rrms_s * (R2_s . W_s^T):
+//   the products are accumulated per stream without rrms and scaled later.
+//   Warp roles:
 //     warp 8      TMA producer: R and y tiles (128 x 64, 128-byte swizzle),
-//                 the matching 64 columns of Wd (all r rows) and of Wi;
-//     warps 0-7   converters: R2 = bf16(R + y * iw) (written to HBM), sum of
-//                 R2^2 and the inject dot products per row on the CUDA cores,
-//                 and the MMA operand in place: R2 for a folded weight, else
-//                 the hi/lo bf16 split of R2 * (1 + Wnorm) (two MMAs, so the
-//                 product keeps ~16 mantissa bits);
-//     warp 9      one thread issues tcgen05.mma (M=128, N=r split in <= 256
-//                 column blocks) into tensor memory.
-//   Epilogue (warps 0-7): rrms_s, inj_next partial, lora partial
-//   rrms_s * acc -> part[s][m][:].
-// R  (reduce): lora = sum_s part[s], inj_next = sum_s inj_part[s], and the
-//   up-GEMM operand h = bf16(SiLU(lora / HC)).
-// K2, persistent over (128-token tile, 64-channel block) units: A = h tile,
-//   B = the HC * 64 rows {s * HS + c} of Wu, D = 128 x (HC * 64) fp32 in
-//   tensor memory (double-buffered when it fits).  Epilogue warps read a
-//   row's gates for all streams, apply sigmoid, rebuild xn from R2, rrms and
-//   Wnorm and write x = (1/HC) * sum_s G * xn.
+//                 the matching 64 columns of the r Wd rows and of the inject
+//                 rows, and the K block's Wnorm values;
+//     warps 0-7   converters: R2 = bf16(R + y * iw) (written to HBM), the sum
+//                 of R2^2 per row, and the MMA operand in place: R2 for a
+//                 folded weight, else the hi/lo bf16 split of R2 * (1 + Wnorm)
+//                 (two MMAs, so the product keeps ~16 mantissa bits);
+//     warp 9      one thread issues tcgen05.mma (M=128, N = r + 16: the Wd
+//                 rows and the inject rows, in <= 256-column blocks).
+//   When r + 16 exceeds the 512 tensor-memory columns the inject dot
+//   products run on the converters' CUDA cores instead.  The epilogue writes
+//   the partial sums of squares and the un-scaled partial products.
+// R  (reduce): rrms_s from the partial sums of squares, lora / inj_next =
+//   sum_s rrms_s * (sum of the stream's partial products), and the up-GEMM
+//   operand h = bf16(SiLU(lora / HC)).  With few token tiles K1 splits each
+//   stream's K range into chunks so that the CTAs cover the SMs.
+// K2, persistent over (128-token tile, NCU-channel block) units: A = h tile,
+//   B = the HC * NCU rows {s * HS + c} of Wu, D = 128 x (HC * NCU) fp32 in
+//   double-buffered tensor memory.  The unit's R2 tile and Wnorm slice
+//   stream through a swizzled ring; epilogue warps read a row's gates for all
+//   streams, apply sigmoid, rebuild xn from R2, rrms and Wnorm and write
+//   x = (1/HC) * sum_s G * xn through a staging tile and a TMA store.
 #include <algorithm>
 
 #include "hc_gr_internal.cuh"
@@ -58,11 +62,10 @@ struct K1Params {
   int64_t ld_inj;
   bf16_t* R2;
   const bf16_t* Wnorm;
-  float* rrms;
-  float* part;        // [HC][M][r]
-  float* inj_part;    // [HC][M][HC]
-  int M, HS, K, r, fold;
-  float eps;
+  float* part;        // [HC * S][M][np]: lora columns, then the HC inject columns
+  float* sumsq;       // [HC * S][M] partial sums of R2^2
+  int M, HS, K, r, np, fold;
+  int S;              // K chunks per stream
   int nkb, wbox_rows, nwbox, n1, n2;   // MMA column blocks: [0, n1) and [n1, n1 + n2)
   int nst;                             // pipeline stages (2 or 3)
   uint32_t stage_bytes, tmem_cols;
@@ -99,9 +102,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   const K1Smem L = k1_smem(p.r, HC, INJ_MMA, p.nst);
   const int NST = p.nst;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int s = blockIdx.x % HC;
-  const int m0 = (blockIdx.x / HC) * BM;
-  const int HS = p.HS, r = p.r, nkb = p.nkb;
+  const int chunk = blockIdx.x % p.S;
+  const int s = (blockIdx.x / p.S) % HC;
+  const int m0 = (blockIdx.x / (p.S * HC)) * BM;
+  const int pid = s * p.S + chunk;                 // partial index
+  const int HS = p.HS, r = p.r;
+  const int kb0 = chunk * p.nkb / p.S, kb1 = (chunk + 1) * p.nkb / p.S;
+  const int nkb = kb1 - kb0;                       // K blocks of this CTA
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + L.off_bar;
   auto full = [&](int st) { return bar + 8u * st; };
@@ -145,14 +152,15 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
           ok = mbar_wait_bounded(freeb(st), ((kb / NST) - 1) & 1, p.err, p.limit_ns);
         if (!ok) break;
         const uint32_t sb = sbase + st * L.stage;
+        const int kx = (kb0 + kb) * BK;           // column within the stream
         mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES + r * 128 + wi_tx + 128);
-        tma_load_2d(sb, &p.tm_R, s * HS + kb * BK, m0, full(st));
-        tma_load_2d(sb + TILE_BYTES, &p.tm_y, kb * BK, m0, full(st));
+        tma_load_2d(sb, &p.tm_R, s * HS + kx, m0, full(st));
+        tma_load_2d(sb + TILE_BYTES, &p.tm_y, kx, m0, full(st));
         for (int bx = 0; bx < p.nwbox; ++bx)
-          tma_load_2d(sb + L.off_b + bx * p.wbox_rows * 128, &p.tm_w, s * HS + kb * BK,
+          tma_load_2d(sb + L.off_b + bx * p.wbox_rows * 128, &p.tm_w, s * HS + kx,
                       bx * p.wbox_rows, full(st));
-        tma_load_2d(sb + L.off_wi, &p.tm_wi, s * HS + kb * BK, 0, full(st));
-        bulk_g2s(sbase + L.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kb * BK, 128,
+        tma_load_2d(sb + L.off_wi, &p.tm_wi, s * HS + kx, 0, full(st));
+        bulk_g2s(sbase + L.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kx, 128,
                  full(st));
         last_issued[st] = kb;
       }
@@ -217,7 +225,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       ok = mbar_wait_bounded(full(st), (kb / NST) & 1, p.err, p.limit_ns);
       if (!ok) break;
       unsigned char* sb = smem + st * L.stage;
-      const int col = kb * BK + ch * 8;           // channel within the stream
+      const int col = (kb0 + kb) * BK + ch * 8;   // channel within the stream
       float f[8];
       unpack8(*reinterpret_cast<const uint4*>(smem + L.off_wn + st * 128 + ch * 16), f);
 #pragma unroll
@@ -292,15 +300,17 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       }
     }
     named_bar_sync(1, K1_CONV_WARPS * 32);
-    // ---------------- epilogue: rrms_s, inj partial, lora partial
+    // ---------------- epilogue: partial sums of squares and the un-scaled
+    // partial products (lora columns, then the inject columns); the reduce
+    // kernel applies rrms once all K chunks of the stream are in.
     if (ok) ok = mbar_wait_bounded(accb, 0, p.err, p.limit_ns);
     tc_fence_after();
     const int q = warp & 3, half = warp >> 2;
     const int erow = 32 * q + lane;
     const int em = m0 + erow;
     const bool v = em < p.M;
-    const float rr = 1.0f / sqrtf(rowss[erow] / static_cast<float>(HS) + p.eps);
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
+    float* dst = p.part + (static_cast<int64_t>(pid) * p.M + (v ? em : 0)) * p.np;
     if (ok && half == 0) {
       float injv[HC];
       if constexpr (INJ_MMA) {
@@ -314,15 +324,13 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
         for (int j = 0; j < HC; ++j) injv[j] = rowinj[erow * HC + j];
       }
       if (v) {
-        p.rrms[static_cast<int64_t>(em) * HC + s] = rr;
+        p.sumsq[static_cast<int64_t>(pid) * p.M + em] = rowss[erow];
 #pragma unroll
-        for (int j = 0; j < HC; ++j)
-          p.inj_part[(static_cast<int64_t>(s) * p.M + em) * HC + j] = rr * injv[j];
+        for (int j = 0; j < HC; ++j) dst[r + j] = injv[j];
       }
     }
     if (ok) {
       const int cols = r / 2;
-      float* dst = p.part + (static_cast<int64_t>(s) * p.M + (v ? em : 0)) * r + half * cols;
       for (int c0 = 0; c0 < cols; c0 += 16) {
         uint32_t acc[16];
         tmem_ld16(tl + half * cols + c0, acc);
@@ -330,9 +338,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
         if (v) {
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(dst + c0 + e) =
-                make_float4(__uint_as_float(acc[e]) * rr, __uint_as_float(acc[e + 1]) * rr,
-                            __uint_as_float(acc[e + 2]) * rr, __uint_as_float(acc[e + 3]) * rr);
+            *reinterpret_cast<float4*>(dst + half * cols + c0 + e) =
+                make_float4(__uint_as_float(acc[e]), __uint_as_float(acc[e + 1]),
+                            __uint_as_float(acc[e + 2]), __uint_as_float(acc[e + 3]));
         }
       }
     }
@@ -346,30 +354,59 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 }
 
 // ================================================================ reduce
-__global__ void k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ inj_part,
-                                 float* __restrict__ lora, float* __restrict__ inj_next,
-                                 bf16_t* __restrict__ h, int64_t M, int HC, int r) {
-  const int64_t n4 = M * r / 4;
-  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+// Per token row: rrms_s from the stream's partial sums of squares, then
+// lora / inj_next = sum_s rrms_s * (sum over the stream's K chunks of the
+// partial products), and the up-GEMM operand h = bf16(SiLU(lora / HC)).
+// Columns go in float4s (np is a multiple of 4 and r of 8, so a float4 never
+// straddles lora and the inject columns).
+constexpr int RED_ROWS = 2;   // token rows per reduce block
+
+__global__ void k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
+                                 float* __restrict__ rrms, float* __restrict__ lora,
+                                 float* __restrict__ inj_next, bf16_t* __restrict__ h, int M,
+                                 int HC, int S, int r, int np, int HS, float eps) {
+  // block = RED_ROWS token rows x (np / 4 rounded up to a warp) float4 columns;
+  // threads 0..HC-1 of a row form its rrms_s in shared memory first
+  __shared__ float s_rr[RED_ROWS][8];
+  const int m = blockIdx.x * RED_ROWS + threadIdx.y;
+  const int n4 = threadIdx.x;
+  const bool live = m < M;
+  if (live && n4 < HC) {
+    float q = 0.f;
+    for (int c = 0; c < S; ++c) q += sumsq[static_cast<int64_t>(n4 * S + c) * M + m];
+    const float rr = 1.0f / sqrtf(q / static_cast<float>(HS) + eps);
+    s_rr[threadIdx.y][n4] = rr;
+    rrms[static_cast<int64_t>(m) * HC + n4] = rr;
+  }
+  __syncthreads();
+  if (!live || n4 * 4 >= np) return;
+  const int n = n4 * 4;
   const float inv_hc = 1.0f / static_cast<float>(HC);
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n4; i += stride) {
-    float4 acc = reinterpret_cast<const float4*>(part)[i];
-    for (int s = 1; s < HC; ++s) {
-      const float4 v = reinterpret_cast<const float4*>(part)[s * n4 + i];
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int ss = 0; ss < HC; ++ss) {
+    const float rs = s_rr[threadIdx.y][ss];
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int c = 0; c < S; ++c) {
+      const float4 v = *reinterpret_cast<const float4*>(
+          part + (static_cast<int64_t>(ss * S + c) * M + m) * np + n);
+      a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
     }
-    reinterpret_cast<float4*>(lora)[i] = acc;
+    acc.x = fmaf(rs, a.x, acc.x); acc.y = fmaf(rs, a.y, acc.y);
+    acc.z = fmaf(rs, a.z, acc.z); acc.w = fmaf(rs, a.w, acc.w);
+  }
+  if (n < r) {
+    *reinterpret_cast<float4*>(lora + static_cast<int64_t>(m) * r + n) = acc;
     const float u0 = acc.x * inv_hc, u1 = acc.y * inv_hc, u2 = acc.z * inv_hc, u3 = acc.w * inv_hc;
     uint2 hv;
     hv.x = pack2(u0 * sigmoidf_dev(u0), u1 * sigmoidf_dev(u1));
     hv.y = pack2(u2 * sigmoidf_dev(u2), u3 * sigmoidf_dev(u3));
-    reinterpret_cast<uint2*>(h)[i] = hv;
-  }
-  const int64_t ni = M * HC;
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < ni; i += stride) {
-    float acc = inj_part[i];
-    for (int s = 1; s < HC; ++s) acc += inj_part[s * ni + i];
-    inj_next[i] = acc;
+    *reinterpret_cast<uint2*>(h + static_cast<int64_t>(m) * r + n) = hv;
+  } else {
+    const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (n + e - r < HC) inj_next[static_cast<int64_t>(m) * HC + (n + e - r)] = vals[e];
   }
 }
 
@@ -688,14 +725,28 @@ bool prefill_supported(const Call& c) {
 }
 static_assert(k2_ncu(4) * 4 == 128 && k2_ncu(8) * 8 == 128, "K2 N = 128 for the workloads");
 
+
+// K chunks per stream: enough (tile, stream, chunk) CTAs to cover the SMs
+// when there are few token tiles, at least two K blocks per chunk.
+int k1_chunks(int n_mt, int HC, int nkb, int sms) {
+  if (HC * n_mt >= sms) return 1;
+  const int want = (sms + HC * n_mt / 2) / (HC * n_mt);
+  return std::max(1, std::min(want, nkb / 2));
+}
+
+int k1_np(int r, int HC) { return (r + HC + 3) / 4 * 4; }
+
 }  // namespace
 
 size_t prefill_ws_bytes(int64_t max_M, int HC, int HS, int r) {
-  (void)HS;
-  const size_t part = static_cast<size_t>(HC) * max_M * r * 4;
-  const size_t injp = static_cast<size_t>(HC) * max_M * HC * 4;
+  // the largest partial buffer over M <= max_M: split-K only for small M,
+  // where HC * S * M stays below a few hundred tiles of rows
+  size_t part = static_cast<size_t>(HC) * max_M * k1_np(r, HC);
+  part = std::max(part, static_cast<size_t>(2 * MAX_GRID) * BM * k1_np(r, HC));
+  const size_t sumsq = std::max(static_cast<size_t>(HC) * max_M, static_cast<size_t>(2 * MAX_GRID) * BM);
   const size_t h = static_cast<size_t>(max_M) * r * 2;
-  return part + 256 + injp + 256 + h + 256;
+  (void)HS;
+  return part * 4 + 256 + sumsq * 4 + 256 + h + 256;
 }
 
 cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev,
@@ -704,12 +755,20 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   if (prefill_ws_bytes(c.M, c.HC, c.HS, c.r) > ws.prefill_bytes) return cudaErrorNotSupported;
   const int M = static_cast<int>(c.M);
   const int n_mt = (M + BM - 1) / BM;
+  const int nkb = c.HS / BK;
+  const int S = k1_chunks(n_mt, c.HC, nkb, dev.sms);
+  const int np = k1_np(c.r, c.HC);
+  const size_t part_floats = static_cast<size_t>(c.HC) * S * M * np;
+  if (part_floats > std::max(static_cast<size_t>(c.HC) * M * np,
+                             static_cast<size_t>(2 * MAX_GRID) * BM * np))
+    return cudaErrorNotSupported;
   // workspace carve-up (sized by prefill_ws_bytes for max_M)
   float* part = ws.k1_part;
-  float* inj_part = reinterpret_cast<float*>(
-      reinterpret_cast<unsigned char*>(part) + ((static_cast<size_t>(c.HC) * M * c.r * 4 + 255) / 256) * 256);
-  bf16_t* h = reinterpret_cast<bf16_t*>(
-      reinterpret_cast<unsigned char*>(inj_part) + ((static_cast<size_t>(c.HC) * M * c.HC * 4 + 255) / 256) * 256);
+  float* sumsq = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(part) +
+                                          (part_floats * 4 + 255) / 256 * 256);
+  const size_t sumsq_floats = static_cast<size_t>(c.HC) * S * M;
+  bf16_t* h = reinterpret_cast<bf16_t*>(reinterpret_cast<unsigned char*>(sumsq) +
+                                        (sumsq_floats * 4 + 255) / 256 * 256);
 
   // ---------------- K1
   {
@@ -736,16 +795,16 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.ld_inj = c.ld_inj;
     p.R2 = c.R2;
     p.Wnorm = c.Wnorm;
-    p.rrms = c.rrms;
     p.part = part;
-    p.inj_part = inj_part;
+    p.sumsq = sumsq;
     p.M = M;
     p.HS = c.HS;
     p.K = c.K;
     p.r = c.r;
+    p.np = np;
     p.fold = c.fold;
-    p.eps = c.eps;
-    p.nkb = c.HS / BK;
+    p.S = S;
+    p.nkb = nkb;
     // MMA column blocks over the B tile (r rows of Wd, then 16 inject rows)
     const int ntot = c.r + (inj_mma ? WI_ROWS : 0);
     if (ntot <= 256) {
@@ -766,7 +825,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const size_t smem = L.total + 1024;
     if (smem > static_cast<size_t>(dev.smem_optin)) return cudaErrorNotSupported;
     cudaError_t e = cudaSuccess;
-    const int grid = n_mt * c.HC;
+    const int grid = n_mt * c.HC * S;
 #define HCGR_K1(HCV)                                                                        \
   case HCV:                                                                                 \
     e = inj_mma ? launch_k1<HCV, true>(p, grid, smem, dev, stream)                          \
@@ -782,10 +841,9 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   }
   // ---------------- reduce
   {
-    const int64_t n4 = c.M * c.r / 4;
-    const int blocks = static_cast<int>(std::min<int64_t>((n4 + 255) / 256, dev.sms * 8));
-    k1_reduce_kernel<<<std::max(blocks, 1), 256, 0, stream>>>(part, inj_part, c.lora, c.inj_next, h,
-                                                             c.M, c.HC, c.r);
+    const dim3 block((np / 4 + 31) / 32 * 32, RED_ROWS);
+    k1_reduce_kernel<<<(M + RED_ROWS - 1) / RED_ROWS, block, 0, stream>>>(
+        part, sumsq, c.rrms, c.lora, c.inj_next, h, M, c.HC, S, c.r, np, c.HS, c.eps);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
