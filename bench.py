@@ -39,6 +39,28 @@ ACT_BYTES_PER_TOKEN = (2 * K_DIM + 2 * HS + 4 * HC + 2 * K_DIM + 4 * HC + 4 * HC
                        + 4 * R_LOW + 2 * HS)                                   # R y inj R2 rrms inj_next lora x
 FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 
+# DRAM bytes (read + write) of one decode_kernel launch per M, from one ncu
+# capture (dram__bytes_read.sum + dram__bytes_write.sum, profiles/
+# decode_kernel_dram_per_M.md).  They hold only for the kernel sources they
+# were taken on: if those changed since, roofline.traffic is null.
+DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
+DECODE_TRAFFIC = {
+    "sources_sha256": "9ce216b552212966cf7809e17106c05170dce2b3d29a42a7750f7726982a2bf1",
+    "bytes": {2: 13348096, 4: 13399808, 8: 13501952, 16: 13707520, 32: 14121216},
+}
+
+
+def decode_traffic_per_launch():
+    """Mean measured DRAM bytes per launch over the sweep, or None if stale."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "hyper_connection_gated_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != DECODE_TRAFFIC["sources_sha256"]:
+        return None
+    return sum(DECODE_TRAFFIC["bytes"][M] for M in SWEEP) / len(SWEEP)
+
 
 def peaks():
     try:
@@ -303,8 +325,9 @@ def run_ours(args, rank, world):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": len(SWEEP) * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
-                     "kernel": "decode_kernel (per launch: weights + activations)",
+                     "frac": achieved / hbm, "traffic": decode_traffic_per_launch(),
+                     "algorithmic_bytes_per_launch": alg_bytes / len(SWEEP),
+                     "kernel": "decode_kernel (per launch, mean over the sweep: weights + activations)",
                      "peak_source": peak_src},
         "per_M_us": {str(M): per_m[M] for M in SWEEP},
         "per_M_roofline_frac": {str(M): (WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN) / hbm / 1e3
