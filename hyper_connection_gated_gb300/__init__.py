@@ -45,12 +45,15 @@ class HcGatedResidual:
     def forward(self, R, y, inj, Wnorm, Wu, Wd=None, Wi=None, Wdi=None, fold_w=False,
                 eps: float = 1e-6, out: dict | None = None, want_lora: bool = True,
                 stream=None, force_path: int = PATH_AUTO, debug_fault: int = 0,
-                check: bool = False) -> dict:
+                pdl: bool = False, check: bool = False) -> dict:
         """Runs the whole forward pass; returns the output tensors.
 
         R [M, HC, HS] bf16, y [M, HS] bf16, inj [M, HC] fp32 (rows may be
         strided), Wnorm [K] bf16, Wu [K, r] bf16, and either Wd [r, K] + Wi
         [HC, K] or a merged Wdi [n_pad, K] (fold_w: (1 + Wnorm) folded in).
+        pdl: let the decode kernel start its weight copies before the
+        previous kernel on the stream has finished (that kernel must not
+        write the weights).
         """
         import torch
 
@@ -90,7 +93,7 @@ class HcGatedResidual:
         a.R2, a.rrms, a.inj_next, a.x = (out["R2"].data_ptr(), out["rrms"].data_ptr(),
                                          out["inj_next"].data_ptr(), out["x"].data_ptr())
         a.lora = out["lora"].data_ptr() if out.get("lora") is not None else None
-        a.force_path, a.debug_fault = force_path, debug_fault
+        a.force_path, a.debug_fault, a.pdl = force_path, debug_fault, 1 if pdl else 0
         s = stream if stream is not None else torch.cuda.current_stream(dev)
         st = self._lib.hc_gr_forward_ex(self._h, ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
         if st != OK:

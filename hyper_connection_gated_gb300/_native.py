@@ -34,6 +34,7 @@ class Args(ctypes.Structure):
         ("n_pad", ctypes.c_int32), ("fold_w", ctypes.c_int32),
         ("Wu", _vp), ("R2", _vp), ("rrms", _fp), ("inj_next", _fp), ("x", _vp), ("lora", _fp),
         ("force_path", ctypes.c_int32), ("debug_fault", ctypes.c_int32),
+        ("pdl", ctypes.c_int32),
     ]
 
 

@@ -1,34 +1,50 @@
-// Decode path of the HC gated residual: one cooperative persistent kernel for
-// small token counts (M <= 32), where the time goes into streaming the
-// weights once (aiter PR #5913, "Technical Details"; the page's skinny decode
-// with split-K partials and a last-stage reduce is the prior art).
+// Decode path of the HC gated residual: one persistent kernel for small token
+// counts (M <= 32), where the time goes into streaming the weights once
+// (aiter PR #5913, "Technical Details"; the page's skinny decode with split-K
+// partials and a last-stage reduce is the prior art).
 //
-// Grid: G = HC * P CTAs (at most one per SM), three phases separated by two
-// bounded grid barriers:
-//   1. CTA b owns a channel slice [c0, c0 + w) of one stream s (every slice
-//      has the same width w; the stream end clips the last one).  It forms
-//      R2 = bf16(R + y * iw) for the slice (stored), the partial sum of R2^2
-//      per token and, on the tensor cores (mma.sync bf16, fp32 accumulate),
-//        part[b][m][n] = sum_{c in slice} a[m, c] * W[n, s * HS + c]
-//      for all r + HC rows of the down and inject weights, with a = R2 *
-//      (1 + Wnorm) split into two bf16 terms (hi + lo, ~16 mantissa bits) or
-//      a = R2 for a folded weight.  Because rrms_s is constant over stream s,
-//      lora = sum_b rrms_{s(b)} part[b] is exact: the per-stream factor
-//      commutes out of the K-sum.
-//   2. One TMA box brings CTA b's share of the outputs from every partial
-//      (and the partial sums of squares) into shared memory: rrms, then lora
-//      and inj_next as rrms-weighted sums in a fixed order (deterministic).
-//   3. One bulk copy brings lora; h = SiLU(lora / HC) in bf16; the gates
-//      G[s, c] = sigmoid(h . Wu[s * HS + c]) for the CTA's channel range and
-//      all streams on the tensor cores; xn is rebuilt from R2 (recomputed
-//      from R, y and inj prefetched at kernel start, bit-identical to phase
-//      1), rrms and Wnorm; x = (1 / HC) sum_s G * xn is stored.
-// Weights move as TMA boxes issued at kernel start: the down/inject slice as
-// 3-D boxes (the stream is its own tensor dimension, so a box never crosses
-// a stream end), the up-weight rows of the channel range as 3-D boxes with
-// 128-byte swizzle (bank-conflict-free fragment loads).  When everything
-// fits in shared memory the whole weight stream is in flight before the
-// first barrier; otherwise both stream through two-slot rings.
+// Grid: G CTAs; CTA b owns the channel slice [c0, c0 + 64 nkc) of stream
+// s = b / P (P slices per stream; the stream end clips the last one).
+//   1. COMBINE on the slice: R2 = bf16(R + y * iw) (stored), the partial sum
+//      of R2^2 per token, and the MMA operand a = R2 * (1 + Wnorm) split into
+//      two bf16 terms (hi + lo, ~16 mantissa bits), or a = R2 for a folded
+//      weight, written to shared memory in the 128-byte swizzled K-major
+//      layout of a tcgen05 operand.
+//   2. On the tensor cores (tcgen05.mma, fp32 accumulators in TMEM), for
+//      every 128-row tile of the down/inject weight (TMA, 128-byte swizzle):
+//      D[n][m] = sum_{c in slice} W[n, s HS + c] a[m, c].  The hi and lo
+//      terms are stacked as the two halves of the MMA's N dimension (one MMA
+//      per weight tile and k-step), and two threads issue, each for alternate
+//      64-column chunks into its own accumulator copy.
+//      rrms_s is constant over stream s, so lora = sum_s rrms_s sum_{b in s}
+//      D_b is exact: the per-stream factor commutes out of the K-sum.
+//   3. Reduce-scatter: the M (r + HC) outputs are cut into blocks of Qn
+//      outputs of one token.  Every CTA writes its piece of every block, plus
+//      its sum of squares, to a global exchange buffer straight from TMEM; the
+//      block's reducer (CTA j mod G) sums the pieces in a fixed order
+//      (deterministic) and forms rrms, lora, inj_next and
+//      h = bf16(SiLU(lora / HC)).
+//   4. All-gather: the reducers publish h and rrms to a second exchange
+//      buffer; every CTA reads all of it into the swizzled operand layout,
+//      forms the gates G[s, c] = sigmoid(Wu[s HS + c] . h) for its channel
+//      range and every stream on the tensor cores, rebuilds xn from R2
+//      (recomputed from R, y and inj bit-identically to step 1), rrms and
+//      Wnorm, and stores x = (1 / HC) sum_s G * xn.
+// The exchanges need no grid barrier.  Every 32-bit word of an exchange
+// buffer is either the empty marker 0xffffffff or a value, and a reader spins
+// (bounded in time) on each word until it holds a value.  A value never equals
+// the marker: floats are stored with NaN canonicalised, and h as a pair of
+// bf16 from the rounding conversion, whose NaN is 0x7fff.  The reduce-scatter
+// buffer is emptied again by its single reader; the all-gather buffer
+// alternates between two copies by call parity (a ticket counter), and each
+// call empties the copy the next call will use.
+//
+// Weights move as TMA boxes issued at kernel start; when they do not all fit
+// in shared memory they stream through rings whose slots the MMA thread hands
+// back with tcgen05.commit.  With a programmatic dependent launch the weight
+// copies start before the previous kernel in the stream has finished;
+// activations are read, and outputs written, only after it has.  The kernel is
+// short enough that instruction fetch matters: loops stay rolled.
 #include <algorithm>
 
 #include "hc_gr_internal.cuh"
@@ -37,128 +53,148 @@
 namespace hcgr {
 namespace {
 
-constexpr int NT = 512;            // threads per CTA
+constexpr int NT = 256;              // threads per CTA
 constexpr int NW = NT / 32;
-constexpr int MAX_SLOTS = 8;
-constexpr int MAXP = 8;            // (row tile, token tile) pairs per warp in phase 3
-constexpr int BOX_CAP = 32 * 1024; // bytes per down/inject weight box
-constexpr int SMEM_BUDGET = 216 * 1024;
+constexpr int MAX_SLOTS = 8;         // ring slots per weight stream
+constexpr int XU = 8;                // exchange loads a thread keeps in flight
+constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
+constexpr int HDR = 512;             // mbarriers, TMEM address, flags
+constexpr int SMEM_BUDGET = 220 * 1024;
 constexpr int SMEM_ALLOC = SMEM_BUDGET + 1024;
 
 struct Geom {
-  int MB;                                   // M rounded up to 8 (MMA token tiles)
-  int G, P, w, nch_max;                     // phase 1: P slices of w channels per stream
-  int nbox, rows_box, slot_w, nslot_w;      // down weight boxes
-  int nc_max, rows_u, rows_u16, nchunk_u, slot_u, nslot_u;   // up weight chunks (64 columns)
-  int Q, part_ld, ss_bytes;                 // phase 2
-  int hstride;                              // bf16 elements per h row in shared memory
-  int off_rr, off_iw, off_x3r, off_x3y, off_x3w, off_wi, off_u, off_un;
-  int off_w, off_ahi, off_alo, off_ss1;     // phase 1 (union region)
-  int off_pbox, off_ss;                     // phase 2 (union region)
-  int off_red;                              // phase 2 (union region)
-  int off_h, off_g;                         // phase 3 (union region)
+  int Nt, Nd, Nu;                 // tokens rounded to 8; down MMA N (hi + lo); up MMA N
+  int nkc, P, G;                  // 64-column chunks per slice, slices per stream, CTAs
+  int merged, rows_w, tail, wi_shared, wi_tile, wi_row, ntd, nsl_w;   // down weight
+  int nc_max, rows_u, ntu, nchunk_u, slot_u, nsl_u;                    // up weight
+  int Qn, Jm, nred, row, nquad, R, ppr, L2w;                           // exchanges
+  int tmem_cols;
+  int off_rr, off_iw, off_x3r, off_x3y, off_x3w, off_ssum, off_ss1, off_rl, off_act, off_u,
+      off_a;                      // (off_act: [nkc][Nd rows][128 B], hi rows then lo rows)
+  int off_acc, off_red, off_hb, off_g;   // region A once the down weights are consumed
   int total;
 };
 
 __host__ __device__ inline int round_up(int v, int a) { return (v + a - 1) / a * a; }
 
 struct Params {
-  CUtensorMap tm_wd;    // Wd as [r][HC][HS] (inner HS), box {w, 1, rows_box}
-  CUtensorMap tm_wi;    // Wi as [HC][HC][HS], box {w, 1, HC}
-  CUtensorMap tm_wu;    // Wu as [HC][HS][r] (inner r), box {64, nc_max, HC}, 128B swizzle
-  CUtensorMap tm_part;  // partials [G][part_ld] fp32, box {Q, G}
+  CUtensorMap tm_w;     // down weight (Wd, or merged Wdi) as [rows][HC][HS], box {64, 1, 128}
+  CUtensorMap tm_wt;    // Wd's last rows when Wi shares their tile, box {64, 1, tail}
+  CUtensorMap tm_wi;    // Wi as [HC][HC][HS], box {64, 1, HC}
+  CUtensorMap tm_wu;    // Wu as [HC][HS][r], box {64, nc_max, HC}
   Call c;
   Geom g;
-  float* part;
-  float* sumsq;
-  bf16_t* hdec;              // h = bf16(SiLU(lora / HC)), written in phase 2
-  unsigned long long* bar;   // this grid size's barrier counter
+  uint32_t* xred;       // reduce-scatter words [nred][G][row]
+  uint32_t* xgat;       // all-gather words, two copies of gat_words
+  int gat_words;
+  unsigned long long* ticket;
   int* err;
   uint64_t limit_ns;
 };
 
 bool layout(const Call& c, Geom& g) {
-  int off = 256;                                       // mbarriers + flag
-  const int MB = g.MB;
-  g.off_rr = off;   off += round_up(MB * c.HC * 4, 128);
-  g.off_iw = off;   off += round_up(MB * c.HC * 4, 128);
-  g.off_x3r = off;  off += round_up(MB * c.HC * g.nc_max * 2, 128);
-  g.off_x3y = off;  off += round_up(MB * g.nc_max * 2, 128);
+  const int M = static_cast<int>(c.M), Nt = g.Nt;
+  int off = HDR;
+  g.off_rr = off;   off += round_up(Nt * c.HC * 4, 128);
+  g.off_iw = off;   off += round_up(Nt * c.HC * 4, 128);
+  g.off_x3r = off;  off += round_up(M * c.HC * g.nc_max * 2, 128);
+  g.off_x3y = off;  off += round_up(M * g.nc_max * 2, 128);
   g.off_x3w = off;  off += round_up(c.HC * g.nc_max * 2, 128);
-  g.off_wi = off;   off += round_up(16 * g.w * 2, 128);
+  g.off_ssum = off; off += round_up(Nt * 4, 128);
+  g.off_ss1 = off;  off += round_up(Nt * g.nkc * 8 * 4, 128);
+  g.off_rl = off;   off += round_up(c.HC * 4, 128);
   off = round_up(off, 1024);
-  g.off_u = off;    off += g.nslot_u * g.slot_u;
-  g.off_un = off;
-  // phase 1
-  int p1 = off;
-  g.off_w = p1;     p1 += g.nslot_w * g.slot_w;
-  g.off_ahi = p1;   p1 += round_up(MB * g.w * 2, 128);
-  g.off_alo = p1;   p1 += round_up(MB * g.w * 2, 128);
-  g.off_ss1 = p1;   p1 += round_up(MB * g.nch_max * 4, 128);
-  // phase 2
-  int p2 = off;
-  g.off_pbox = p2;  p2 += round_up(g.G * g.Q * 4, 128);
-  g.off_ss = p2;    p2 += round_up(g.ss_bytes, 128);
-  g.off_red = p2;   p2 += round_up(g.Q * c.HC * 4, 128);
-  // phase 3
-  int p3 = off;
-  g.off_h = p3;     p3 += round_up(MB * g.hstride * 2, 128);
-  g.off_g = p3;     p3 += round_up(MB * g.rows_u * 4, 128);
-  g.total = std::max(p1, std::max(p2, p3));
+  g.off_act = off;  off += g.nkc * g.Nd * 128;
+  g.off_u = off;    off += g.nsl_u * g.slot_u;
+  g.off_a = off;
+  const int pw = g.nsl_w * TILE;
+  const int acc_bytes = round_up(c.HC * g.R * g.row * 4, 128);
+  g.off_acc = off;
+  g.off_red = off + acc_bytes;
+  const int pr = acc_bytes + round_up(c.HC * g.row * 4, 128);
+  g.off_hb = off;
+  g.off_g = off + g.nchunk_u * g.Nu * 128;
+  const int pg = g.nchunk_u * g.Nu * 128 + round_up(M * g.rows_u * 4, 128);
+  // the up-weight A tiles read ntu * TILE bytes from a slot's start: the
+  // region after the last slot covers the overhang
+  const int over = g.ntu * TILE - g.slot_u;
+  g.total = off + std::max(std::max(pw, pr), std::max(pg, over));
   return g.total <= SMEM_BUDGET;
 }
 
 bool make_geom(const Call& c, const Device& dev, Geom& g) {
   const int M = static_cast<int>(c.M);
-  g.MB = round_up(M, 8);
-  const int P0 = std::max(1, dev.sms / c.HC);
-  int w = round_up((c.HS + P0 - 1) / P0, 8);
-  if (((w / 8) & 1) == 0 && w + 8 <= c.HS) w += 8;   // odd 16-byte units: no bank conflicts
-  w = std::min(w, c.HS);
-  if (w > 256) return false;
-  g.w = w;
-  g.P = (c.HS + w - 1) / w;
-  g.G = c.HC * g.P;
-  if (g.G > dev.sms) return false;
-  g.nch_max = w / 8;
-  g.nc_max = (c.HS + g.G - 1) / g.G;
-  g.rows_u = c.HC * g.nc_max;
-  g.rows_u16 = round_up(g.rows_u, 16);
-  if (g.rows_u16 > 256 || (g.rows_u16 / 16) * (g.MB / 8) > NW * MAXP) return false;
+  if (M < 1 || M > DECODE_MAX_M || c.HS % 64 != 0 || c.r % 8 != 0 || c.HC > 8) return false;
+  g.Nt = round_up(M, 8);
+  g.Nd = 2 * g.Nt;
+  g.Nu = round_up(M, 16);
+  g.merged = c.Wi == c.Wd + static_cast<int64_t>(c.r) * c.K;   // rows r.. follow in one tensor
+  g.rows_w = g.merged ? c.n_out : c.r;
+  g.tail = g.rows_w % 128;
+  const int nwd = (g.rows_w + 127) / 128;
+  g.wi_shared = !g.merged && g.tail != 0 && g.tail + c.HC <= 128;
+  g.wi_tile = g.merged ? -1 : (g.wi_shared ? nwd - 1 : nwd);
+  g.wi_row = g.wi_shared ? g.tail : 0;
+  g.ntd = g.merged || g.wi_shared ? nwd : nwd + 1;
   g.nchunk_u = (c.r + 63) / 64;
-  g.slot_u = round_up(g.rows_u16 * 128, 1024);
-  const int n_out = c.n_out;
-  g.Q = round_up((M * n_out + g.G - 1) / g.G, 4);
-  if (g.Q > 256) return false;
-  g.part_ld = round_up(M * n_out, 4);
-  g.ss_bytes = round_up(g.G * M * 4, 16);
-  g.hstride = round_up(c.r, 8) + 8;
-  // down weight boxes: rows a multiple of 16 (one MMA row tile never spans boxes)
-  g.nbox = std::max(1, (c.r * w * 2 + BOX_CAP - 1) / BOX_CAP);
-  g.rows_box = round_up((c.r + g.nbox - 1) / g.nbox, 16);
-  while (g.rows_box > 256) {
-    ++g.nbox;
-    g.rows_box = round_up((c.r + g.nbox - 1) / g.nbox, 16);
-  }
-  g.nbox = (c.r + g.rows_box - 1) / g.rows_box;
-  g.slot_w = round_up(g.rows_box * w * 2, 128);
-  // everything resident when it fits, else two-slot rings
-  g.nslot_w = g.nbox;
-  g.nslot_u = g.nchunk_u;
-  if (g.nbox <= MAX_SLOTS && g.nchunk_u <= MAX_SLOTS && layout(c, g)) return true;
-  g.nslot_u = std::min(g.nchunk_u, 2);
-  for (int rows = std::min(256, round_up(c.r, 16)); rows >= 16; rows -= 16) {
-    g.rows_box = rows;
-    g.nbox = (c.r + rows - 1) / rows;
-    g.slot_w = round_up(rows * w * 2, 128);
-    g.nslot_w = std::min(g.nbox, 2);
-    if (layout(c, g)) return true;
+  const int hsc = c.HS / 64;                            // 64-column chunks per stream
+  for (g.nkc = 1; g.nkc <= hsc; ++g.nkc) {
+    g.P = (hsc + g.nkc - 1) / g.nkc;
+    g.G = c.HC * g.P;
+    if (g.G > MAX_GRID) continue;
+    g.nc_max = round_up((c.HS + g.G - 1) / g.G, 2);
+    g.rows_u = c.HC * g.nc_max;
+    if (g.nc_max > 256 || g.rows_u > 256) continue;
+    g.ntu = (g.rows_u + 127) / 128;
+    g.slot_u = round_up(g.rows_u * 128, 1024);
+    for (g.Qn = 4;; g.Qn += 4) {
+      g.Jm = (c.n_out + g.Qn - 1) / g.Qn;
+      if (M * g.Jm <= g.G || g.Jm == 1) break;
+    }
+    g.nred = M * g.Jm;
+    g.row = g.Qn + 4;                       // Qn partials, the sum of squares, 3 pad words
+    g.nquad = g.row / 4;
+    if (g.nquad > NT) return false;
+    // reducer: R sub-ranges of ppr pieces per stream and quad
+    g.R = std::max(1, NT / (c.HC * g.nquad));
+    g.ppr = (g.P + g.R - 1) / g.R;
+    g.L2w = round_up(c.r / 2 + c.HC, 4);     // h pairs, then rrms, then pad words
+    // two accumulator copies (one per issuing thread) for each product
+    const int cols = std::max(2 * g.ntd * g.Nd, 2 * g.ntu * g.Nu);
+    if (cols > 512) return false;
+    g.tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+    // all weight tiles resident when they fit, else rings
+    const int nbox = g.ntd * g.nkc;
+    bool fits = false;
+    for (int ring = 0; ring < 2 && !fits; ++ring) {
+      g.nsl_w = ring ? std::min(nbox, 4) : nbox;
+      g.nsl_u = ring ? std::min(g.nchunk_u, 2) : g.nchunk_u;
+      if (g.nsl_w > MAX_SLOTS || g.nsl_u > MAX_SLOTS) continue;
+      fits = layout(c, g);
+    }
+    // a kernel that allocates TMEM runs one CTA per SM
+    if (fits && g.G <= dev.sms) return true;
   }
   return false;
 }
 
-__device__ __forceinline__ uint32_t lds32(const unsigned char* p) {
-  return *reinterpret_cast<const uint32_t*>(p);
+// Out-of-line slow paths of the bounded waits: one copy of each wait loop
+// however many call sites.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, int* err, uint64_t limit_ns) {
+  return mbar_wait_bounded(bar, parity, err, limit_ns);
+}
+// A wait that ignores the status word (copies and MMAs always finish; this
+// only lets them land before the CTA leaves), bounded by the time limit.
+__device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity) && clock64() - t0 < limit) {
+  }
+}
+// Four exchange words, waited for; on failure some word is still empty.
+__device__ __noinline__ uint4 wait_words(const uint32_t* p, int* err, long long limit) {
+  uint4 v;
+  xwait4(p, v, err, limit);
+  return v;
 }
 
 // --------------------------------------------------------------- the kernel
@@ -169,84 +205,120 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   const Call& c = p.c;
   const Geom& g = p.g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int gq = lane >> 2, tq = lane & 3;       // MMA fragment coordinates
   const int b = blockIdx.x;
-  const int M = static_cast<int>(c.M), MB = g.MB;
-  const int HC = c.HC, HS = c.HS, K = c.K, r = c.r, n_out = c.n_out, w = g.w;
-  const int ntok = MB / 8;
+  const int M = static_cast<int>(c.M), Nt = g.Nt, Nd = g.Nd, Nu = g.Nu;
+  const int HC = c.HC, HS = c.HS, K = c.K, r = c.r, n_out = c.n_out;
+  const long long limit = wait_limit_cycles(p.limit_ns);
 
-  int* s_flag = reinterpret_cast<int*>(smem + 240);
-  float* s_rr = reinterpret_cast<float*>(smem + g.off_rr);     // [MB][HC]
-  float* s_iw = reinterpret_cast<float*>(smem + g.off_iw);     // [MB][HC]
+  const uint32_t bar0 = smem_u32(smem);
+  auto full_w = [&](int i) { return bar0 + 8u * i; };
+  auto free_w = [&](int i) { return bar0 + 64u + 8u * i; };
+  auto full_u = [&](int i) { return bar0 + 128u + 8u * i; };
+  auto free_u = [&](int i) { return bar0 + 192u + 8u * i; };
+  const uint32_t barD = bar0 + 256u, barG = bar0 + 264u;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 272);
+  uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + 276);
+  int* s_mma_ok = reinterpret_cast<int*>(smem + 280);
+  float* s_rr = reinterpret_cast<float*>(smem + g.off_rr);     // [Nt][HC] rrms (all-gather)
+  float* s_iw = reinterpret_cast<float*>(smem + g.off_iw);     // [Nt][HC]
   bf16_t* s_x3r = reinterpret_cast<bf16_t*>(smem + g.off_x3r); // [M][HC][nc_max]
   bf16_t* s_x3y = reinterpret_cast<bf16_t*>(smem + g.off_x3y); // [M][nc_max]
   bf16_t* s_x3w = reinterpret_cast<bf16_t*>(smem + g.off_x3w); // [HC][nc_max]
-  bf16_t* s_ahi = reinterpret_cast<bf16_t*>(smem + g.off_ahi); // [MB][w]
-  bf16_t* s_alo = reinterpret_cast<bf16_t*>(smem + g.off_alo);
-  float* s_ss1 = reinterpret_cast<float*>(smem + g.off_ss1);   // [MB][nch_max]
-  float* s_pbox = reinterpret_cast<float*>(smem + g.off_pbox); // [G][Q]
-  float* s_ss = reinterpret_cast<float*>(smem + g.off_ss);     // [G][M]
-  float* s_red = reinterpret_cast<float*>(smem + g.off_red);   // [HC][Q]
-  bf16_t* s_h = reinterpret_cast<bf16_t*>(smem + g.off_h);     // [MB][hstride]
-  float* s_g = reinterpret_cast<float*>(smem + g.off_g);       // [MB][rows_u]
+  float* s_ssum = reinterpret_cast<float*>(smem + g.off_ssum); // [Nt] sum of R2^2 on the slice
+  float* s_ss1 = reinterpret_cast<float*>(smem + g.off_ss1);   // [Nt][8 nkc]
+  float* s_rl = reinterpret_cast<float*>(smem + g.off_rl);     // [HC] the reducer's rrms
+  float* s_acc = reinterpret_cast<float*>(smem + g.off_acc);   // [HC][R][row]
+  float* s_red = reinterpret_cast<float*>(smem + g.off_red);   // [HC][row]
+  float* s_g = reinterpret_cast<float*>(smem + g.off_g);       // [M][rows_u]
+  const uint32_t act = smem_u32(smem + g.off_act);             // [nkc][Nd rows][128 B]
+  const uint32_t wbase = smem_u32(smem + g.off_a);             // down weight slots
+  const uint32_t ubase = smem_u32(smem + g.off_u);             // up weight slots
+  const uint32_t hbase = smem_u32(smem + g.off_hb);            // [nchunk_u][Nu rows][128 B]
 
-  // phase-1 slice and phase-3 channel range of this CTA
+  // this CTA's slice (step 1) and channel range (step 4)
   const int s = b / g.P;
-  const int c0 = (b % g.P) * w;
-  const int nch = (min(HS, c0 + w) - c0) / 8;
+  const int c0 = (b % g.P) * 64 * g.nkc;
+  const int nkv = min(g.nkc, (HS - c0) / 64);                  // chunks of the slice
   const int k0 = s * HS + c0;
   const int cp0 = min(HS, b * g.nc_max);
   const int nc = min(HS, cp0 + g.nc_max) - cp0;
+  const int nbox = g.ntd * nkv;                                // down weight boxes
+  const int nub = nc > 0 ? g.nchunk_u : 0;                     // up weight boxes
 
-  const uint32_t bar0 = smem_u32(smem);
-  auto barW = [&](int i) { return bar0 + 8u * i; };               // slots 0..7
-  auto barU = [&](int i) { return bar0 + 64u + 8u * i; };         // slots 8..15
-  const uint32_t barWi = bar0 + 128u, barP = bar0 + 136u, barL = bar0 + 144u;
-
-  if (tid == 0) {
-    prefetch_tmap(&p.tm_wd);
-    prefetch_tmap(&p.tm_wi);
-    prefetch_tmap(&p.tm_wu);
-    prefetch_tmap(&p.tm_part);
-    for (int i = 0; i < 19; ++i) mbar_init(bar0 + 8u * i, 1);
-    fence_mbar_init();
-  }
-  __syncthreads();
-
-  auto issue_w = [&](int bx) {
-    const int slot = bx % g.nslot_w;
-    mbar_arrive_expect_tx(barW(slot), static_cast<uint32_t>(g.rows_box * w * 2));
-    tma_load_3d(smem_u32(smem + g.off_w + slot * g.slot_w), &p.tm_wd, c0, s, bx * g.rows_box,
-                barW(slot));
+  auto issue_w = [&](int i) {   // box i: chunk i / ntd, row tile i % ntd
+    const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
+    const uint32_t dst = wbase + slot * TILE;
+    const int x = c0 + ch * 64;
+    const bool wd = t * 128 < g.rows_w;
+    const bool wt = wd && g.wi_shared && t == g.wi_tile;
+    const bool wi = t == g.wi_tile;
+    const uint32_t bytes = (wd ? (wt ? g.tail : 128) * 128 : 0) + (wi ? HC * 128 : 0);
+    mbar_arrive_expect_tx(full_w(slot), bytes);
+    if (wd) tma_load_3d(dst, wt ? &p.tm_wt : &p.tm_w, x, s, t * 128, full_w(slot));
+    if (wi) tma_load_3d(dst + g.wi_row * 128, &p.tm_wi, x, s, 0, full_w(slot));
   };
   auto issue_u = [&](int q) {
-    const int slot = q % g.nslot_u;
-    mbar_arrive_expect_tx(barU(slot), static_cast<uint32_t>(g.rows_u * 128));
-    tma_load_3d(smem_u32(smem + g.off_u + slot * g.slot_u), &p.tm_wu, q * 64, cp0, 0, barU(slot));
+    const int slot = q % g.nsl_u;
+    mbar_arrive_expect_tx(full_u(slot), static_cast<uint32_t>(g.rows_u * 128));
+    tma_load_3d(ubase + slot * g.slot_u, &p.tm_wu, q * 64, cp0, 0, full_u(slot));
   };
-  int issued_w = 0, issued_u = 0, done_w = 0, done_u = 0;   // uniform across the CTA
-  for (; issued_w < g.nslot_w; ++issued_w)
-    if (tid == 0) issue_w(issued_w);
-  if (tid == 0) {
-    mbar_arrive_expect_tx(barWi, static_cast<uint32_t>(HC * w * 2));
-    tma_load_3d(smem_u32(smem + g.off_wi), &p.tm_wi, c0, s, 0, barWi);
-  }
-  if (nc > 0)
-    for (; issued_u < g.nslot_u; ++issued_u)
-      if (tid == 0) issue_u(issued_u);
 
-  // --- phase 1a: COMBINE on this CTA's slice, R2 stored, MMA operands
-  for (int it = tid; it < MB * g.nch_max; it += NT) {
-    const int m = it / g.nch_max, ch = it % g.nch_max;
+  // Weight copies first (they do not depend on the previous kernel): two
+  // threads each initialise the barriers they arm and start their stream at
+  // once; a third takes the call ticket; warp 3 allocates TMEM meanwhile.
+  const int pre_w = min(g.nsl_w, nbox), pre_u = min(g.nsl_u, nub);
+  int issued_w = pre_w, issued_u = pre_u;   // kept by thread 0, which drains them
+  if (tid == 0) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) mbar_init(full_w(0) + 8u * i, 1);   // full_w, free_w
+    mbar_init(barD, 2);
+    fence_mbar_init();
+    *s_mma_ok = 1;
+    prefetch_tmap(&p.tm_w);
+    if (g.wi_tile >= 0) prefetch_tmap(&p.tm_wi);
+    if (g.wi_shared) prefetch_tmap(&p.tm_wt);
+#pragma unroll 1
+    for (int i = 0; i < pre_w; ++i) issue_w(i);
+  } else if (tid == 32) {
+#pragma unroll 1
+    for (int i = 0; i < 16; ++i) mbar_init(full_u(0) + 8u * i, 1);   // full_u, free_u
+    mbar_init(barG, 2);
+    fence_mbar_init();
+    prefetch_tmap(&p.tm_wu);
+#pragma unroll 1
+    for (int q = 0; q < pre_u; ++q) issue_u(q);
+  } else if (tid == 64) {
+    // arrivals in the low half, the call's epoch in the high half; the last
+    // arrival moves the epoch on and clears the count
+    const unsigned long long old = atomicAdd(p.ticket, 1ull);
+    if ((old & 0xffffffffull) == static_cast<unsigned long long>(g.G - 1))
+      atomicAdd(p.ticket, (1ull << 32) - static_cast<unsigned long long>(g.G));
+    *s_epoch = static_cast<uint32_t>(old >> 32);
+  }
+  if (warp == 3) {
+    tmem_alloc(smem_u32(s_tmem), g.tmem_cols);
+    tmem_relinquish();
+  }
+  // inputs and outputs may belong to the previous kernel in the stream
+  grid_dep_wait();
+
+  // --- step 1: COMBINE on this CTA's slice, R2 stored, MMA operands in the
+  // swizzled layout (16-byte unit u of row m of a chunk at (u ^ (m & 7)) * 16;
+  // hi in rows m, lo in rows Nt + m)
+  const int nu = g.nkc * 8;                                    // 16-byte units per row
+#pragma unroll 1
+  for (int it = tid; it < Nt * nu; it += NT) {
+    const int m = it / nu, un = it - m * nu;
+    const int ch = un >> 3, u = un & 7;
     uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
     float ss = 0.f;
-    if (m < M && ch < nch) {
-      const int64_t kk = static_cast<int64_t>(m) * K + k0 + ch * 8;
+    if (m < M && ch < nkv) {
+      const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
       const float iw = 2.0f * sigmoidf_dev(c.inj[m * c.ld_inj + s] / static_cast<float>(HC));
       float rv[8], yv[8], wv[8], a[8];
       unpack8(__ldg(reinterpret_cast<const uint4*>(c.R + kk)), rv);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + ch * 8)), yv);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + k0 + ch * 8)), wv);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + k0 + un * 8)), wv);
       uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
@@ -267,269 +339,376 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       hv = make_uint4(ph[0], ph[1], ph[2], ph[3]);
       lv = make_uint4(pl[0], pl[1], pl[2], pl[3]);
     }
-    *reinterpret_cast<uint4*>(s_ahi + m * w + ch * 8) = hv;
-    *reinterpret_cast<uint4*>(s_alo + m * w + ch * 8) = lv;
-    s_ss1[m * g.nch_max + ch] = ss;
+    const int sw = ch * Nd * 128 + m * 128 + ((u ^ (m & 7)) << 4);
+    *reinterpret_cast<uint4*>(smem + g.off_act + sw) = hv;
+    *reinterpret_cast<uint4*>(smem + g.off_act + sw + Nt * 128) = lv;
+    s_ss1[m * nu + un] = ss;
   }
-  __syncthreads();
-  if (tid < M) {
-    float ss = 0.f;
-    for (int ch = 0; ch < nch; ++ch) ss += s_ss1[tid * g.nch_max + ch];
-    p.sumsq[b * M + tid] = ss;
-  }
-
-  // --- phase 0: inputs of this CTA's channel range for the final mix (iw,
-  // R, y and Wnorm), one merged index space so a thread's loads overlap
+  // inputs of this CTA's channel range for the final mix: iw, and R, y and
+  // Wnorm in channel pairs, XU loads in flight per thread
   {
-    const int n_iw = M * HC, n_r = M * HC * nc, n_y = M * nc, n_w = HC * nc;
-#pragma unroll 4
-    for (int i = tid; i < n_iw + n_r + n_y + n_w; i += NT) {
-      if (i < n_iw) {
-        s_iw[i] = 2.0f * sigmoidf_dev(c.inj[(i / HC) * c.ld_inj + (i % HC)] / static_cast<float>(HC));
-      } else if (i < n_iw + n_r) {
-        const int j = i - n_iw;
-        const int m = j / (HC * nc), rem = j % (HC * nc), ss = rem / nc, cc = rem % nc;
-        s_x3r[(m * HC + ss) * g.nc_max + cc] =
-            __ldg(c.R + static_cast<int64_t>(m) * K + ss * HS + cp0 + cc);
-      } else if (i < n_iw + n_r + n_y) {
-        const int j = i - n_iw - n_r;
-        const int m = j / nc, cc = j % nc;
-        s_x3y[m * g.nc_max + cc] = __ldg(c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
-      } else {
-        const int j = i - n_iw - n_r - n_y;
-        const int ss = j / nc, cc = j % nc;
-        s_x3w[ss * g.nc_max + cc] = __ldg(c.Wnorm + ss * HS + cp0 + cc);
+    const int np = nc / 2;
+    const int n_iw = M * HC, n_r = M * HC * np, n_y = M * np, n_w = HC * np;
+    const int n_all = n_r + n_y + n_w;
+#pragma unroll 1
+    for (int i = tid; i < n_iw; i += NT)
+      s_iw[i] = 2.0f * sigmoidf_dev(c.inj[(i / HC) * c.ld_inj + (i % HC)] / static_cast<float>(HC));
+#pragma unroll 1
+    for (int i0 = tid; i0 < n_all; i0 += XU * NT) {
+      uint32_t v[XU];
+      uint32_t* dst[XU];
+#pragma unroll
+      for (int k = 0; k < XU; ++k) {
+        const int i = i0 + k * NT;
+        const unsigned int* src = nullptr;
+        dst[k] = nullptr;
+        if (i < n_r) {
+          const int row = i / np, cc = 2 * (i - row * np);     // row = m * HC + stream
+          const int m = row / HC, ss = row - m * HC;
+          src = reinterpret_cast<const unsigned int*>(c.R + static_cast<int64_t>(m) * K + ss * HS + cp0 + cc);
+          dst[k] = reinterpret_cast<uint32_t*>(s_x3r + row * g.nc_max + cc);
+        } else if (i < n_r + n_y) {
+          const int j = i - n_r, m = j / np, cc = 2 * (j - m * np);
+          src = reinterpret_cast<const unsigned int*>(c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
+          dst[k] = reinterpret_cast<uint32_t*>(s_x3y + m * g.nc_max + cc);
+        } else if (i < n_all) {
+          const int j = i - n_r - n_y, ss = j / np, cc = 2 * (j - ss * np);
+          src = reinterpret_cast<const unsigned int*>(c.Wnorm + ss * HS + cp0 + cc);
+          dst[k] = reinterpret_cast<uint32_t*>(s_x3w + ss * g.nc_max + cc);
+        }
+        v[k] = src ? __ldg(src) : 0u;
       }
+#pragma unroll
+      for (int k = 0; k < XU; ++k)
+        if (dst[k]) *dst[k] = v[k];
     }
   }
+  fence_proxy_async_smem();   // the operand rows are read by the tensor cores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
 
-  // --- phase 1b: partial products on the tensor cores
-  const int nk16 = w / 16;
-  const bool k8 = (w & 15) != 0;
-  const bool lo_pass = !c.fold;
-  auto tile_mma = [&](const unsigned char* rows, int row0, int tt, float* acc) {
-    // rows: shared-memory rows of w bf16 (stride 2w bytes); 16 rows from row0.
-    // The hi and lo terms accumulate separately (two short MMA chains).
-    const unsigned char* ra = rows + (row0 + gq) * w * 2;
-    const unsigned char* rb = ra + 8 * w * 2;
-    const unsigned char* bh = reinterpret_cast<const unsigned char*>(s_ahi + (tt * 8 + gq) * w);
-    const unsigned char* bl = reinterpret_cast<const unsigned char*>(s_alo + (tt * 8 + gq) * w);
-    float lo[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-    for (int ks = 0; ks < nk16; ++ks) {
-      const int cb = (ks * 16 + 2 * tq) * 2;
-      const uint32_t a0 = lds32(ra + cb), a1 = lds32(rb + cb), a2 = lds32(ra + cb + 16),
-                     a3 = lds32(rb + cb + 16);
-      mma_16816(acc, a0, a1, a2, a3, lds32(bh + cb), lds32(bh + cb + 16));
-      if (lo_pass) mma_16816(lo, a0, a1, a2, a3, lds32(bl + cb), lds32(bl + cb + 16));
+  // --- step 2: the down/inject products on the tensor cores.  Threads 32
+  // and 96 issue, for even and odd chunks, each into its own accumulator
+  // copy, when every box has its own slot; with a ring (whose slots the
+  // issuer hands back) thread 32 alone consumes the boxes, in order, and
+  // thread 0 refills.
+  const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
+  const int nis = g.nsl_w >= nbox ? 2 : 1;          // issuing threads of the down step
+  if (tid == 32 || tid == 96) {
+    const int me = tid == 96 ? 1 : 0;
+    const uint32_t idesc = idesc_bf16(128, Nd);
+    bool okm = true;
+#pragma unroll 1
+    for (int i = 0; i < nbox && okm; ++i) {
+      const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
+      if (ch % nis != me) continue;
+      okm = wait_bar(full_w(slot), (i / g.nsl_w) & 1, p.err, p.limit_ns);
+      if (!okm) break;
+      tc_fence_after();
+      const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
+      const uint32_t d = tmem + (me * g.ntd + t) * Nd;
+#pragma unroll 1
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc,
+                  (ch >= nis || ks) ? 1u : 0u);
+      umma_commit(free_w(slot));
     }
-    if (k8) {
-      const int cb = (nk16 * 16 + 2 * tq) * 2;
-      const uint32_t a0 = lds32(ra + cb), a1 = lds32(rb + cb);
-      mma_1688(acc, a0, a1, lds32(bh + cb));
-      if (lo_pass) mma_1688(lo, a0, a1, lds32(bl + cb));
-    }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) acc[e] += lo[e];
-  };
-  auto store_part = [&](int nbase, int nvalid, int row0, int tt, const float* acc) {
-    const int m0 = tt * 8 + 2 * tq;
-    const int rows[2] = {row0 + gq, row0 + gq + 8};
-#pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      if (rows[h] >= nvalid) continue;
-      const int n = nbase + rows[h];
-      float* dst = p.part + static_cast<int64_t>(b) * g.part_ld + n;
-      if (m0 < M) dst[m0 * n_out] = acc[2 * h];
-      if (m0 + 1 < M) dst[(m0 + 1) * n_out] = acc[2 * h + 1];
-    }
-  };
-
-  bool ok = true;
-  for (int bx = 0; bx < g.nbox && ok; ++bx) {
-    const int slot = bx % g.nslot_w;
-    const bool got = mbar_wait_bounded(barW(slot), (bx / g.nslot_w) & 1, p.err, p.limit_ns);
-    if (!__syncthreads_and(got)) { ok = false; break; }
-    ++done_w;
-    const int n_lo = bx * g.rows_box;
-    const int nrows = min(r, n_lo + g.rows_box) - n_lo;
-    const int ntile = (nrows + 15) / 16;
-    const unsigned char* base = smem + g.off_w + slot * g.slot_w;
-    for (int pr = warp; pr < ntile * ntok; pr += NW) {
-      const int nt = pr / ntok, tt = pr % ntok;
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
-      tile_mma(base, nt * 16, tt, acc);
-      store_part(n_lo, nrows, nt * 16, tt, acc);
-    }
-    __syncthreads();
-    if (issued_w < g.nbox) {
-      if (tid == 0) issue_w(issued_w);
+    if (!okm) *s_mma_ok = 0;
+    umma_commit(barD);
+  } else if (tid == 0) {
+    // ring refills: a slot is free once the MMAs that read it have completed
+#pragma unroll 1
+    for (int i = pre_w; i < nbox; ++i) {
+      const int slot = i % g.nsl_w;
+      if (!wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)) break;
+      issue_w(i);
       ++issued_w;
     }
   }
-  bool wi_done = false;
-  if (ok) {
-    const bool got = mbar_wait_bounded(barWi, 0, p.err, p.limit_ns);
-    wi_done = ok = __syncthreads_and(got);
-    if (ok) {
-      for (int tt = warp; tt < ntok; tt += NW) {
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        tile_mma(smem + g.off_wi, 0, tt, acc);
-        store_part(r, HC, 0, tt, acc);
+  // meanwhile: the sum of squares, and the non-product words of this CTA's
+  // piece of every reduce-scatter block ([Qn partials][sum of squares][3 pad
+  // words], partials past n_out zero)
+  if (tid < Nt) {
+    float ss = 0.f;
+#pragma unroll 1
+    for (int j = 0; j < nkv * 8; ++j) ss += s_ss1[tid * nu + j];
+    s_ssum[tid] = ss;
+  }
+  __syncthreads();
+  if (!dead) {
+#pragma unroll 1
+    for (int j = tid; j < g.nred; j += NT) {
+      const int m = j / g.Jm, jn = j - m * g.Jm;
+      uint32_t* dst = p.xred + (static_cast<size_t>(j) * g.G + b) * g.row;
+      st_relaxed_v4(dst + g.Qn, make_uint4(xword(s_ssum[m]), 0u, 0u, 0u));
+#pragma unroll 1
+      for (int q = n_out - jn * g.Qn; q < g.Qn; ++q) st_relaxed_u32(dst + q, 0u);
+    }
+  }
+  // the products, straight from TMEM (hi + lo halves, both accumulator
+  // copies): warp w reads lanes 32 (w % 4) ..; the two warp groups take
+  // alternate row tiles
+  bool ok = wait_bar(barD, 0, p.err, p.limit_ns);
+  tc_fence_after();
+  ok = __syncthreads_and(ok && *s_mma_ok != 0);
+  if (ok && !dead) {
+    const int q4 = warp & 3, half = warp >> 2;
+    const int tr = 32 * q4 + lane;                             // row within a tile
+    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+#pragma unroll 1
+    for (int t = half; t < g.ntd; t += 2) {
+      const int rt = t * 128 + tr;
+      const bool inj_row = t == g.wi_tile && tr >= g.wi_row;
+      const int n = inj_row ? r + (tr - g.wi_row) : rt;
+      const bool valid = inj_row ? n < n_out : rt < g.rows_w;
+      const int jn = n / g.Qn, qn = n - jn * g.Qn;
+#pragma unroll 1
+      for (int m0 = 0; m0 < Nt; m0 += 8) {
+        uint32_t hv[8], lv[8];
+        float v[8];
+        tmem_ld8(tl + t * Nd + m0, hv);
+        tmem_ld8(tl + t * Nd + Nt + m0, lv);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(hv[e]) + __uint_as_float(lv[e]);
+        if (nis > 1 && nkv > 1) {
+          tmem_ld8(tl + (g.ntd + t) * Nd + m0, hv);
+          tmem_ld8(tl + (g.ntd + t) * Nd + Nt + m0, lv);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(hv[e]) + __uint_as_float(lv[e]);
+        }
+        if (valid) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (m0 + e < M)
+              st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.G + b) * g.row + qn,
+                             xword(v[e]));
+        }
       }
     }
   }
+  // The weights of the down step are consumed: the next kernel in the stream
+  // may start launching.
+  grid_dep_launch();
+  tc_fence_before();
+  __syncthreads();
+  const uint32_t par = *s_epoch & 1u;
+  uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
 
-  // A test hook: this CTA leaves before the first barrier, as if it had died.
-  if (c.debug_fault == 1 && b == 0) ok = false;
-  if (ok) ok = grid_barrier(p.bar, g.G, p.err, p.limit_ns, s_flag);
-
-  // --- phase 2: rrms, then lora / inj_next for this CTA's output range
-  if (ok) {
-    if (tid == 0) {
-      fence_proxy_async_global();
-      fence_proxy_async_smem();
-      mbar_arrive_expect_tx(barP, static_cast<uint32_t>(g.G * g.Q * 4 + g.ss_bytes));
-      tma_load_2d(smem_u32(s_pbox), &p.tm_part, b * g.Q, 0, barP);
-      bulk_g2s(smem_u32(s_ss), p.sumsq, static_cast<uint32_t>(g.ss_bytes), barP);
+  // --- step 3: the reducer of blocks b, b + G, ...  Work item (stream, sub-
+  // range, quad) sums quad u of the stream's pieces in its sub-range, XU loads
+  // in flight; one thread per (stream, word) then folds the sub-ranges.
+#pragma unroll 1
+  for (int j = b; j < g.nred && ok; j += g.G) {
+    const int m = j / g.Jm, jn = j - m * g.Jm;
+    const uint32_t* blk = p.xred + static_cast<size_t>(j) * g.G * g.row;
+    bool got = true;
+#pragma unroll 1
+    for (int wi = tid; wi < HC * g.R * g.nquad && got; wi += NT) {
+      const int sr = wi / g.nquad, u = wi - sr * g.nquad;   // sr = stream * R + sub-range
+      const int ss = sr / g.R, jr = sr - ss * g.R;
+      const int p0 = jr * g.ppr, p1 = min(g.P, p0 + g.ppr);
+      float run[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+      for (int pp0 = p0; pp0 < p1 && got; pp0 += XU) {
+        uint4 v[XU];
+#pragma unroll
+        for (int k = 0; k < XU; ++k)
+          v[k] = pp0 + k < p1 ? ld_relaxed_v4(blk + (ss * g.P + pp0 + k) * g.row + u * 4)
+                              : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int k = 0; k < XU; ++k) {
+          if (pp0 + k >= p1 || !got) break;
+          uint32_t* src = const_cast<uint32_t*>(blk) + (ss * g.P + pp0 + k) * g.row + u * 4;
+          if (!all_set(v[k])) {
+            v[k] = wait_words(src, p.err, limit);
+            if (!all_set(v[k])) { got = false; break; }
+          }
+          *reinterpret_cast<uint4*>(src) = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
+          run[0] += __uint_as_float(v[k].x);
+          run[1] += __uint_as_float(v[k].y);
+          run[2] += __uint_as_float(v[k].z);
+          run[3] += __uint_as_float(v[k].w);
+        }
+      }
+      *reinterpret_cast<float4*>(s_acc + sr * g.row + u * 4) = make_float4(run[0], run[1], run[2], run[3]);
     }
-    const bool got = mbar_wait_bounded(barP, 0, p.err, p.limit_ns);
     ok = __syncthreads_and(got);
-  }
-  if (ok) {
-    for (int i = warp; i < M * HC; i += NW) {
-      const int m = i / HC, ss = i % HC;
+    if (!ok) break;
+#pragma unroll 1
+    for (int it = tid; it < HC * g.row; it += NT) {
+      const int ss = it / g.row, q = it - ss * g.row;
       float a = 0.f;
-      for (int j = lane; j < g.P; j += 32) a += s_ss[(ss * g.P + j) * M + m];
-      a = warp_sum(a);
-      const float rr = 1.0f / sqrtf(a / static_cast<float>(HS) + c.eps);
-      if (lane == 0) {
-        s_rr[i] = rr;
-        if (b == 0) c.rrms[i] = rr;
-      }
+#pragma unroll 1
+      for (int jr = 0; jr < g.R; ++jr) a += s_acc[(ss * g.R + jr) * g.row + q];
+      s_red[it] = a;
     }
-    // per (output o, stream s): the stream's P partials in order (consecutive
-    // threads read consecutive outputs: no bank conflicts), scaled by rrms_s
-    const int n_own = min(g.Q, M * n_out - b * g.Q);
-    for (int i = tid; i < g.Q * HC; i += NT) {
-      const int o = i % g.Q, ss = i / g.Q;
-      const int og = b * g.Q + o;
-      float a = 0.f;
-      if (o < n_own) {
-        const float* col = s_pbox + ss * g.P * g.Q + o;
-        for (int j = 0; j < g.P; ++j) a += col[j * g.Q];
-        a *= s_rr[(og / n_out) * HC + ss];
-      }
-      s_red[ss * g.Q + o] = a;
+    __syncthreads();
+    if (tid < HC) {
+      const float rr = 1.0f / sqrtf(s_red[tid * g.row + g.Qn] / static_cast<float>(HS) + c.eps);
+      s_rl[tid] = rr;
+      if (jn == 0) c.rrms[m * HC + tid] = rr;
     }
     __syncthreads();
     const float inv_hc = 1.0f / static_cast<float>(HC);
-    for (int o = tid; o < n_own; o += NT) {
-      const int og = b * g.Q + o;
-      const int m = og / n_out, n = og % n_out;
-      float acc = 0.f;
-      for (int ss = 0; ss < HC; ++ss) acc += s_red[ss * g.Q + o];
-      if (n < r) {
-        c.lora[static_cast<int64_t>(m) * r + n] = acc;
-        const float u = acc * inv_hc;
-        p.hdec[m * r + n] = f32_to_bf16(u * sigmoidf_dev(u));
-      } else {
-        c.inj_next[static_cast<int64_t>(m) * HC + (n - r)] = acc;
+#pragma unroll 1
+    for (int qp = tid; qp < g.Qn / 2; qp += NT) {
+      float v[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int q = 2 * qp + e;
+        float a = 0.f;
+#pragma unroll 1
+        for (int ss = 0; ss < HC; ++ss) a += s_rl[ss] * s_red[ss * g.row + q];
+        v[e] = a;
+        const int n = jn * g.Qn + q;
+        if (n < r)
+          c.lora[static_cast<int64_t>(m) * r + n] = a;
+        else if (n < n_out)
+          c.inj_next[static_cast<int64_t>(m) * HC + (n - r)] = a;
+      }
+      const int n0 = jn * g.Qn + 2 * qp;
+      if (n0 < r) {   // r is even: n0 + 1 < r too
+        const float u0 = v[0] * inv_hc, u1 = v[1] * inv_hc;
+        st_relaxed_u32(gat + m * g.L2w + n0 / 2,
+                       pack2(u0 * sigmoidf_dev(u0), u1 * sigmoidf_dev(u1)));
       }
     }
-    ok = grid_barrier(p.bar, g.G, p.err, p.limit_ns, s_flag);
+    if (jn == 0) {
+#pragma unroll 1
+      for (int i = r / 2 + tid; i < g.L2w; i += NT) {
+        const int ss = i - r / 2;
+        st_relaxed_u32(gat + m * g.L2w + i, ss < HC ? xword(s_rl[ss]) : 0u);
+      }
+    }
+    __syncthreads();   // s_acc and s_red are reused by the next block
+  }
+  // empty this CTA's share of the copy the next call uses
+  {
+    uint4* nxt = reinterpret_cast<uint4*>(p.xgat + static_cast<size_t>(par ^ 1u) * p.gat_words);
+    const int nq = p.gat_words / 4;
+    const int per = (nq + g.G - 1) / g.G;
+#pragma unroll 1
+    for (int i = b * per + tid; i < min(nq, (b + 1) * per); i += NT)
+      nxt[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
   }
 
-  // --- phase 3: h, gates for this CTA's channels, gated mean
+  // --- step 4: all-gather of h (into the swizzled operand layout) and rrms
   if (ok && nc > 0) {
-    if (warp == 0) {
-      if (lane == 0) {
-        fence_proxy_async_global();
-        fence_proxy_async_smem();
-        mbar_arrive_expect_tx(barL, static_cast<uint32_t>(M * r * 2));
+    bool got = true;
+    const int hw = r / 2;
+    const int nq = M * g.L2w / 4;
+#pragma unroll 1
+    for (int i0 = tid; i0 < nq && got; i0 += XU * NT) {
+      uint4 v[XU];
+#pragma unroll
+      for (int k = 0; k < XU; ++k)
+        v[k] = i0 + k * NT < nq ? ld_relaxed_v4(gat + (i0 + k * NT) * 4) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int k = 0; k < XU; ++k) {
+        const int i = i0 + k * NT;
+        if (i >= nq || !got) break;
+        if (!all_set(v[k])) {
+          v[k] = wait_words(gat + i * 4, p.err, limit);
+          if (!all_set(v[k])) { got = false; break; }
+        }
+        // r / 2 and L2w are multiples of 4: a quad is 8 h values or rrms/pad
+        const int m = (i * 4) / g.L2w, w0 = i * 4 - m * g.L2w;
+        if (w0 < hw) {
+          const int n0 = 2 * w0;                                  // 8 values from n0
+          const int q = n0 >> 6, un = (n0 & 63) >> 3;
+          *reinterpret_cast<uint4*>(smem + g.off_hb + q * Nu * 128 + m * 128 +
+                                    ((un ^ (m & 7)) << 4)) = v[k];
+        } else {
+          const uint32_t vv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            if (w0 + e < hw + HC) s_rr[m * HC + w0 + e - hw] = __uint_as_float(vv[e]);
+        }
       }
-      __syncwarp();
-      for (int m = lane; m < M; m += 32)   // rows land at the padded stride
-        bulk_g2s(smem_u32(s_h + m * g.hstride), p.hdec + m * r, static_cast<uint32_t>(r * 2), barL);
     }
-    for (int i = tid; i < (MB - M) * g.hstride; i += NT) s_h[M * g.hstride + i] = 0;
-    const bool got = mbar_wait_bounded(barL, 0, p.err, p.limit_ns);
+    // token rows past M, and h columns past r in the last chunk, are zero
+#pragma unroll 1
+    for (int i = tid; i < g.nchunk_u * Nu * 8; i += NT) {
+      const int q = i / (Nu * 8), rem = i - q * Nu * 8, m = rem >> 3, un = rem & 7;
+      if (m >= M || q * 64 + un * 8 >= r)
+        *reinterpret_cast<uint4*>(smem + g.off_hb + q * Nu * 128 + m * 128 + ((un ^ (m & 7)) << 4)) =
+            make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
     ok = __syncthreads_and(got);
   }
-  if (ok && nc > 0) {
-    const float inv_hc = 1.0f / static_cast<float>(HC);
-    const int nrt = g.rows_u16 / 16;
-    const int npair = nrt * ntok;
-    float acc[MAXP][4];
-#pragma unroll
-    for (int j = 0; j < MAXP; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.f;
-    auto chunk_mma = [&](const unsigned char* ub, int q) {
-      const int kc = min(64, r - q * 64);
-#pragma unroll
-      for (int j = 0; j < MAXP; ++j) {
-        const int pr = warp + j * NW;
-        if (pr >= npair) break;
-        const int rt = pr / ntok, tt = pr % ntok;
-        const int i0 = rt * 16 + gq, i1 = i0 + 8;       // rows of the swizzled box (i1 % 8 == i0 % 8)
-        const unsigned char* ra = ub + i0 * 128;
-        const unsigned char* rb = ub + i1 * 128;
-        const int sw = i0 & 7;
-        const unsigned char* hb = reinterpret_cast<const unsigned char*>(
-            s_h + (tt * 8 + gq) * g.hstride + q * 64);
-        int ks = 0;
-        for (; ks + 16 <= kc; ks += 16) {
-          const int ch0 = ks >> 3;
-          const int o0 = ((ch0 ^ sw) << 4) + tq * 4, o1 = (((ch0 + 1) ^ sw) << 4) + tq * 4;
-          mma_16816(acc[j], lds32(ra + o0), lds32(rb + o0), lds32(ra + o1), lds32(rb + o1),
-                    lds32(hb + (ks + 2 * tq) * 2), lds32(hb + (ks + 8 + 2 * tq) * 2));
-        }
-        if (ks < kc) {
-          const int o0 = (((ks >> 3) ^ sw) << 4) + tq * 4;
-          mma_1688(acc[j], lds32(ra + o0), lds32(rb + o0), lds32(hb + (ks + 2 * tq) * 2));
-        }
+  // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
+  // channel) of this CTA's range; threads 32 and 96 take alternate chunks
+  // into their own accumulator copies (the ring has two slots or none, so
+  // each slot serves one issuer)
+  const bool up_issued = ok && nc > 0;
+  if (up_issued) {
+    if (tid == 32 || tid == 96) {
+      const int me = tid == 96 ? 1 : 0;
+      tc_fence_after();
+      const uint32_t idesc = idesc_bf16(128, Nu);
+      bool okm = true;
+#pragma unroll 1
+      for (int q = me; q < nub && okm; q += 2) {
+        const int slot = q % g.nsl_u;
+        okm = wait_bar(full_u(slot), (q / g.nsl_u) & 1, p.err, p.limit_ns);
+        if (!okm) break;
+        tc_fence_after();
+        const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
+#pragma unroll 1
+        for (int tu = 0; tu < g.ntu; ++tu)
+#pragma unroll 1
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
+                      desc_sw128(bq + ks * 32), idesc, (q > 1 || ks) ? 1u : 0u);
+        umma_commit(free_u(slot));
       }
-    };
-    if (g.nslot_u == g.nchunk_u) {
-      // every chunk has its own slot, all issued at kernel start
-      bool got = true;
-      for (int q = 0; q < g.nchunk_u; ++q)
-        got = mbar_wait_bounded(barU(q), 0, p.err, p.limit_ns) && got;
-      ok = __syncthreads_and(got);
-      if (ok) {
-        done_u = issued_u;
-        for (int q = 0; q < g.nchunk_u; ++q) chunk_mma(smem + g.off_u + q * g.slot_u, q);
-      }
-    } else {
-      for (int q = 0; q < g.nchunk_u && ok; ++q) {
-        const int slot = q % g.nslot_u;
-        const bool got = mbar_wait_bounded(barU(slot), (q / g.nslot_u) & 1, p.err, p.limit_ns);
-        if (!__syncthreads_and(got)) { ok = false; break; }
-        ++done_u;
-        chunk_mma(smem + g.off_u + slot * g.slot_u, q);
-        __syncthreads();
-        if (issued_u < g.nchunk_u) {
-          if (tid == 0) issue_u(issued_u);
-          ++issued_u;
-        }
+      if (!okm) *s_mma_ok = 0;
+      umma_commit(barG);
+    } else if (tid == 0) {
+#pragma unroll 1
+      for (int q = pre_u; q < nub; ++q) {
+        const int slot = q % g.nsl_u;
+        if (!wait_bar(free_u(slot), ((q / g.nsl_u) - 1) & 1, p.err, p.limit_ns)) break;
+        issue_u(q);
+        ++issued_u;
       }
     }
+    bool got = wait_bar(barG, 0, p.err, p.limit_ns);
+    tc_fence_after();
+    ok = __syncthreads_and(got && *s_mma_ok != 0);
     if (ok) {
+      const int q4 = warp & 3, half = warp >> 2;
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+#pragma unroll 1
+      for (int tu = half; tu < g.ntu; tu += 2) {
+        const int i = tu * 128 + 32 * q4 + lane;               // row (stream, channel)
+#pragma unroll 1
+        for (int m0 = 0; m0 < Nu; m0 += 8) {
+          uint32_t v0[8], v1[8];
+          tmem_ld8(tl + tu * Nu + m0, v0);
+          if (nub > 1) tmem_ld8(tl + (g.ntu + tu) * Nu + m0, v1);
+          tmem_ld_wait();
+          if (i < g.rows_u) {
 #pragma unroll
-      for (int j = 0; j < MAXP; ++j) {
-        const int pr = warp + j * NW;
-        if (pr >= npair) break;
-        const int rt = pr / ntok, tt = pr % ntok;
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = rt * 16 + gq + (e >> 1) * 8;
-          const int m = tt * 8 + 2 * tq + (e & 1);
-          if (i < g.rows_u && m < M) s_g[m * g.rows_u + i] = sigmoidf_dev(acc[j][e]);
+            for (int e = 0; e < 8; ++e)
+              if (m0 + e < M)
+                s_g[(m0 + e) * g.rows_u + i] = sigmoidf_dev(
+                    __uint_as_float(v0[e]) + (nub > 1 ? __uint_as_float(v1[e]) : 0.f));
+          }
         }
       }
       __syncthreads();
+      const float inv_hc = 1.0f / static_cast<float>(HC);
+#pragma unroll 1
       for (int i = tid; i < M * nc; i += NT) {
-        const int m = i / nc, cc = i % nc, ch = cp0 + cc;
+        const int m = i / nc, cc = i - m * nc, ch = cp0 + cc;
         float sum = 0.f;
+#pragma unroll 1
         for (int ss = 0; ss < HC; ++ss) {
           const float rv = bf16_to_f32(s_x3r[(m * HC + ss) * g.nc_max + cc]);
           const float yv = bf16_to_f32(s_x3y[m * g.nc_max + cc]);
@@ -542,54 +721,82 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     }
   }
 
-  // Let every copy this CTA issued land before its shared memory is released
-  // (only outstanding after a failed wait or an early exit).
-  for (int i = done_w; i < issued_w; ++i)
-    mbar_wait_bounded(barW(i % g.nslot_w), (i / g.nslot_w) & 1, p.err, p.limit_ns);
-  if (!wi_done) mbar_wait_bounded(barWi, 0, p.err, p.limit_ns);
-  for (int i = done_u; i < issued_u; ++i)
-    mbar_wait_bounded(barU(i % g.nslot_u), (i / g.nslot_u) & 1, p.err, p.limit_ns);
+  // Teardown: every copy this CTA issued lands and every MMA it issued
+  // completes (outstanding only after a failed wait), then TMEM is released.
+  if (tid == 0) {
+#pragma unroll 1
+    for (int i = max(0, issued_w - g.nsl_w); i < issued_w; ++i)
+      drain_bar(full_w(i % g.nsl_w), (i / g.nsl_w) & 1, limit);
+#pragma unroll 1
+    for (int q = max(0, issued_u - g.nsl_u); q < issued_u; ++q)
+      drain_bar(full_u(q % g.nsl_u), (q / g.nsl_u) & 1, limit);
+    drain_bar(barD, 0, limit);
+    if (up_issued) drain_bar(barG, 0, limit);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 3) {
+    tc_fence_after();
+    tmem_dealloc(tmem, g.tmem_cols);
+  }
+}
+
+Call shape_call(int64_t M, int HC, int HS, int r) {
+  Call c{};
+  c.M = M;
+  c.HC = HC;
+  c.HS = HS;
+  c.r = r;
+  c.K = HC * HS;
+  c.n_out = r + HC;
+  return c;
 }
 
 }  // namespace
 
-size_t decode_ws_part_floats(const Device& dev, int K_max, int n_out_max) {
-  (void)K_max;
-  return static_cast<size_t>(dev.sms) * (static_cast<size_t>(DECODE_MAX_M) * n_out_max + 4);
+size_t decode_xred_words(const Device& dev, int64_t M, int HC, int HS, int r) {
+  Geom g;
+  if (!make_geom(shape_call(M, HC, HS, r), dev, g)) return 0;
+  return static_cast<size_t>(g.nred) * g.G * g.row;
+}
+
+size_t decode_xgat_words(int n_out_max) {
+  // r / 2 + HC <= r + HC: every shape a handle accepts fits
+  return static_cast<size_t>(DECODE_MAX_M) * round_up(n_out_max, 4);
 }
 
 cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
                           cudaStream_t stream) {
   Params prm;
   prm.c = c;
-  prm.part = ws.part;
-  prm.sumsq = ws.sumsq;
-  prm.hdec = ws.hdec;
-  prm.bar = nullptr;
+  prm.xred = ws.xred;
+  prm.xgat = ws.xgat;
+  prm.gat_words = static_cast<int>(ws.xgat_words);
+  prm.ticket = ws.ticket;
   prm.err = ws.err;
   prm.limit_ns = c.debug_fault ? 50ull * 1000 * 1000 : 1000ull * 1000 * 1000;
   if (!make_geom(c, dev, prm.g)) return cudaErrorNotSupported;
   const Geom& g = prm.g;
-  if (g.G > MAX_GRID) return cudaErrorNotSupported;
-  prm.bar = ws.bar + g.G;
+  if (static_cast<size_t>(g.nred) * g.G * g.row > ws.xred_words ||
+      static_cast<size_t>(c.M) * g.L2w > ws.xgat_words || ws.xgat_words % 4 != 0)
+    return cudaErrorNotSupported;
   const uint64_t wstr[2] = {static_cast<uint64_t>(c.HS) * 2, static_cast<uint64_t>(c.K) * 2};
-  const uint64_t dwd[3] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(c.HC),
-                           static_cast<uint64_t>(c.r)};
-  const uint32_t bwd[3] = {static_cast<uint32_t>(g.w), 1u, static_cast<uint32_t>(g.rows_box)};
+  const uint64_t dw[3] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(c.HC),
+                          static_cast<uint64_t>(g.rows_w)};
+  const uint32_t bw[3] = {64u, 1u, 128u};
+  const uint32_t bwt[3] = {64u, 1u, static_cast<uint32_t>(g.tail > 0 ? g.tail : 8)};
   const uint64_t dwi[3] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(c.HC),
                            static_cast<uint64_t>(c.HC)};
-  const uint32_t bwi[3] = {static_cast<uint32_t>(g.w), 1u, static_cast<uint32_t>(c.HC)};
+  const uint32_t bwi[3] = {64u, 1u, static_cast<uint32_t>(c.HC)};
   const uint64_t dwu[3] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(c.HS),
                            static_cast<uint64_t>(c.HC)};
   const uint64_t swu[2] = {static_cast<uint64_t>(c.r) * 2, static_cast<uint64_t>(c.HS) * c.r * 2};
   const uint32_t bwu[3] = {64u, static_cast<uint32_t>(g.nc_max), static_cast<uint32_t>(c.HC)};
-  const uint64_t dp[2] = {static_cast<uint64_t>(g.part_ld), static_cast<uint64_t>(g.G)};
-  const uint64_t sp[1] = {static_cast<uint64_t>(g.part_ld) * 4};
-  const uint32_t bp[2] = {static_cast<uint32_t>(g.Q), static_cast<uint32_t>(g.G)};
-  if (!make_tmap_bf16(&prm.tm_wd, c.Wd, 3, dwd, wstr, bwd) ||
-      !make_tmap_bf16(&prm.tm_wi, c.Wi, 3, dwi, wstr, bwi) ||
-      !make_tmap_bf16(&prm.tm_wu, c.Wu, 3, dwu, swu, bwu, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&prm.tm_part, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, ws.part, 2, dp, sp, bp))
+  const auto SW = CU_TENSOR_MAP_SWIZZLE_128B;
+  if (!make_tmap_bf16(&prm.tm_w, c.Wd, 3, dw, wstr, bw, SW) ||
+      !make_tmap_bf16(&prm.tm_wt, c.Wd, 3, dw, wstr, bwt, SW) ||
+      !make_tmap_bf16(&prm.tm_wi, c.Wi, 3, dwi, wstr, bwi, SW) ||
+      !make_tmap_bf16(&prm.tm_wu, c.Wu, 3, dwu, swu, bwu, SW))
     return cudaErrorNotSupported;
   static bool attr_done = false;
   if (!attr_done) {
@@ -604,8 +811,13 @@ cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
   cfg.dynamicSmemBytes = g.total + 1024;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeCooperative;
-  attr[0].val.cooperative = 1;
+  if (c.pdl) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+  } else {
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+  }
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, decode_kernel, prm);

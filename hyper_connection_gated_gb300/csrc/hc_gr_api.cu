@@ -2,6 +2,7 @@
 // workspace, the M-based dispatch between the decode and prefill paths, and
 // device status reporting.  The operation and the layouts are documented in
 // include/hc_gr.h.
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstring>
@@ -55,6 +56,15 @@ bool overlap(const Range& a, const Range& b) {
 
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
+// Ticket and status word to zero, every exchange word to the empty marker.
+cudaError_t reset_control(const hcgr::Workspace& ws, cudaStream_t s) {
+  cudaError_t e = cudaMemsetAsync(ws.ticket, 0, hcgr::CTL_BYTES, s);
+  if (e == cudaSuccess && ws.xred_words)
+    e = cudaMemsetAsync(ws.xred, 0xff, ws.xred_words * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.xgat, 0xff, 2 * ws.xgat_words * 4, s);
+  return e;
+}
+
 }  // namespace
 
 extern "C" {
@@ -101,16 +111,18 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   h->r_max = r;
   h->n_out_max = r + HC;
 
-  // one allocation: [bar/err | part | sumsq | lora | prefill]
-  const size_t part_f = hcgr::decode_ws_part_floats(h->dev, h->K_max, h->n_out_max);
-  const size_t sumsq_f = static_cast<size_t>(h->dev.sms) * hcgr::DECODE_MAX_M;
+  // one allocation: [ticket/err | reduce-scatter words | all-gather words (two
+  // copies) | lora | prefill scratch]
+  size_t xred_words = 0;
+  for (int64_t M = 1; M <= std::min<int64_t>(max_M, hcgr::DECODE_MAX_M); ++M)
+    xred_words = std::max(xred_words, hcgr::decode_xred_words(h->dev, M, HC, HS, r));
+  const size_t xgat_words = hcgr::decode_xgat_words(r + HC);
   const size_t lora_f = static_cast<size_t>(max_M) * (r + HC);
   size_t off = 0;
   const size_t off_ctl = off;    off += hcgr::CTL_BYTES;
-  const size_t off_part = off;   off = align_up(off + part_f * 4, 256);
-  const size_t off_sumsq = off;  off = align_up(off + sumsq_f * 4, 256);
+  const size_t off_xred = off;   off = align_up(off + xred_words * 4, 256);
+  const size_t off_xgat = off;   off = align_up(off + 2 * xgat_words * 4, 256);
   const size_t off_lora = off;   off = align_up(off + lora_f * 4, 256);
-  const size_t off_hdec = off;   off = align_up(off + static_cast<size_t>(hcgr::DECODE_MAX_M) * (r + HC) * 2, 256);
   const size_t off_pre = off;    off = align_up(off + hcgr::prefill_ws_bytes(max_M, HC, HS, r), 256);
   void* base = nullptr;
   e = cudaMalloc(&base, off);
@@ -118,23 +130,25 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
     delete h;
     return HC_GR_ERR_CUDA;
   }
-  e = cudaMemset(base, 0, hcgr::CTL_BYTES);
+  unsigned char* b = static_cast<unsigned char*>(base);
+  h->ws.base = base;
+  h->ws.bytes = off;
+  h->ws.ticket = reinterpret_cast<unsigned long long*>(b + off_ctl);
+  h->ws.err = reinterpret_cast<int*>(b + off_ctl + hcgr::MAX_GRID * 8);
+  h->ws.xred = reinterpret_cast<uint32_t*>(b + off_xred);
+  h->ws.xred_words = xred_words;
+  h->ws.xgat = reinterpret_cast<uint32_t*>(b + off_xgat);
+  h->ws.xgat_words = xgat_words;
+  h->ws.lora = reinterpret_cast<float*>(b + off_lora);
+  h->ws.k1_part = reinterpret_cast<float*>(b + off_pre);
+  h->ws.prefill_bytes = hcgr::prefill_ws_bytes(max_M, HC, HS, r);
+  e = reset_control(h->ws, nullptr);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cudaFree(base);
     delete h;
     return HC_GR_ERR_CUDA;
   }
-  unsigned char* b = static_cast<unsigned char*>(base);
-  h->ws.base = base;
-  h->ws.bytes = off;
-  h->ws.bar = reinterpret_cast<unsigned long long*>(b + off_ctl);
-  h->ws.err = reinterpret_cast<int*>(b + off_ctl + hcgr::MAX_GRID * 8);
-  h->ws.part = reinterpret_cast<float*>(b + off_part);
-  h->ws.sumsq = reinterpret_cast<float*>(b + off_sumsq);
-  h->ws.lora = reinterpret_cast<float*>(b + off_lora);
-  h->ws.hdec = reinterpret_cast<hcgr::bf16_t*>(b + off_hdec);
-  h->ws.k1_part = reinterpret_cast<float*>(b + off_pre);
-  h->ws.prefill_bytes = hcgr::prefill_ws_bytes(max_M, HC, HS, r);
   *out = h;
   return HC_GR_OK;
 }
@@ -225,6 +239,7 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
   c.x = static_cast<bf16_t*>(a->x);
   c.lora = a->lora ? a->lora : h->ws.lora;
   c.debug_fault = a->debug_fault;
+  c.pdl = a->pdl ? 1 : 0;
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   DeviceGuard guard(h->dev.id);
@@ -281,8 +296,9 @@ int hc_gr_check(hc_gr_handle h, struct CUstream_st* stream) {
   e = cudaMemcpy(&dev_status, h->ws.err, sizeof(int), cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(h, e);
   if (dev_status == hcgr::DEV_OK) return HC_GR_OK;
-  // clear the status and the barrier counters so the handle can be used again
-  e = cudaMemset(h->ws.base, 0, hcgr::CTL_BYTES);
+  // clear the status, the ticket and the exchange buffers (a failed call can
+  // leave values in them) so the handle can be used again
+  e = reset_control(h->ws, s);
   if (e != cudaSuccess) return cuda_fail(h, e);
   e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(h, e);

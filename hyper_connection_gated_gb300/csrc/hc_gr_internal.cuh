@@ -17,12 +17,13 @@ constexpr int DEV_TIMEOUT = 1;
 
 // Workspace of a handle: all device memory the library owns.
 struct Workspace {
-  float* part = nullptr;      // decode: per-CTA split-K partial products
-  float* sumsq = nullptr;     // decode: per-CTA partial sums of R2^2
-  float* lora = nullptr;      // lora when the caller passes lora == NULL
-  bf16_t* hdec = nullptr;     // decode: h = bf16(SiLU(lora / HC)) [DECODE_MAX_M][r_max]
-  unsigned long long* bar = nullptr;  // grid-barrier counters, one per grid size
+  unsigned long long* ticket = nullptr;  // decode: call ticket (arrivals | epoch << 32)
   int* err = nullptr;         // device status word
+  uint32_t* xred = nullptr;   // decode: reduce-scatter exchange words (empty = 0xffffffff)
+  size_t xred_words = 0;
+  uint32_t* xgat = nullptr;   // decode: all-gather exchange words, two copies of xgat_words
+  size_t xgat_words = 0;
+  float* lora = nullptr;      // lora when the caller passes lora == NULL
   void* base = nullptr;       // single allocation holding everything above
   size_t bytes = 0;
   // prefill workspace
@@ -50,6 +51,7 @@ struct Call {
   bf16_t* x;
   float* lora;        // never NULL here (workspace substitute)
   int debug_fault;
+  int pdl;            // decode: launched as a programmatic dependent of the previous kernel
 };
 
 struct Device {
@@ -59,11 +61,13 @@ struct Device {
   int l2_bytes = 0;
 };
 
-// Decode path (M <= DECODE_MAX_M): one cooperative persistent kernel.
+// Decode path (M <= DECODE_MAX_M): one persistent kernel.
 constexpr int DECODE_MAX_M = 32;
-constexpr int MAX_GRID = 256;            // grid-barrier counters in the workspace
-constexpr int CTL_BYTES = MAX_GRID * 8 + 256;   // counters, then the status word
-size_t decode_ws_part_floats(const Device& dev, int HC_times_HS_max, int n_out_max);
+constexpr int MAX_GRID = 256;            // largest prefill grid the scratch is sized for
+constexpr int CTL_BYTES = MAX_GRID * 8 + 256;   // ticket at 0, status word at MAX_GRID * 8
+// Exchange words the decode kernel needs for one call (0: shape unsupported).
+size_t decode_xred_words(const Device& dev, int64_t M, int HC, int HS, int r);
+size_t decode_xgat_words(int n_out_max);
 cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
                           cudaStream_t stream);
 
@@ -376,6 +380,59 @@ __device__ __forceinline__ bool grid_barrier(unsigned long long* cnt, unsigned n
   }
   __syncthreads();
   return *s_flag != 0;
+}
+
+// Exchange words: 0xffffffff marks an empty word; a value never equals it.
+constexpr uint32_t XEMPTY = 0xffffffffu;
+
+__device__ __forceinline__ uint4 ld_relaxed_v4(const uint32_t* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.b32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_v4(uint32_t* p, uint4 v) {
+  asm volatile("st.relaxed.gpu.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x),
+               "r"(v.y), "r"(v.z), "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ bool all_set(const uint4& v) {
+  return v.x != XEMPTY && v.y != XEMPTY && v.z != XEMPTY && v.w != XEMPTY;
+}
+// A float as an exchange word (NaN canonicalised, so never the empty marker).
+__device__ __forceinline__ uint32_t xword(float v) {
+  return v != v ? 0x7fc00000u : __float_as_uint(v);
+}
+// Spin (bounded) until four consecutive exchange words all hold values.
+// Gives up when the status word reports an error elsewhere or after the time
+// limit (then it reports the timeout itself).
+__device__ __forceinline__ bool xwait4(const uint32_t* p, uint4& v, int* err, long long limit) {
+  v = ld_relaxed_v4(p);
+  if (all_set(v)) return true;
+  const long long t0 = clock64();
+  uint32_t it = 0;
+  while (true) {
+    v = ld_relaxed_v4(p);
+    if (all_set(v)) return true;
+    if ((++it & 15u) == 0) {
+      if (*((volatile int*)err) != DEV_OK) return false;
+      if (clock64() - t0 > limit) {
+        atomicCAS(err, DEV_OK, DEV_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+// Programmatic dependent launch: wait for the grid this one depends on (a
+// no-op without that dependency), and let the next grid start launching.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // Warp-level bf16 MMA (D += A * B, fp32 accumulate).  Fragment layouts (g =

@@ -21,8 +21,7 @@ namespace {
 // NOALLOC_MAX_NOUT; everything else as for hc_gr_forward's decode path.
 constexpr int NOALLOC_MAX_M = 8;
 constexpr int NOALLOC_MAX_NOUT = 336;
-constexpr int NOALLOC_MAX_SMS = 160;
-constexpr size_t NOALLOC_SCRATCH_BYTES = 2u << 20;   // 2 MiB
+constexpr size_t NOALLOC_SCRATCH_BYTES = 4u << 20;   // 4 MiB
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[NOALLOC_SCRATCH_BYTES];
 
@@ -37,21 +36,22 @@ std::mutex g_mu;
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Carve the scratch array into the decode kernel's workspace.
-bool carve(unsigned char* base, const Device& dev, int n_out, Workspace& ws) {
-  size_t off = 0;
+// Carve the scratch array into the decode kernel's workspace for a call that
+// needs xred_words reduce-scatter words: [ticket/status | reduce-scatter |
+// all-gather (two copies) | lora].
+bool carve(unsigned char* base, size_t xred_words, Workspace& ws) {
   ws.base = base;
-  ws.bar = reinterpret_cast<unsigned long long*>(base);
+  ws.ticket = reinterpret_cast<unsigned long long*>(base);
   ws.err = reinterpret_cast<int*>(base + MAX_GRID * 8);
-  off = align256(CTL_BYTES);
-  ws.part = reinterpret_cast<float*>(base + off);
-  off = align256(off + static_cast<size_t>(dev.sms) * (NOALLOC_MAX_M * n_out + 4) * 4);
-  ws.sumsq = reinterpret_cast<float*>(base + off);
-  off = align256(off + static_cast<size_t>(dev.sms) * DECODE_MAX_M * 4);
+  size_t off = align256(CTL_BYTES);
+  ws.xred = reinterpret_cast<uint32_t*>(base + off);
+  ws.xred_words = xred_words;
+  off = align256(off + xred_words * 4);
+  ws.xgat = reinterpret_cast<uint32_t*>(base + off);
+  ws.xgat_words = decode_xgat_words(NOALLOC_MAX_NOUT);
+  off = align256(off + 2 * ws.xgat_words * 4);
   ws.lora = reinterpret_cast<float*>(base + off);
-  off = align256(off + static_cast<size_t>(NOALLOC_MAX_M) * n_out * 4);
-  ws.hdec = reinterpret_cast<bf16_t*>(base + off);
-  off = align256(off + static_cast<size_t>(NOALLOC_MAX_M) * n_out * 2);
+  off = align256(off + static_cast<size_t>(NOALLOC_MAX_M) * NOALLOC_MAX_NOUT * 4);
   ws.bytes = off;
   ws.k1_part = nullptr;
   ws.prefill_bytes = 0;
@@ -128,9 +128,9 @@ extern "C" int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps
       pd.ready = true;
     }
   }
-  if (pd.dev.sms > NOALLOC_MAX_SMS) return HC_GR_ERR_UNSUPPORTED;
+  const size_t xred_words = decode_xred_words(pd.dev, M, HC, HS, r);
   Workspace ws;
-  if (!carve(pd.scratch, pd.dev, NOALLOC_MAX_NOUT, ws)) return HC_GR_ERR_UNSUPPORTED;
+  if (xred_words == 0 || !carve(pd.scratch, xred_words, ws)) return HC_GR_ERR_UNSUPPORTED;
 
   Call c;
   c.M = M;
@@ -155,11 +155,16 @@ extern "C" int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps
   c.x = static_cast<bf16_t*>(x);
   c.lora = lora ? lora : ws.lora;
   c.debug_fault = 0;
+  c.pdl = 0;
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The barrier counters and the status word start at zero on every call
-  // (the array keeps whatever the previous call left there).
+  // The ticket and the status word start at zero and every exchange word
+  // empty on every call (the array keeps whatever the previous call left
+  // there, and a call that timed out can leave values behind).
   if (cudaMemsetAsync(ws.base, 0, CTL_BYTES, s) != cudaSuccess) return HC_GR_ERR_CUDA;
+  const size_t xbytes = reinterpret_cast<unsigned char*>(ws.lora) -
+                        reinterpret_cast<unsigned char*>(ws.xred);
+  if (cudaMemsetAsync(ws.xred, 0xff, xbytes, s) != cudaSuccess) return HC_GR_ERR_CUDA;
   const cudaError_t e = launch_decode(c, ws, pd.dev, s);
   if (e == cudaErrorNotSupported) return HC_GR_ERR_UNSUPPORTED;
   return e == cudaSuccess ? HC_GR_OK : HC_GR_ERR_CUDA;

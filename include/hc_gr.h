@@ -41,14 +41,17 @@
  *
  * Streams and concurrency: hc_gr_forward* only enqueues work on `stream`
  * (a cudaStream_t; NULL is the legacy default stream) and returns.  A handle
- * owns one workspace (cross-CTA partial sums, a grid-barrier word pair and
- * a device status word); calls on one handle must be ordered on one stream.
- * Use one handle per concurrent stream.
+ * owns one workspace (the decode kernel's cross-CTA exchange buffers and call
+ * ticket, the prefill kernels' scratch and a device status word); calls on
+ * one handle must be ordered on one stream.  Use one handle per concurrent
+ * stream.
  *
  * Errors: every entry point returns an hc_gr_status.  Argument errors are
  * detected on the host before anything is enqueued and leave outputs
  * untouched.  A device-side failure (a bounded wait that expired) is
- * recorded in the handle and reported by hc_gr_check.
+ * recorded in the handle and reported by hc_gr_check; the outputs of that
+ * call, and of every later call on the handle until hc_gr_check has cleared
+ * the status, are undefined.
  */
 #ifndef HC_GR_H_
 #define HC_GR_H_
@@ -102,9 +105,17 @@ typedef struct hc_gr_args {
   void* x;
   float* lora;         /* may be NULL: lora is then kept in the workspace */
   int32_t force_path;  /* hc_gr_path */
-  int32_t debug_fault; /* tests only: 1 = one CTA of the decode kernel leaves
-                          before the first grid barrier, so the others' bounded
-                          wait expires and hc_gr_check reports TIMEOUT */
+  int32_t debug_fault; /* tests only: 1 = one CTA of the decode kernel writes
+                          none of its partial sums, as if it had died, so the
+                          others' bounded waits expire and hc_gr_check reports
+                          TIMEOUT */
+  int32_t pdl;         /* 1: launch the decode kernel as a programmatic
+                          dependent of the previous kernel on `stream`: its
+                          weight copies (Wd and Wi or Wdi, and Wu) may start
+                          before that kernel has finished, so that kernel must
+                          not write them; activations are read and outputs
+                          written only after it has finished.  0: plain stream
+                          order.  The prefill kernels ignore it. */
 } hc_gr_args;
 
 /* Creates a handle bound to `device` and allocates its workspace for calls
@@ -129,9 +140,10 @@ int hc_gr_forward(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps,
 int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* stream);
 
 /* Waits for `stream`, then returns the device status recorded by the
- * handle's kernels since the last check (HC_GR_OK or HC_GR_ERR_TIMEOUT) and
- * clears it, resetting the grid-barrier words so the handle is usable again.
- * Returns HC_GR_ERR_CUDA if the stream reports a CUDA error. */
+ * handle's kernels since the last check (HC_GR_OK or HC_GR_ERR_TIMEOUT).
+ * After a TIMEOUT it clears the status and resets the exchange buffers and
+ * the call ticket, so the handle is usable again.  Returns HC_GR_ERR_CUDA if
+ * the stream reports a CUDA error. */
 int hc_gr_check(hc_gr_handle h, struct CUstream_st* stream);
 
 /* Releases the workspace.  Waits for the device first.  NULL is a no-op. */
@@ -148,10 +160,10 @@ const char* hc_gr_last_cuda_error(hc_gr_handle h);
  * call cudaMalloc on their call path, for instance an engine whose memory
  * manager owns all device memory, or code that must not risk the implicit
  * device synchronisation of an allocation.  It runs the decode kernel with
- * its scratch memory (cross-CTA partial sums, h, lora when lora is NULL, the
- * grid-barrier counters and the status word) in one fixed 2 MiB device array
- * inside the library, which every GPU that loads the library holds until the
- * process exits.
+ * its scratch memory (the cross-CTA exchange buffers, lora when lora is NULL,
+ * the call ticket and the status word) in one fixed 4 MiB device array inside
+ * the library, which every GPU that loads the library holds until the process
+ * exits.
  *   - Limits: M <= 8 tokens and r + HC <= 336; larger sizes return
  *     HC_GR_ERR_UNSUPPORTED.  Other arguments, layouts and alignment as for
  *     hc_gr_forward; the current device is used.
@@ -160,8 +172,9 @@ const char* hc_gr_last_cuda_error(hc_gr_handle h);
  *     capture.
  *   - Every call shares the one array: calls that overlap on the GPU (on
  *     different streams, or on several host threads) race and corrupt each
- *     other.  Each call clears the barrier counters and the status word
- *     first; a device-side timeout ends the kernel but is not reported here.
+ *     other.  Each call first clears the ticket and the status word and
+ *     empties the exchange buffers (two memsets on `stream`); a device-side
+ *     timeout ends the kernel but is not reported here.
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *     routine.  Asynchronous on `stream`. */
 int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps,
