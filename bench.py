@@ -202,9 +202,10 @@ def run_ours(args, rank, world):
                            Wd=s["Wd"], Wi=s["Wi"]) for s in sets] for M in SWEEP}
     op.check()
 
-    def prepared(M, j):
+    def prepared(M, j, pdl):
         s, o = sets[j], outs[M][j]
         ar = _native.Args()
+        ar.pdl = 1 if pdl else 0
         ar.M, ar.HC, ar.HS, ar.r, ar.eps = M, HC, HS, R_LOW, 1e-6
         ar.R, ar.y, ar.inj, ar.ld_inj = s["R"].data_ptr(), s["y"].data_ptr(), s["inj"].data_ptr(), HC
         ar.Wnorm, ar.Wd, ar.Wi, ar.Wu = (s["Wnorm"].data_ptr(), s["Wd"].data_ptr(),
@@ -213,7 +214,10 @@ def run_ours(args, rank, world):
         ar.x, ar.lora = o["x"].data_ptr(), o["lora"].data_ptr()
         return ar
 
-    args_tab = {(M, j): prepared(M, j) for M in SWEEP for j in range(nsets)}
+    # pdl: each call may start its weight copies while the previous call in
+    # the stream finishes (the library's programmatic-dependent-launch mode)
+    args_tab = {(M, j, pdl): prepared(M, j, pdl) for M in SWEEP for j in range(nsets)
+                for pdl in (True, False)}
     stream = torch.cuda.Stream()
 
     def capture(calls):
@@ -224,26 +228,29 @@ def run_ours(args, rank, world):
                 assert st == 0, st
         return g
 
-    step_graphs = [capture([args_tab[(M, j)] for M in SWEEP]) for j in range(nsets)]
-    per_m_graphs = {M: capture([args_tab[(M, j)] for j in range(nsets)]) for M in SWEEP}
+    step_graphs = [capture([args_tab[(M, j, True)] for M in SWEEP]) for j in range(nsets)]
+    per_m_graphs = {(M, pdl): capture([args_tab[(M, j, pdl)] for j in range(nsets)])
+                    for M in SWEEP for pdl in (True, False)}
     torch.cuda.synchronize()
 
-    # per-M latency (graph replay, nsets calls per replay)
-    per_m = {}
+    # per-M latency (graph replay, nsets calls per replay), both launch modes
+    per_m, per_m_plain = {}, {}
     with torch.cuda.stream(stream):
         for M in SWEEP:
-            for _ in range(3):
-                per_m_graphs[M].replay()
-            samples = []
-            for _ in range(5):
-                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                e0.record(stream)
-                for _ in range(4):
-                    per_m_graphs[M].replay()
-                e1.record(stream)
-                e1.synchronize()
-                samples.append(e0.elapsed_time(e1) * 1e3 / (4 * nsets))
-            per_m[M] = statistics.median(samples)
+            for pdl, dst in ((True, per_m), (False, per_m_plain)):
+                gr = per_m_graphs[(M, pdl)]
+                for _ in range(3):
+                    gr.replay()
+                samples = []
+                for _ in range(5):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    for _ in range(4):
+                        gr.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    samples.append(e0.elapsed_time(e1) * 1e3 / (4 * nsets))
+                dst[M] = statistics.median(samples)
 
     # timed steps
     with torch.cuda.stream(stream):
@@ -319,6 +326,8 @@ def run_ours(args, rank, world):
                                "unfolded Wd/Wi", "tokens_per_step": tokens_per_step,
                    "l2": f"rotating {nsets} weight+input sets ({nsets * per_set / 1e6:.0f} MB > 2x L2)",
                    "timing": "CUDA graph replay, CUDA events on the launching stream",
+                   "launch": "programmatic dependent launch (hc_gr_args.pdl = 1): a call's "
+                             "weight copies overlap the previous call's tail",
                    "parallelism": f"replicas x{world}"},
         "clocks": clocks,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -330,6 +339,7 @@ def run_ours(args, rank, world):
                      "kernel": "decode_kernel (per launch, mean over the sweep: weights + activations)",
                      "peak_source": peak_src},
         "per_M_us": {str(M): per_m[M] for M in SWEEP},
+        "per_M_us_plain_launch": {str(M): per_m_plain[M] for M in SWEEP},
         "per_M_roofline_frac": {str(M): (WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN) / hbm / 1e3
                                 / per_m[M] for M in SWEEP},
     }

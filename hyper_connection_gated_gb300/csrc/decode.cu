@@ -53,7 +53,7 @@
 namespace hcgr {
 namespace {
 
-constexpr int NT = 256;              // threads per CTA
+constexpr int NT = 512;              // threads per CTA
 constexpr int NW = NT / 32;
 constexpr int MAX_SLOTS = 8;         // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
@@ -71,7 +71,7 @@ struct Geom {
   int tmem_cols;
   int off_rr, off_iw, off_x3r, off_x3y, off_x3w, off_ssum, off_ss1, off_rl, off_act, off_u,
       off_a;                      // (off_act: [nkc][Nd rows][128 B], hi rows then lo rows)
-  int off_acc, off_red, off_hb, off_g;   // region A once the down weights are consumed
+  int off_red, off_hb, off_g;            // region A once the down weights are consumed
   int total;
 };
 
@@ -108,10 +108,8 @@ bool layout(const Call& c, Geom& g) {
   g.off_u = off;    off += g.nsl_u * g.slot_u;
   g.off_a = off;
   const int pw = g.nsl_w * TILE;
-  const int acc_bytes = round_up(c.HC * g.R * g.row * 4, 128);
-  g.off_acc = off;
-  g.off_red = off + acc_bytes;
-  const int pr = acc_bytes + round_up(c.HC * g.row * 4, 128);
+  g.off_red = off;
+  const int pr = round_up(c.HC * g.row * 4, 128);
   g.off_hb = off;
   g.off_g = off + g.nchunk_u * g.Nu * 128;
   const int pg = g.nchunk_u * g.Nu * 128 + round_up(M * g.rows_u * 4, 128);
@@ -155,8 +153,10 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     g.row = g.Qn + 4;                       // Qn partials, the sum of squares, 3 pad words
     g.nquad = g.row / 4;
     if (g.nquad > NT) return false;
-    // reducer: R sub-ranges of ppr pieces per stream and quad
-    g.R = std::max(1, NT / (c.HC * g.nquad));
+    // reducer: R sub-ranges (a power of two, consecutive lanes) of ppr
+    // pieces per stream and quad
+    g.R = 1;
+    while (2 * g.R <= 32 && 2 * g.R * c.HC * g.nquad <= NT) g.R *= 2;
     g.ppr = (g.P + g.R - 1) / g.R;
     g.L2w = round_up(c.r / 2 + c.HC, 4);     // h pairs, then rrms, then pad words
     // two accumulator copies (one per issuing thread) for each product
@@ -227,7 +227,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   float* s_ssum = reinterpret_cast<float*>(smem + g.off_ssum); // [Nt] sum of R2^2 on the slice
   float* s_ss1 = reinterpret_cast<float*>(smem + g.off_ss1);   // [Nt][8 nkc]
   float* s_rl = reinterpret_cast<float*>(smem + g.off_rl);     // [HC] the reducer's rrms
-  float* s_acc = reinterpret_cast<float*>(smem + g.off_acc);   // [HC][R][row]
   float* s_red = reinterpret_cast<float*>(smem + g.off_red);   // [HC][row]
   float* s_g = reinterpret_cast<float*>(smem + g.off_g);       // [M][rows_u]
   const uint32_t act = smem_u32(smem + g.off_act);             // [nkc][Nd rows][128 B]
@@ -263,31 +262,33 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     tma_load_3d(ubase + slot * g.slot_u, &p.tm_wu, q * 64, cp0, 0, full_u(slot));
   };
 
-  // Weight copies first (they do not depend on the previous kernel): two
-  // threads each initialise the barriers they arm and start their stream at
-  // once; a third takes the call ticket; warp 3 allocates TMEM meanwhile.
+  // Weight copies first (they do not depend on the previous kernel): thread
+  // 0 initialises the barriers, then lane 0 of warp w issues box w (down
+  // boxes first, then up chunks), so the issue latencies overlap; warp 15
+  // takes the call ticket and warp 3 allocates TMEM meanwhile.
   const int pre_w = min(g.nsl_w, nbox), pre_u = min(g.nsl_u, nub);
   int issued_w = pre_w, issued_u = pre_u;   // kept by thread 0, which drains them
   if (tid == 0) {
 #pragma unroll 1
-    for (int i = 0; i < 16; ++i) mbar_init(full_w(0) + 8u * i, 1);   // full_w, free_w
+    for (int i = 0; i < 32; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
     mbar_init(barD, 2);
-    fence_mbar_init();
-    *s_mma_ok = 1;
-    prefetch_tmap(&p.tm_w);
-    if (g.wi_tile >= 0) prefetch_tmap(&p.tm_wi);
-    if (g.wi_shared) prefetch_tmap(&p.tm_wt);
-#pragma unroll 1
-    for (int i = 0; i < pre_w; ++i) issue_w(i);
-  } else if (tid == 32) {
-#pragma unroll 1
-    for (int i = 0; i < 16; ++i) mbar_init(full_u(0) + 8u * i, 1);   // full_u, free_u
     mbar_init(barG, 2);
     fence_mbar_init();
-    prefetch_tmap(&p.tm_wu);
+    *s_mma_ok = 1;
+  }
+  __syncthreads();
+  if (lane == 0) {
 #pragma unroll 1
-    for (int q = 0; q < pre_u; ++q) issue_u(q);
-  } else if (tid == 64) {
+    for (int k = warp; k < pre_w + pre_u; k += NW) {
+      if (k < pre_w) {
+        prefetch_tmap(&p.tm_w);
+        issue_w(k);
+      } else {
+        prefetch_tmap(&p.tm_wu);
+        issue_u(k - pre_w);
+      }
+    }
+  } else if (warp == NW - 1 && lane == 1) {
     // arrivals in the low half, the call's epoch in the high half; the last
     // arrival moves the epoch on and clears the count
     const unsigned long long old = atomicAdd(p.ticket, 1ull);
@@ -296,6 +297,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     *s_epoch = static_cast<uint32_t>(old >> 32);
   }
   if (warp == 3) {
+    __syncwarp();
     tmem_alloc(smem_u32(s_tmem), g.tmem_cols);
     tmem_relinquish();
   }
@@ -344,8 +346,53 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     *reinterpret_cast<uint4*>(smem + g.off_act + sw + Nt * 128) = lv;
     s_ss1[m * nu + un] = ss;
   }
-  // inputs of this CTA's channel range for the final mix: iw, and R, y and
-  // Wnorm in channel pairs, XU loads in flight per thread
+  fence_proxy_async_smem();   // the operand rows are read by the tensor cores
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+
+  // --- step 2: the down/inject products on the tensor cores.  Threads 32
+  // and 96 issue, for even and odd chunks, each into its own accumulator
+  // copy, when every box has its own slot; with a ring (whose slots the
+  // issuer hands back) thread 32 alone consumes the boxes, in order, and
+  // thread 0 refills.
+  const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
+  const int nis = g.nsl_w >= nbox ? 2 : 1;          // issuing threads of the down step
+  if (tid == 32 || tid == 96) {
+    const int me = tid == 96 ? 1 : 0;
+    const uint32_t idesc = idesc_bf16(128, Nd);
+    bool okm = true;
+#pragma unroll 1
+    for (int i = 0; i < nbox && okm; ++i) {
+      const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
+      if (ch % nis != me) continue;
+      const uint32_t ph = (i / g.nsl_w) & 1;
+      okm = mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns);
+      if (!okm) break;
+      tc_fence_after();
+      const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
+      const uint32_t d = tmem + (me * g.ntd + t) * Nd;
+#pragma unroll 1
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc,
+                  (ch >= nis || ks) ? 1u : 0u);
+      umma_commit(free_w(slot));
+    }
+    if (!okm) *s_mma_ok = 0;
+    umma_commit(barD);
+  } else if (tid == 0) {
+    // ring refills: a slot is free once the MMAs that read it have completed
+#pragma unroll 1
+    for (int i = pre_w; i < nbox; ++i) {
+      const int slot = i % g.nsl_w;
+      if (!wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)) break;
+      issue_w(i);
+      ++issued_w;
+    }
+  }
+  // meanwhile: inputs of this CTA's channel range for the final mix (iw,
+  // and R, y, Wnorm in channel pairs, XU loads in flight per thread)
   {
     const int np = nc / 2;
     const int n_iw = M * HC, n_r = M * HC * np, n_y = M * np, n_w = HC * np;
@@ -383,51 +430,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         if (dst[k]) *dst[k] = v[k];
     }
   }
-  fence_proxy_async_smem();   // the operand rows are read by the tensor cores
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
-
-  // --- step 2: the down/inject products on the tensor cores.  Threads 32
-  // and 96 issue, for even and odd chunks, each into its own accumulator
-  // copy, when every box has its own slot; with a ring (whose slots the
-  // issuer hands back) thread 32 alone consumes the boxes, in order, and
-  // thread 0 refills.
-  const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
-  const int nis = g.nsl_w >= nbox ? 2 : 1;          // issuing threads of the down step
-  if (tid == 32 || tid == 96) {
-    const int me = tid == 96 ? 1 : 0;
-    const uint32_t idesc = idesc_bf16(128, Nd);
-    bool okm = true;
-#pragma unroll 1
-    for (int i = 0; i < nbox && okm; ++i) {
-      const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
-      if (ch % nis != me) continue;
-      okm = wait_bar(full_w(slot), (i / g.nsl_w) & 1, p.err, p.limit_ns);
-      if (!okm) break;
-      tc_fence_after();
-      const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
-      const uint32_t d = tmem + (me * g.ntd + t) * Nd;
-#pragma unroll 1
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc,
-                  (ch >= nis || ks) ? 1u : 0u);
-      umma_commit(free_w(slot));
-    }
-    if (!okm) *s_mma_ok = 0;
-    umma_commit(barD);
-  } else if (tid == 0) {
-    // ring refills: a slot is free once the MMAs that read it have completed
-#pragma unroll 1
-    for (int i = pre_w; i < nbox; ++i) {
-      const int slot = i % g.nsl_w;
-      if (!wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)) break;
-      issue_w(i);
-      ++issued_w;
-    }
-  }
-  // meanwhile: the sum of squares, and the non-product words of this CTA's
+  // and the sum of squares, and the non-product words of this CTA's
   // piece of every reduce-scatter block ([Qn partials][sum of squares][3 pad
   // words], partials past n_out zero)
   if (tid < Nt) {
@@ -454,38 +457,35 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   tc_fence_after();
   ok = __syncthreads_and(ok && *s_mma_ok != 0);
   if (ok && !dead) {
-    const int q4 = warp & 3, half = warp >> 2;
+    const int q4 = warp & 3, grp = warp >> 2;                  // 4 groups of 4 warps
     const int tr = 32 * q4 + lane;                             // row within a tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+    const int nmc = Nt / 8;                                    // 8-token chunks
+    const bool two = nis > 1 && nkv > 1;
 #pragma unroll 1
-    for (int t = half; t < g.ntd; t += 2) {
+    for (int item = grp; item < g.ntd * nmc; item += NW / 4) {
+      const int t = item / nmc, m0 = (item - t * nmc) * 8;
       const int rt = t * 128 + tr;
       const bool inj_row = t == g.wi_tile && tr >= g.wi_row;
       const int n = inj_row ? r + (tr - g.wi_row) : rt;
       const bool valid = inj_row ? n < n_out : rt < g.rows_w;
       const int jn = n / g.Qn, qn = n - jn * g.Qn;
-#pragma unroll 1
-      for (int m0 = 0; m0 < Nt; m0 += 8) {
-        uint32_t hv[8], lv[8];
-        float v[8];
-        tmem_ld8(tl + t * Nd + m0, hv);
-        tmem_ld8(tl + t * Nd + Nt + m0, lv);
-        tmem_ld_wait();
+      uint32_t h0[8], l0[8], h1[8], l1[8];
+      tmem_ld8(tl + t * Nd + m0, h0);
+      tmem_ld8(tl + t * Nd + Nt + m0, l0);
+      if (two) {
+        tmem_ld8(tl + (g.ntd + t) * Nd + m0, h1);
+        tmem_ld8(tl + (g.ntd + t) * Nd + Nt + m0, l1);
+      }
+      tmem_ld_wait();
+      if (valid) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = __uint_as_float(hv[e]) + __uint_as_float(lv[e]);
-        if (nis > 1 && nkv > 1) {
-          tmem_ld8(tl + (g.ntd + t) * Nd + m0, hv);
-          tmem_ld8(tl + (g.ntd + t) * Nd + Nt + m0, lv);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(hv[e]) + __uint_as_float(lv[e]);
-        }
-        if (valid) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (m0 + e < M)
-              st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.G + b) * g.row + qn,
-                             xword(v[e]));
+        for (int e = 0; e < 8; ++e) {
+          float v = __uint_as_float(h0[e]) + __uint_as_float(l0[e]);
+          if (two) v += __uint_as_float(h1[e]) + __uint_as_float(l1[e]);
+          if (m0 + e < M)
+            st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.G + b) * g.row + qn,
+                           xword(v));
         }
       }
     }
@@ -498,19 +498,22 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   const uint32_t par = *s_epoch & 1u;
   uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
 
-  // --- step 3: the reducer of blocks b, b + G, ...  Work item (stream, sub-
-  // range, quad) sums quad u of the stream's pieces in its sub-range, XU loads
-  // in flight; one thread per (stream, word) then folds the sub-ranges.
+  // --- step 3: the reducer of blocks b, b + G, ...  Work item (stream, quad,
+  // sub-range) sums quad u of the stream's pieces in its sub-range, XU loads
+  // in flight; the R sub-ranges of one (stream, quad) sit in consecutive
+  // lanes and fold with a fixed shuffle tree (deterministic).
 #pragma unroll 1
   for (int j = b; j < g.nred && ok; j += g.G) {
     const int m = j / g.Jm, jn = j - m * g.Jm;
     const uint32_t* blk = p.xred + static_cast<size_t>(j) * g.G * g.row;
     bool got = true;
+    const int nitem = HC * g.nquad * g.R;
 #pragma unroll 1
-    for (int wi = tid; wi < HC * g.R * g.nquad && got; wi += NT) {
-      const int sr = wi / g.nquad, u = wi - sr * g.nquad;   // sr = stream * R + sub-range
-      const int ss = sr / g.R, jr = sr - ss * g.R;
-      const int p0 = jr * g.ppr, p1 = min(g.P, p0 + g.ppr);
+    for (int wi0 = 0; wi0 < nitem; wi0 += NT) {            // uniform: whole warps shuffle
+      const int wi = wi0 + tid;
+      const int su = wi / g.R, jr = wi - su * g.R;         // su = stream * nquad + quad
+      const int ss = su / g.nquad, u = su - ss * g.nquad;
+      const int p0 = jr * g.ppr, p1 = wi < nitem ? min(g.P, p0 + g.ppr) : p0;
       float run[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
       for (int pp0 = p0; pp0 < p1 && got; pp0 += XU) {
@@ -534,19 +537,15 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
           run[3] += __uint_as_float(v[k].w);
         }
       }
-      *reinterpret_cast<float4*>(s_acc + sr * g.row + u * 4) = make_float4(run[0], run[1], run[2], run[3]);
+#pragma unroll 1
+      for (int o = g.R / 2; o > 0; o >>= 1)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) run[e] += __shfl_xor_sync(0xffffffffu, run[e], o);
+      if (wi < nitem && jr == 0)
+        *reinterpret_cast<float4*>(s_red + ss * g.row + u * 4) = make_float4(run[0], run[1], run[2], run[3]);
     }
     ok = __syncthreads_and(got);
     if (!ok) break;
-#pragma unroll 1
-    for (int it = tid; it < HC * g.row; it += NT) {
-      const int ss = it / g.row, q = it - ss * g.row;
-      float a = 0.f;
-#pragma unroll 1
-      for (int jr = 0; jr < g.R; ++jr) a += s_acc[(ss * g.R + jr) * g.row + q];
-      s_red[it] = a;
-    }
-    __syncthreads();
     if (tid < HC) {
       const float rr = 1.0f / sqrtf(s_red[tid * g.row + g.Qn] / static_cast<float>(HS) + c.eps);
       s_rl[tid] = rr;
@@ -584,7 +583,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         st_relaxed_u32(gat + m * g.L2w + i, ss < HC ? xword(s_rl[ss]) : 0u);
       }
     }
-    __syncthreads();   // s_acc and s_red are reused by the next block
+    __syncthreads();   // s_red is reused by the next block
   }
   // empty this CTA's share of the copy the next call uses
   {
@@ -655,7 +654,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll 1
       for (int q = me; q < nub && okm; q += 2) {
         const int slot = q % g.nsl_u;
-        okm = wait_bar(full_u(slot), (q / g.nsl_u) & 1, p.err, p.limit_ns);
+        const uint32_t ph = (q / g.nsl_u) & 1;
+        okm = mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns);
         if (!okm) break;
         tc_fence_after();
         const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
@@ -682,24 +682,23 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     tc_fence_after();
     ok = __syncthreads_and(got && *s_mma_ok != 0);
     if (ok) {
-      const int q4 = warp & 3, half = warp >> 2;
+      const int q4 = warp & 3, grp = warp >> 2;
       const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+      const int nmc = Nu / 8;
 #pragma unroll 1
-      for (int tu = half; tu < g.ntu; tu += 2) {
+      for (int item = grp; item < g.ntu * nmc; item += NW / 4) {
+        const int tu = item / nmc, m0 = (item - tu * nmc) * 8;
         const int i = tu * 128 + 32 * q4 + lane;               // row (stream, channel)
-#pragma unroll 1
-        for (int m0 = 0; m0 < Nu; m0 += 8) {
-          uint32_t v0[8], v1[8];
-          tmem_ld8(tl + tu * Nu + m0, v0);
-          if (nub > 1) tmem_ld8(tl + (g.ntu + tu) * Nu + m0, v1);
-          tmem_ld_wait();
-          if (i < g.rows_u) {
+        uint32_t v0[8], v1[8];
+        tmem_ld8(tl + tu * Nu + m0, v0);
+        if (nub > 1) tmem_ld8(tl + (g.ntu + tu) * Nu + m0, v1);
+        tmem_ld_wait();
+        if (i < g.rows_u) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-              if (m0 + e < M)
-                s_g[(m0 + e) * g.rows_u + i] = sigmoidf_dev(
-                    __uint_as_float(v0[e]) + (nub > 1 ? __uint_as_float(v1[e]) : 0.f));
-          }
+          for (int e = 0; e < 8; ++e)
+            if (m0 + e < M)
+              s_g[(m0 + e) * g.rows_u + i] = sigmoidf_dev(
+                  __uint_as_float(v0[e]) + (nub > 1 ? __uint_as_float(v1[e]) : 0.f));
         }
       }
       __syncthreads();
