@@ -412,15 +412,18 @@ __global__ void k1_reduce_kernel(const float* __restrict__ part, const float* __
 
 // ===================================================================== K2
 // Unit = (128-token tile t, NCU-channel block cb); the MMA N dimension holds
-// the HC streams of those channels (N = HC * NCU rows of Wu).  Warp roles:
-//   warp 0  TMA: the h tile (resident per token tile when it fits) and the Wu
-//           K blocks;
-//   warp 1  one thread issues tcgen05.mma into a double-buffered accumulator;
+// the HC streams of those channels (N = HC * NCU rows of Wu, at most 256, so
+// that one tcgen05.mma does 128 tensor cycles of work per issue).  Roles:
+//   warp 0  TMA: per K block, the h tile (128 x 64) and the HC x NCU rows of
+//           Wu (one 3-D box over Wu viewed as [HC][HS][r]) into a stage ring;
+//   warp 1  tcgen05.mma into a double-buffered accumulator; the whole warp
+//           walks the loop and one elected lane issues;
 //   warp 2  tensor-memory allocation;
-//   warp 3  TMA: the unit's R2 tile (HC boxes, 64- or 32-byte swizzle) and
-//           its Wnorm slice into a two-slot ring;
-//   warps 4-11  epilogue: one token row per thread, NCU/2 channels each.
-// The epilogue writes x into a swizzled staging tile that leaves by TMA store.
+//   warp 3  TMA: the unit's R2 tile one stream at a time (128 x NCU box) and
+//           that stream's Wnorm slice, into a ring of stream slots;
+//   warps 4-11  epilogue: thread = (token row, half of the NCU channels); it
+//           reads the row's gates stream by stream from tensor memory,
+//           rebuilds xn from R2, rrms and Wnorm and stores its x channels.
 constexpr int K2_THREADS = 384;
 constexpr int K2_TMA_WARP = 0;
 constexpr int K2_MMA_WARP = 1;
@@ -428,20 +431,26 @@ constexpr int K2_ALLOC_WARP = 2;
 constexpr int K2_R2_WARP = 3;
 constexpr int K2_EPI_WARP0 = 4;
 constexpr int K2_EPI_WARPS = 8;
+constexpr int K2_MAX_ST = 8;     // stage ring slots
+constexpr int K2_MAX_R2 = 16;    // R2 stream slots
+constexpr uint32_t K2_BAR_BYTES = 512;
 
-__host__ __device__ constexpr int k2_ncu(int hc) { return hc <= 4 ? 32 : 16; }
+__host__ __device__ constexpr int k2_ncu(int hc) { return hc <= 4 ? 64 : 32; }
+__host__ __device__ constexpr uint32_t k2_tmem_cols(int hc) {
+  return 2 * hc * k2_ncu(hc) <= 128 ? 128u : (2 * hc * k2_ncu(hc) <= 256 ? 256u : 512u);
+}
 
 struct K2Params {
   CUtensorMap tm_h;    // h [M][r], box {64, 128}, 128B swizzle
-  CUtensorMap tm_wu;   // Wu [K][r], box {64, NCU}, 128B swizzle
-  CUtensorMap tm_r2;   // R2 [M][K], box {NCU, 128}, NCU*2-byte swizzle
-  CUtensorMap tm_wn;   // Wnorm as [HC][HS], box {NCU, HC}
-  CUtensorMap tm_x;    // x [M][HS], box {NCU, 128}, same swizzle (store)
+  CUtensorMap tm_wu;   // Wu as [HC][HS][r], box {64, NCU, HC}, 128B swizzle
+  CUtensorMap tm_r2;   // R2 [M][K], box {NCU, 128}, (NCU * 2)-byte swizzle
+  CUtensorMap tm_wn;   // Wnorm as [HC][HS], box {NCU, 1}
   const float* rrms;
-  int M, HS, K, r;
-  int nkb, ncb, n_units, nst, a_res;
-  uint32_t b_bytes, stage_bytes, r2_slot, x_slot;
-  uint32_t off_st, off_r2, off_x, off_bar;
+  bf16_t* x;
+  int M, HS, r;
+  int nkb, ncb, n_units, nst, nr2;
+  uint32_t stage_bytes;
+  uint32_t off_r2, off_wn, off_bar;
   int* err;
   uint64_t limit_ns;
 };
@@ -451,8 +460,18 @@ struct K2Params {
 // is XORed with address bits 7.. of the row start).
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
-  if constexpr (ROWB == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
+  if constexpr (ROWB == 128) return row * 128 + ((chunk ^ (row & 7)) << 4);
+  else if constexpr (ROWB == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
   else return row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4);
+}
+
+// One lane of the (converged) warp; used for the single-thread tcgen05 issue.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
 }
 
 template <int HCT>
@@ -464,18 +483,18 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
   constexpr int NCU = k2_ncu(HCT);
   constexpr int N = HC * NCU;
   constexpr uint32_t BOXB = BM * NCU * 2;        // one stream's R2 box
+  constexpr uint32_t TMEM_COLS = k2_tmem_cols(HCT);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int HS = p.HS, nkb = p.nkb, nst = p.nst;
+  const int HS = p.HS, nkb = p.nkb, nst = p.nst, nr2 = p.nr2;
   const uint32_t sbase = smem_u32(smem);
   const uint32_t bar = sbase + p.off_bar;
-  auto full = [&](int st) { return bar + 8u * st; };           // 0..7
-  auto freeb = [&](int st) { return bar + 64u + 8u * st; };    // 8..15
+  auto full = [&](int st) { return bar + 8u * st; };
+  auto freeb = [&](int st) { return bar + 64u + 8u * st; };
   auto accfull = [&](int a) { return bar + 128u + 8u * a; };
   auto accfree = [&](int a) { return bar + 144u + 8u * a; };
-  auto r2full = [&](int a) { return bar + 160u + 8u * a; };
-  auto r2free = [&](int a) { return bar + 176u + 8u * a; };
-  const uint32_t afull = bar + 192u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 224);
+  auto r2full = [&](int q) { return bar + 160u + 8u * q; };
+  auto r2free = [&](int q) { return bar + 288u + 8u * q; };
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 416);
 
   const int u0 = static_cast<int>(static_cast<int64_t>(blockIdx.x) * p.n_units / gridDim.x);
   const int u1 = static_cast<int>(static_cast<int64_t>(blockIdx.x + 1) * p.n_units / gridDim.x);
@@ -486,7 +505,6 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
     prefetch_tmap(&p.tm_wu);
     prefetch_tmap(&p.tm_r2);
     prefetch_tmap(&p.tm_wn);
-    prefetch_tmap(&p.tm_x);
     for (int i = 0; i < nst; ++i) {
       mbar_init(full(i), 1);
       mbar_init(freeb(i), 1);
@@ -494,195 +512,171 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
     for (int a = 0; a < 2; ++a) {
       mbar_init(accfull(a), 1);
       mbar_init(accfree(a), K2_EPI_WARPS);
-      mbar_init(r2full(a), 1);
-      mbar_init(r2free(a), K2_EPI_WARPS);
     }
-    mbar_init(afull, 1);
+    for (int q = 0; q < nr2; ++q) {
+      mbar_init(r2full(q), 1);
+      mbar_init(r2free(q), K2_EPI_WARPS);
+    }
     fence_mbar_init();
   }
   if (warp == K2_ALLOC_WARP) {
-    tmem_alloc(smem_u32(tmem_slot), 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256)));
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tmem_cols = 2 * N <= 32 ? 32 : (2 * N <= 64 ? 64 : (2 * N <= 128 ? 128 : 256));
 
   if (warp == K2_TMA_WARP) {
     if (lane == 0) {
       bool ok = true;
-      int g = 0, cur_t = -1;
-      int last_g[8];
-      for (int i = 0; i < 8; ++i) last_g[i] = -1;
-      int a_loads = 0;
+      int g = 0;
       for (int i = 0; i < n_local && ok; ++i) {
         const int u = u0 + i, t = u / p.ncb, cb = u % p.ncb;
-        if (p.a_res && t != cur_t) {
-          // the previous token tile's MMAs are done with the resident h tile
-          if (i > 0) ok = mbar_wait_bounded(accfull((i - 1) & 1), ((i - 1) >> 1) & 1, p.err, p.limit_ns);
-          if (!ok) break;
-          mbar_arrive_expect_tx(afull, nkb * TILE_BYTES);
-          for (int kb = 0; kb < nkb; ++kb)
-            tma_load_2d(sbase + kb * TILE_BYTES, &p.tm_h, kb * BK, t * BM, afull);
-          cur_t = t;
-          ++a_loads;
-        }
         for (int kb = 0; kb < nkb; ++kb, ++g) {
           const int st = g % nst;
           if (g >= nst) ok = mbar_wait_bounded(freeb(st), ((g / nst) - 1) & 1, p.err, p.limit_ns);
           if (!ok) break;
-          const uint32_t sb = sbase + p.off_st + st * p.stage_bytes;
+          const uint32_t sb = sbase + st * p.stage_bytes;
           mbar_arrive_expect_tx(full(st), p.stage_bytes);
-          uint32_t bb = sb;
-          if (!p.a_res) {
-            tma_load_2d(sb, &p.tm_h, kb * BK, t * BM, full(st));
-            bb += TILE_BYTES;
-          }
-          for (int ss = 0; ss < HC; ++ss)
-            tma_load_2d(bb + ss * NCU * 128, &p.tm_wu, kb * BK, ss * HS + cb * NCU, full(st));
-          last_g[st] = g;
+          tma_load_2d(sb, &p.tm_h, kb * BK, t * BM, full(st));
+          tma_load_3d(sb + TILE_BYTES, &p.tm_wu, kb * BK, cb * NCU, 0, full(st));
         }
       }
-      for (int st = 0; st < nst; ++st)
-        if (last_g[st] >= 0) mbar_wait_bounded(full(st), (last_g[st] / nst) & 1, p.err, p.limit_ns);
-      if (a_loads > 0) mbar_wait_bounded(afull, (a_loads - 1) & 1, p.err, p.limit_ns);
+      // the copies still in flight land before the CTA can leave
+      for (int j = max(0, g - nst); j < g; ++j)
+        mbar_wait_bounded(full(j % nst), (j / nst) & 1, p.err, p.limit_ns);
     }
   } else if (warp == K2_R2_WARP) {
     if (lane == 0) {
       bool ok = true;
-      int issued = 0;
+      int n = 0;
       for (int i = 0; i < n_local && ok; ++i) {
         const int u = u0 + i, t = u / p.ncb, cb = u % p.ncb;
-        const int slot = i & 1;
-        if (i >= 2) ok = mbar_wait_bounded(r2free(slot), ((i >> 1) - 1) & 1, p.err, p.limit_ns);
-        if (!ok) break;
-        const uint32_t rb = sbase + p.off_r2 + slot * p.r2_slot;
-        mbar_arrive_expect_tx(r2full(slot), HC * BOXB + HC * NCU * 2);
-        for (int ss = 0; ss < HC; ++ss)
-          tma_load_2d(rb + ss * BOXB, &p.tm_r2, ss * HS + cb * NCU, t * BM, r2full(slot));
-        tma_load_2d(rb + HC * BOXB, &p.tm_wn, cb * NCU, 0, r2full(slot));
-        ++issued;
+        for (int ss = 0; ss < HC; ++ss, ++n) {
+          const int q = n % nr2;
+          if (n >= nr2) ok = mbar_wait_bounded(r2free(q), ((n / nr2) - 1) & 1, p.err, p.limit_ns);
+          if (!ok) break;
+          mbar_arrive_expect_tx(r2full(q), BOXB + NCU * 2);
+          tma_load_2d(sbase + p.off_r2 + q * BOXB, &p.tm_r2, ss * HS + cb * NCU, t * BM, r2full(q));
+          tma_load_2d(sbase + p.off_wn + q * 128u, &p.tm_wn, cb * NCU, ss, r2full(q));
+        }
       }
-      for (int i = max(0, issued - 2); i < issued; ++i)
-        mbar_wait_bounded(r2full(i & 1), (i >> 1) & 1, p.err, p.limit_ns);
+      for (int j = max(0, n - nr2); j < n; ++j)
+        mbar_wait_bounded(r2full(j % nr2), (j / nr2) & 1, p.err, p.limit_ns);
     }
   } else if (warp == K2_MMA_WARP) {
-    if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(BM, N);
-      bool ok = true;
-      int g = 0, cur_t = -1, a_ph = 0, issued = 0;
-      for (int i = 0; i < n_local && ok; ++i) {
-        const int u = u0 + i, t = u / p.ncb;
-        const int ab = i & 1;
-        if (i >= 2) ok = mbar_wait_bounded(accfree(ab), ((i >> 1) - 1) & 1, p.err, p.limit_ns);
-        if (ok && p.a_res && t != cur_t) {
-          ok = mbar_wait_bounded(afull, a_ph & 1, p.err, p.limit_ns);
-          ++a_ph;
-          cur_t = t;
-        }
+    // Every lane waits on the barriers (so the electing lane has observed
+    // them); the vote keeps the warp on one path if a wait expires.
+    constexpr uint32_t idesc = idesc_bf16(BM, N);
+    bool ok = true;
+    int g = 0, issued = 0;
+    for (int i = 0; i < n_local && ok; ++i) {
+      const int ab = i & 1;
+      if (i >= 2)
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(accfree(ab), ((i >> 1) - 1) & 1, p.err, p.limit_ns));
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t dcol = tmem + ab * N;
+      for (int kb = 0; kb < nkb; ++kb, ++g) {
+        const int st = g % nst;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(full(st), (g / nst) & 1, p.err, p.limit_ns));
         if (!ok) break;
         tc_fence_after();
-        const uint32_t dcol = tmem + ab * N;
-        for (int kb = 0; kb < nkb; ++kb, ++g) {
-          const int st = g % nst;
-          ok = mbar_wait_bounded(full(st), (g / nst) & 1, p.err, p.limit_ns);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t sb = sbase + p.off_st + st * p.stage_bytes;
-          const uint32_t a_base = p.a_res ? sbase + kb * TILE_BYTES : sb;
-          const uint32_t b_base = p.a_res ? sb : sb + TILE_BYTES;
+        const uint32_t sb = sbase + st * p.stage_bytes;
+        const uint64_t ad = desc_sw128(sb), bd = desc_sw128(sb + TILE_BYTES);
+        if (elect_one()) {
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks)
-            umma_bf16(dcol, desc_sw128(a_base + ks * 32), desc_sw128(b_base + ks * 32), idesc,
-                      (kb | ks) != 0);
+            umma_bf16(dcol, ad + 2u * ks, bd + 2u * ks, idesc, (kb | ks) != 0);
           umma_commit(freeb(st));
         }
-        if (!ok) break;
-        umma_commit(accfull(ab));
-        ++issued;
+        __syncwarp();
       }
-      if (issued > 0) mbar_wait_bounded(accfull((issued - 1) & 1), ((issued - 1) >> 1) & 1, p.err, p.limit_ns);
+      if (!ok) break;
+      if (elect_one()) umma_commit(accfull(ab));
+      __syncwarp();
+      ++issued;
     }
+    if (issued > 0)
+      mbar_wait_bounded(accfull((issued - 1) & 1), ((issued - 1) >> 1) & 1, p.err, p.limit_ns);
   } else if (warp >= K2_EPI_WARP0) {
     constexpr int CPT = NCU / 2;          // channels per thread
     constexpr int V = CPT / 8;            // 16-byte chunks per thread and stream
     const int ew = warp - K2_EPI_WARP0;
     const int q4 = warp & 3, half = ew >> 2;
     const int row = 32 * q4 + lane;
-    const bool leader = (ew == 0 && lane == 0);
     const float inv_hc = 1.0f / static_cast<float>(HC);
-    for (int i = 0; i < n_local; ++i) {
+    int n = 0;
+    for (int i = 0; i < n_local; ++i, n += HC) {
       const int u = u0 + i, t = u / p.ncb, cb = u % p.ncb;
-      const int ab = i & 1, slot = i & 1;
+      const int ab = i & 1;
       const int64_t m = static_cast<int64_t>(t) * BM + row;
       const bool v = m < p.M;
       float rr[HC];
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss) rr[ss] = v ? __ldg(p.rrms + m * HC + ss) : 0.f;
-      bool got = mbar_wait_bounded(accfull(ab), (i >> 1) & 1, p.err, p.limit_ns);
-      got = got && mbar_wait_bounded(r2full(slot), (i >> 1) & 1, p.err, p.limit_ns);
-      // all eight epilogue warps take the same branch (they meet at named
-      // barriers below)
-      if (!named_bar_and(1, K2_EPI_WARPS * 32, got)) break;
+      if (!__all_sync(0xffffffffu, mbar_wait_bounded(accfull(ab), (i >> 1) & 1, p.err, p.limit_ns)))
+        break;
       tc_fence_after();
-      const unsigned char* rb = smem + p.off_r2 + slot * p.r2_slot;
-      const bf16_t* wns = reinterpret_cast<const bf16_t*>(rb + HC * BOXB);
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q4) << 16) + ab * N + half * CPT;
       float acc[CPT];
 #pragma unroll
       for (int e = 0; e < CPT; ++e) acc[e] = 0.f;
+      uint32_t gv[2][CPT];
+      if constexpr (CPT == 32) tmem_ld32(tbase, gv[0]);
+      else tmem_ld16(tbase, gv[0]);
+      bool ok = true;
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss) {
-        uint32_t gv[CPT];
-        if constexpr (CPT == 16) tmem_ld16(tbase + ss * NCU, gv);
-        else tmem_ld8(tbase + ss * NCU, gv);
+        const int q = (n + ss) % nr2;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(r2full(q), ((n + ss) / nr2) & 1, p.err, p.limit_ns));
         tmem_ld_wait();
-        float r2[CPT], wn[CPT];
+        if (!ok) break;
+        // the next stream's gates load while this one is processed
+        if (ss + 1 < HC) {
+          if constexpr (CPT == 32) tmem_ld32(tbase + (ss + 1) * NCU, gv[(ss + 1) & 1]);
+          else tmem_ld16(tbase + (ss + 1) * NCU, gv[(ss + 1) & 1]);
+        }
+        const unsigned char* rb = smem + p.off_r2 + q * BOXB;
+        const unsigned char* wb = smem + p.off_wn + q * 128u + half * CPT * 2;
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-          unpack8(*reinterpret_cast<const uint4*>(rb + ss * BOXB + swz_off<NCU * 2>(row, half * V + j)),
-                  r2 + 8 * j);
-          unpack8(*reinterpret_cast<const uint4*>(wns + ss * NCU + half * CPT + 8 * j), wn + 8 * j);
-        }
+          float r2[8], wn[8];
+          unpack8(*reinterpret_cast<const uint4*>(rb + swz_off<NCU * 2>(row, half * V + j)), r2);
+          unpack8(*reinterpret_cast<const uint4*>(wb + 16 * j), wn);
 #pragma unroll
-        for (int e = 0; e < CPT; ++e)
-          acc[e] = fmaf(sigmoid_tanh(__uint_as_float(gv[e])), r2[e] * rr[ss] * (1.0f + wn[e]), acc[e]);
+          for (int e = 0; e < 8; ++e)
+            acc[8 * j + e] = fmaf(sigmoid_tanh(__uint_as_float(gv[ss & 1][8 * j + e])),
+                                  r2[e] * rr[ss] * (1.0f + wn[e]), acc[8 * j + e]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(r2free(q));
       }
-      // R2 slot and accumulator buffer are free again
+      if (!ok) break;
+      // every tensor-memory load of this accumulator has completed
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(r2free(slot));
-        mbar_arrive(accfree(ab));
-      }
-      // x staging buffer i % 2: the store issued two units ago has read it
-      if (leader) bulk_wait_read<1>();
-      named_bar_sync(1, K2_EPI_WARPS * 32);
-      unsigned char* xs = smem + p.off_x + (i & 1) * p.x_slot;
+      if (lane == 0) mbar_arrive(accfree(ab));
+      if (v) {
+        uint4* dst = reinterpret_cast<uint4*>(p.x + m * HS + cb * NCU + half * CPT);
 #pragma unroll
-      for (int j = 0; j < V; ++j) {
-        uint32_t o[4];
+        for (int j = 0; j < V; ++j) {
+          uint32_t o[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-          o[e] = pack2(acc[8 * j + 2 * e] * inv_hc, acc[8 * j + 2 * e + 1] * inv_hc);
-        *reinterpret_cast<uint4*>(xs + swz_off<NCU * 2>(row, half * V + j)) = make_uint4(o[0], o[1], o[2], o[3]);
-      }
-      fence_proxy_async_smem();
-      named_bar_sync(1, K2_EPI_WARPS * 32);
-      if (leader) {
-        tma_store_2d(&p.tm_x, cb * NCU, t * BM, smem_u32(xs));
-        bulk_commit();
+          for (int e = 0; e < 4; ++e)
+            o[e] = pack2(acc[8 * j + 2 * e] * inv_hc, acc[8 * j + 2 * e + 1] * inv_hc);
+          dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
       }
     }
-    if (leader) bulk_wait<0>();
   }
   tc_fence_before();
   __syncthreads();
   if (warp == K2_ALLOC_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols);
+    tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -723,7 +717,8 @@ cudaError_t launch_k2(const K2Params& p, int grid, size_t smem, const Device& de
 bool prefill_supported(const Call& c) {
   return c.HS % 64 == 0 && c.r % 64 == 0 && c.r <= 512 && c.HC >= 1 && c.HC <= 8;
 }
-static_assert(k2_ncu(4) * 4 == 128 && k2_ncu(8) * 8 == 128, "K2 N = 128 for the workloads");
+static_assert(k2_ncu(4) * 4 == 256 && k2_ncu(8) * 8 == 256 && k2_ncu(1) * 8 <= 512,
+              "K2 MMA N = 256 for HC = 4 and 8; 2N tensor-memory columns fit");
 
 
 // K chunks per stream: enough (tile, stream, chunk) CTAs to cover the SMs
@@ -851,53 +846,52 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   {
     K2Params p;
     const int ncu = k2_ncu(c.HC);
+    const int N = c.HC * ncu;
     const uint64_t dh[2] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(M)};
     const uint64_t sh[1] = {static_cast<uint64_t>(c.r) * 2};
     const uint32_t bh[2] = {BK, BM};
-    const uint64_t du[2] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(c.K)};
-    const uint32_t bu[2] = {BK, static_cast<uint32_t>(ncu)};
+    const uint64_t du[3] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(c.HS),
+                            static_cast<uint64_t>(c.HC)};
+    const uint64_t su[2] = {static_cast<uint64_t>(c.r) * 2, static_cast<uint64_t>(c.HS) * c.r * 2};
+    const uint32_t bu[3] = {BK, static_cast<uint32_t>(ncu), static_cast<uint32_t>(c.HC)};
     const uint64_t dr[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(M)};
     const uint64_t sr[1] = {static_cast<uint64_t>(c.K) * 2};
     const uint32_t br[2] = {static_cast<uint32_t>(ncu), BM};
     const uint64_t dn[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(c.HC)};
     const uint64_t sn[1] = {static_cast<uint64_t>(c.HS) * 2};
-    const uint32_t bn[2] = {static_cast<uint32_t>(ncu), static_cast<uint32_t>(c.HC)};
-    const uint64_t dx[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(M)};
-    const CUtensorMapSwizzle sw = ncu == 32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B;
+    const uint32_t bn[2] = {static_cast<uint32_t>(ncu), 1};
+    const CUtensorMapSwizzle sw = ncu == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (!make_tmap_bf16(&p.tm_h, h, 2, dh, sh, bh, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_bf16(&p.tm_wu, c.Wu, 2, du, sh, bu, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_bf16(&p.tm_wu, c.Wu, 3, du, su, bu, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_bf16(&p.tm_r2, c.R2, 2, dr, sr, br, sw) ||
-        !make_tmap_bf16(&p.tm_wn, c.Wnorm, 2, dn, sn, bn) ||
-        !make_tmap_bf16(&p.tm_x, c.x, 2, dx, sn, br, sw))
+        !make_tmap_bf16(&p.tm_wn, c.Wnorm, 2, dn, sn, bn))
       return cudaErrorInvalidValue;
     p.rrms = c.rrms;
+    p.x = c.x;
     p.M = M;
     p.HS = c.HS;
-    p.K = c.K;
     p.r = c.r;
     p.nkb = c.r / BK;
     p.ncb = c.HS / ncu;
     p.n_units = n_mt * p.ncb;
-    p.b_bytes = static_cast<uint32_t>(c.HC * ncu * 128);
-    p.r2_slot = static_cast<uint32_t>(((c.HC * BM * ncu * 2 + c.HC * ncu * 2) + 1023) / 1024 * 1024);
-    p.x_slot = static_cast<uint32_t>(BM * ncu * 2);
-    const int fixed = 2 * static_cast<int>(p.r2_slot) + 2 * static_cast<int>(p.x_slot) + 256 + 1024;
-    const int a_bytes = p.nkb * static_cast<int>(TILE_BYTES);
-    // The h tile stays resident only when that still leaves five Wu stages;
-    // otherwise it is streamed with each Wu K block (an L2 re-read, cheap),
-    // which keeps more bytes in flight per SM.
-    p.a_res = (dev.smem_optin - fixed - a_bytes) / static_cast<int>(p.b_bytes) >= 5 ? 1 : 0;
-    p.stage_bytes = p.b_bytes + (p.a_res ? 0 : TILE_BYTES);
-    p.nst = std::min(8, (dev.smem_optin - fixed - (p.a_res ? a_bytes : 0)) /
-                            static_cast<int>(p.stage_bytes));
-    if (p.nst < 2) return cudaErrorNotSupported;
-    p.off_st = p.a_res ? static_cast<uint32_t>(a_bytes) : 0u;
-    p.off_r2 = p.off_st + p.nst * p.stage_bytes;
-    p.off_x = p.off_r2 + 2 * p.r2_slot;
-    p.off_bar = p.off_x + 2 * p.x_slot;
+    // shared memory: [stage ring | R2 stream slots | Wnorm slices | barriers]
+    p.stage_bytes = TILE_BYTES + static_cast<uint32_t>(N) * 128u;
+    const int box = BM * ncu * 2;
+    const int avail = dev.smem_optin - 1024 - static_cast<int>(K2_BAR_BYTES);
+    p.nst = 3;
+    p.nr2 = std::min(K2_MAX_R2, (avail - p.nst * static_cast<int>(p.stage_bytes)) / (box + 128));
+    if (p.nr2 < 2) {
+      p.nst = 2;
+      p.nr2 = std::min(K2_MAX_R2, (avail - p.nst * static_cast<int>(p.stage_bytes)) / (box + 128));
+    }
+    if (p.nr2 < 2 || p.nst > K2_MAX_ST) return cudaErrorNotSupported;
+    p.off_r2 = static_cast<uint32_t>(p.nst) * p.stage_bytes;
+    p.off_wn = p.off_r2 + static_cast<uint32_t>(p.nr2 * box);
+    p.off_bar = p.off_wn + static_cast<uint32_t>(p.nr2) * 128u;
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
-    const size_t smem = p.off_bar + 256 + 1024;
+    const size_t smem = p.off_bar + K2_BAR_BYTES + 1024;
+    if (smem > static_cast<size_t>(dev.smem_optin)) return cudaErrorNotSupported;
     const int grid = std::min(p.n_units, dev.sms);
     cudaError_t e = cudaSuccess;
     switch (c.HC) {
