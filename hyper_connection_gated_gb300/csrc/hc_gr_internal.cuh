@@ -302,13 +302,14 @@ __device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
       : "=r"(r) : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads) : "memory");
   return r != 0;
 }
-// sigmoid(x) = (1 + tanh(x / 2)) / 2 with the hardware tanh approximation
-// (one MUFU operation).
-__device__ __forceinline__ float sigmoid_tanh(float x) {
+// Hardware tanh approximation (one MUFU operation).
+__device__ __forceinline__ float tanh_approx(float x) {
   float t;
-  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(0.5f * x));
-  return fmaf(0.5f, t, 0.5f);
+  asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+  return t;
 }
+// sigmoid(x) = (1 + tanh(x / 2)) / 2.
+__device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
 
 // Tiled TMA store shared -> global (bulk-group completion); rows and columns
 // outside the tensor are not written.

@@ -25,14 +25,17 @@
 //   the partial sums of squares and the un-scaled partial products.
 // R  (reduce): rrms_s from the partial sums of squares, lora / inj_next =
 //   sum_s rrms_s * (sum of the stream's partial products), and the up-GEMM
-//   operand h = bf16(SiLU(lora / HC)).  With few token tiles K1 splits each
-//   stream's K range into chunks so that the CTAs cover the SMs.
-// K2, persistent over (128-token tile, NCU-channel block) units: A = h tile,
-//   B = the HC * NCU rows {s * HS + c} of Wu, D = 128 x (HC * NCU) fp32 in
-//   double-buffered tensor memory.  The unit's R2 tile and Wnorm slice
-//   stream through a swizzled ring; epilogue warps read a row's gates for all
-//   streams, apply sigmoid, rebuild xn from R2, rrms and Wnorm and write
-//   x = (1/HC) * sum_s G * xn through a staging tile and a TMA store.
+//   operand hh = bf16(SiLU(lora / HC) / 2).  With few token tiles K1 splits
+//   each stream's K range into chunks so that the CTAs cover the SMs.  The
+//   partials are laid out [token][stream, chunk][column], so a row's reduce
+//   reads one contiguous run.
+// K2, persistent over (128-token tile, NCU-channel block) units with
+//   N = HC * NCU = 256 for HC = 4 and 8: A = hh tile, B = the HC * NCU rows
+//   {s * HS + c} of Wu, D = 128 x N fp32 (G / 2) in double-buffered tensor
+//   memory.  The unit's R2 tile and 1 + Wnorm stream through a ring of
+//   per-stream slots; epilogue warps read a row's gates stream by stream,
+//   apply sigmoid, rebuild xn from R2, rrms and 1 + Wnorm and store
+//   x = (1/HC) * sum_s G * xn.
 #include <algorithm>
 
 #include "hc_gr_internal.cuh"
@@ -62,8 +65,8 @@ struct K1Params {
   int64_t ld_inj;
   bf16_t* R2;
   const bf16_t* Wnorm;
-  float* part;        // [HC * S][M][np]: lora columns, then the HC inject columns
-  float* sumsq;       // [HC * S][M] partial sums of R2^2
+  float* part;        // [M][HC * S][np]: lora columns, then the HC inject columns
+  float* sumsq;       // [M][HC * S] partial sums of R2^2
   int M, HS, K, r, np, fold;
   int S;              // K chunks per stream
   int nkb, wbox_rows, nwbox, n1, n2;   // MMA column blocks: [0, n1) and [n1, n1 + n2)
@@ -310,7 +313,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     const int em = m0 + erow;
     const bool v = em < p.M;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    float* dst = p.part + (static_cast<int64_t>(pid) * p.M + (v ? em : 0)) * p.np;
+    float* dst = p.part + (static_cast<int64_t>(v ? em : 0) * (HC * p.S) + pid) * p.np;
     if (ok && half == 0) {
       float injv[HC];
       if constexpr (INJ_MMA) {
@@ -324,7 +327,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
         for (int j = 0; j < HC; ++j) injv[j] = rowinj[erow * HC + j];
       }
       if (v) {
-        p.sumsq[static_cast<int64_t>(pid) * p.M + em] = rowss[erow];
+        p.sumsq[static_cast<int64_t>(em) * (HC * p.S) + pid] = rowss[erow];
 #pragma unroll
         for (int j = 0; j < HC; ++j) dst[r + j] = injv[j];
       }
@@ -356,52 +359,64 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // ================================================================ reduce
 // Per token row: rrms_s from the stream's partial sums of squares, then
 // lora / inj_next = sum_s rrms_s * (sum over the stream's K chunks of the
-// partial products), and the up-GEMM operand h = bf16(SiLU(lora / HC)).
-// Columns go in float4s (np is a multiple of 4 and r of 8, so a float4 never
-// straddles lora and the inject columns).
-constexpr int RED_ROWS = 2;   // token rows per reduce block
+// partial products), and the up-GEMM operand hh = bf16(SiLU(lora / HC) / 2):
+// the halving is exact and makes K2's accumulator hold G / 2, the argument of
+// tanh in sigmoid(G) = (1 + tanh(G / 2)) / 2.  The grid also writes
+// w1 = 1 + Wnorm in fp32 for K2's epilogue.  Columns go in float4s (np is a
+// multiple of 4 and r of 8, so a float4 never straddles lora and the inject
+// columns).
+constexpr int RED_THREADS = 256;
 
-__global__ void k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
-                                 float* __restrict__ rrms, float* __restrict__ lora,
-                                 float* __restrict__ inj_next, bf16_t* __restrict__ h, int M,
-                                 int HC, int S, int r, int np, int HS, float eps) {
-  // block = RED_ROWS token rows x (np / 4 rounded up to a warp) float4 columns;
-  // threads 0..HC-1 of a row form its rrms_s in shared memory first
-  __shared__ float s_rr[RED_ROWS][8];
-  const int m = blockIdx.x * RED_ROWS + threadIdx.y;
-  const int n4 = threadIdx.x;
-  const bool live = m < M;
-  if (live && n4 < HC) {
-    float q = 0.f;
-    for (int c = 0; c < S; ++c) q += sumsq[static_cast<int64_t>(n4 * S + c) * M + m];
-    const float rr = 1.0f / sqrtf(q / static_cast<float>(HS) + eps);
-    s_rr[threadIdx.y][n4] = rr;
-    rrms[static_cast<int64_t>(m) * HC + n4] = rr;
+// One thread per (token row, float4 column): it loads the row's partial sums
+// of squares and its column's HC * S partial products together (a single
+// round trip to memory), forms rrms_s itself and writes its four outputs.
+template <int HC>
+__global__ void __launch_bounds__(RED_THREADS)
+    k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
+                     float* __restrict__ rrms, float* __restrict__ lora,
+                     float* __restrict__ inj_next, bf16_t* __restrict__ hh,
+                     const bf16_t* __restrict__ Wnorm, float* __restrict__ w1, int M, int S,
+                     int r, int np, int HS, float eps) {
+  const int tid = threadIdx.x;
+  const int K = HC * HS;
+  for (int k = blockIdx.x * RED_THREADS + tid; k < K; k += gridDim.x * RED_THREADS)
+    w1[k] = 1.0f + bf16_to_f32(Wnorm[k]);
+  const int np4 = np / 4;
+  const int64_t idx = static_cast<int64_t>(blockIdx.x) * RED_THREADS + tid;
+  if (idx >= static_cast<int64_t>(M) * np4) return;
+  const int m = static_cast<int>(idx / np4);
+  const int n = static_cast<int>(idx % np4) * 4;
+  const int ns = HC * S;
+  const float* prow = part + static_cast<int64_t>(m) * ns * np + n;
+  const float* qrow = sumsq + static_cast<int64_t>(m) * ns;
+  float4 a[HC];
+  float q[HC];
+#pragma unroll
+  for (int ss = 0; ss < HC; ++ss) {
+    a[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
+    q[ss] = 0.f;
+    for (int c = 0; c < S; ++c) {
+      const float4 v = *reinterpret_cast<const float4*>(prow + (ss * S + c) * np);
+      a[ss].x += v.x; a[ss].y += v.y; a[ss].z += v.z; a[ss].w += v.w;
+      q[ss] += qrow[ss * S + c];
+    }
   }
-  __syncthreads();
-  if (!live || n4 * 4 >= np) return;
-  const int n = n4 * 4;
   const float inv_hc = 1.0f / static_cast<float>(HC);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
   for (int ss = 0; ss < HC; ++ss) {
-    const float rs = s_rr[threadIdx.y][ss];
-    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int c = 0; c < S; ++c) {
-      const float4 v = *reinterpret_cast<const float4*>(
-          part + (static_cast<int64_t>(ss * S + c) * M + m) * np + n);
-      a.x += v.x; a.y += v.y; a.z += v.z; a.w += v.w;
-    }
-    acc.x = fmaf(rs, a.x, acc.x); acc.y = fmaf(rs, a.y, acc.y);
-    acc.z = fmaf(rs, a.z, acc.z); acc.w = fmaf(rs, a.w, acc.w);
+    const float rs = 1.0f / sqrtf(q[ss] / static_cast<float>(HS) + eps);
+    if (n == 0) rrms[static_cast<int64_t>(m) * HC + ss] = rs;
+    acc.x = fmaf(rs, a[ss].x, acc.x); acc.y = fmaf(rs, a[ss].y, acc.y);
+    acc.z = fmaf(rs, a[ss].z, acc.z); acc.w = fmaf(rs, a[ss].w, acc.w);
   }
   if (n < r) {
     *reinterpret_cast<float4*>(lora + static_cast<int64_t>(m) * r + n) = acc;
     const float u0 = acc.x * inv_hc, u1 = acc.y * inv_hc, u2 = acc.z * inv_hc, u3 = acc.w * inv_hc;
     uint2 hv;
-    hv.x = pack2(u0 * sigmoidf_dev(u0), u1 * sigmoidf_dev(u1));
-    hv.y = pack2(u2 * sigmoidf_dev(u2), u3 * sigmoidf_dev(u3));
-    *reinterpret_cast<uint2*>(h + static_cast<int64_t>(m) * r + n) = hv;
+    hv.x = pack2(0.5f * (u0 * sigmoidf_dev(u0)), 0.5f * (u1 * sigmoidf_dev(u1)));
+    hv.y = pack2(0.5f * (u2 * sigmoidf_dev(u2)), 0.5f * (u3 * sigmoidf_dev(u3)));
+    *reinterpret_cast<uint2*>(hh + static_cast<int64_t>(m) * r + n) = hv;
   } else {
     const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
 #pragma unroll
@@ -414,13 +429,14 @@ __global__ void k1_reduce_kernel(const float* __restrict__ part, const float* __
 // Unit = (128-token tile t, NCU-channel block cb); the MMA N dimension holds
 // the HC streams of those channels (N = HC * NCU rows of Wu, at most 256, so
 // that one tcgen05.mma does 128 tensor cycles of work per issue).  Roles:
-//   warp 0  TMA: per K block, the h tile (128 x 64) and the HC x NCU rows of
+//   warp 0  TMA: per K block, the hh tile (128 x 64) and the HC x NCU rows of
 //           Wu (one 3-D box over Wu viewed as [HC][HS][r]) into a stage ring;
 //   warp 1  tcgen05.mma into a double-buffered accumulator; the whole warp
 //           walks the loop and one elected lane issues;
 //   warp 2  tensor-memory allocation;
 //   warp 3  TMA: the unit's R2 tile one stream at a time (128 x NCU box) and
-//           that stream's Wnorm slice, into a ring of stream slots;
+//           that stream's slice of 1 + Wnorm (fp32), into a ring of stream
+//           slots;
 //   warps 4-11  epilogue: thread = (token row, half of the NCU channels); it
 //           reads the row's gates stream by stream from tensor memory,
 //           rebuilds xn from R2, rrms and Wnorm and stores its x channels.
@@ -441,16 +457,16 @@ __host__ __device__ constexpr uint32_t k2_tmem_cols(int hc) {
 }
 
 struct K2Params {
-  CUtensorMap tm_h;    // h [M][r], box {64, 128}, 128B swizzle
+  CUtensorMap tm_h;    // hh [M][r], box {64, 128}, 128B swizzle
   CUtensorMap tm_wu;   // Wu as [HC][HS][r], box {64, NCU, HC}, 128B swizzle
   CUtensorMap tm_r2;   // R2 [M][K], box {NCU, 128}, (NCU * 2)-byte swizzle
-  CUtensorMap tm_wn;   // Wnorm as [HC][HS], box {NCU, 1}
+  CUtensorMap tm_w1;   // 1 + Wnorm (fp32) as [HC][HS], box {NCU, 1}
   const float* rrms;
   bf16_t* x;
   int M, HS, r;
   int nkb, ncb, n_units, nst, nr2;
   uint32_t stage_bytes;
-  uint32_t off_r2, off_wn, off_bar;
+  uint32_t off_r2, off_w1, off_bar;
   int* err;
   uint64_t limit_ns;
 };
@@ -504,7 +520,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
     prefetch_tmap(&p.tm_h);
     prefetch_tmap(&p.tm_wu);
     prefetch_tmap(&p.tm_r2);
-    prefetch_tmap(&p.tm_wn);
+    prefetch_tmap(&p.tm_w1);
     for (int i = 0; i < nst; ++i) {
       mbar_init(full(i), 1);
       mbar_init(freeb(i), 1);
@@ -558,9 +574,9 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
           const int q = n % nr2;
           if (n >= nr2) ok = mbar_wait_bounded(r2free(q), ((n / nr2) - 1) & 1, p.err, p.limit_ns);
           if (!ok) break;
-          mbar_arrive_expect_tx(r2full(q), BOXB + NCU * 2);
+          mbar_arrive_expect_tx(r2full(q), BOXB + NCU * 4);
           tma_load_2d(sbase + p.off_r2 + q * BOXB, &p.tm_r2, ss * HS + cb * NCU, t * BM, r2full(q));
-          tma_load_2d(sbase + p.off_wn + q * 128u, &p.tm_wn, cb * NCU, ss, r2full(q));
+          tma_load_2d(sbase + p.off_w1 + q * 256u, &p.tm_w1, cb * NCU, ss, r2full(q));
         }
       }
       for (int j = max(0, n - nr2); j < n; ++j)
@@ -621,9 +637,9 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
         break;
       tc_fence_after();
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q4) << 16) + ab * N + half * CPT;
-      float acc[CPT];
+      float2 acc[CPT / 2];
 #pragma unroll
-      for (int e = 0; e < CPT; ++e) acc[e] = 0.f;
+      for (int e = 0; e < CPT / 2; ++e) acc[e] = make_float2(0.f, 0.f);
       uint32_t gv[2][CPT];
       if constexpr (CPT == 32) tmem_ld32(tbase, gv[0]);
       else tmem_ld16(tbase, gv[0]);
@@ -640,16 +656,25 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
           else tmem_ld16(tbase + (ss + 1) * NCU, gv[(ss + 1) & 1]);
         }
         const unsigned char* rb = smem + p.off_r2 + q * BOXB;
-        const unsigned char* wb = smem + p.off_wn + q * 128u + half * CPT * 2;
+        const float* wb = reinterpret_cast<const float*>(smem + p.off_w1 + q * 256u) + half * CPT;
+        const float2 rr2 = make_float2(rr[ss], rr[ss]);
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-          float r2[8], wn[8];
-          unpack8(*reinterpret_cast<const uint4*>(rb + swz_off<NCU * 2>(row, half * V + j)), r2);
-          unpack8(*reinterpret_cast<const uint4*>(wb + 16 * j), wn);
+          const uint4 rv = *reinterpret_cast<const uint4*>(rb + swz_off<NCU * 2>(row, half * V + j));
+          const float4 wa = *reinterpret_cast<const float4*>(wb + 8 * j);
+          const float4 wc = *reinterpret_cast<const float4*>(wb + 8 * j + 4);
+          const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+          const float2 w[4] = {make_float2(wa.x, wa.y), make_float2(wa.z, wa.w),
+                               make_float2(wc.x, wc.y), make_float2(wc.z, wc.w)};
 #pragma unroll
-          for (int e = 0; e < 8; ++e)
-            acc[8 * j + e] = fmaf(sigmoid_tanh(__uint_as_float(gv[ss & 1][8 * j + e])),
-                                  r2[e] * rr[ss] * (1.0f + wn[e]), acc[8 * j + e]);
+          for (int e = 0; e < 4; ++e) {
+            // xn = R2 * rrms * (1 + Wnorm); sigmoid(G) = 1/2 + tanh(G / 2) / 2
+            const float2 xn = __fmul2_rn(__fmul2_rn(make_float2(lo_bf16(rw[e]), hi_bf16(rw[e])), rr2), w[e]);
+            const float2 th = make_float2(tanh_approx(__uint_as_float(gv[ss & 1][8 * j + 2 * e])),
+                                          tanh_approx(__uint_as_float(gv[ss & 1][8 * j + 2 * e + 1])));
+            const float2 sg = __ffma2_rn(th, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
+            acc[4 * j + e] = __ffma2_rn(sg, xn, acc[4 * j + e]);
+          }
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(r2free(q));
@@ -665,8 +690,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
         for (int j = 0; j < V; ++j) {
           uint32_t o[4];
 #pragma unroll
-          for (int e = 0; e < 4; ++e)
-            o[e] = pack2(acc[8 * j + 2 * e] * inv_hc, acc[8 * j + 2 * e + 1] * inv_hc);
+          for (int e = 0; e < 4; ++e) o[e] = pack2(acc[4 * j + e].x * inv_hc, acc[4 * j + e].y * inv_hc);
           dst[j] = make_uint4(o[0], o[1], o[2], o[3]);
         }
       }
@@ -740,8 +764,8 @@ size_t prefill_ws_bytes(int64_t max_M, int HC, int HS, int r) {
   part = std::max(part, static_cast<size_t>(2 * MAX_GRID) * BM * k1_np(r, HC));
   const size_t sumsq = std::max(static_cast<size_t>(HC) * max_M, static_cast<size_t>(2 * MAX_GRID) * BM);
   const size_t h = static_cast<size_t>(max_M) * r * 2;
-  (void)HS;
-  return part * 4 + 256 + sumsq * 4 + 256 + h + 256;
+  const size_t w1 = static_cast<size_t>(HC) * HS;
+  return part * 4 + 256 + sumsq * 4 + 256 + h + 256 + w1 * 4 + 256;
 }
 
 cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev,
@@ -764,6 +788,8 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   const size_t sumsq_floats = static_cast<size_t>(c.HC) * S * M;
   bf16_t* h = reinterpret_cast<bf16_t*>(reinterpret_cast<unsigned char*>(sumsq) +
                                         (sumsq_floats * 4 + 255) / 256 * 256);
+  float* w1 = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(h) +
+                                       (static_cast<size_t>(M) * c.r * 2 + 255) / 256 * 256);
 
   // ---------------- K1
   {
@@ -836,9 +862,19 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   }
   // ---------------- reduce
   {
-    const dim3 block((np / 4 + 31) / 32 * 32, RED_ROWS);
-    k1_reduce_kernel<<<(M + RED_ROWS - 1) / RED_ROWS, block, 0, stream>>>(
-        part, sumsq, c.rrms, c.lora, c.inj_next, h, M, c.HC, S, c.r, np, c.HS, c.eps);
+    const int64_t items = static_cast<int64_t>(M) * (np / 4);
+    const unsigned grid = static_cast<unsigned>((items + RED_THREADS - 1) / RED_THREADS);
+#define HCGR_RED(HCV)                                                                        \
+  case HCV:                                                                                  \
+    k1_reduce_kernel<HCV><<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,     \
+                                                          c.inj_next, h, c.Wnorm, w1, M, S,  \
+                                                          c.r, np, c.HS, c.eps);             \
+    break;
+    switch (c.HC) {
+      HCGR_RED(1) HCGR_RED(2) HCGR_RED(3) HCGR_RED(4) HCGR_RED(5) HCGR_RED(6) HCGR_RED(7)
+      default: HCGR_RED(8)
+    }
+#undef HCGR_RED
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
@@ -858,13 +894,13 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const uint64_t sr[1] = {static_cast<uint64_t>(c.K) * 2};
     const uint32_t br[2] = {static_cast<uint32_t>(ncu), BM};
     const uint64_t dn[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(c.HC)};
-    const uint64_t sn[1] = {static_cast<uint64_t>(c.HS) * 2};
+    const uint64_t sn[1] = {static_cast<uint64_t>(c.HS) * 4};
     const uint32_t bn[2] = {static_cast<uint32_t>(ncu), 1};
     const CUtensorMapSwizzle sw = ncu == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (!make_tmap_bf16(&p.tm_h, h, 2, dh, sh, bh, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_bf16(&p.tm_wu, c.Wu, 3, du, su, bu, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_bf16(&p.tm_r2, c.R2, 2, dr, sr, br, sw) ||
-        !make_tmap_bf16(&p.tm_wn, c.Wnorm, 2, dn, sn, bn))
+        !make_tmap(&p.tm_w1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w1, 2, dn, sn, bn))
       return cudaErrorInvalidValue;
     p.rrms = c.rrms;
     p.x = c.x;
@@ -874,20 +910,20 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.nkb = c.r / BK;
     p.ncb = c.HS / ncu;
     p.n_units = n_mt * p.ncb;
-    // shared memory: [stage ring | R2 stream slots | Wnorm slices | barriers]
+    // shared memory: [stage ring | R2 stream slots | 1 + Wnorm slices | barriers]
     p.stage_bytes = TILE_BYTES + static_cast<uint32_t>(N) * 128u;
     const int box = BM * ncu * 2;
     const int avail = dev.smem_optin - 1024 - static_cast<int>(K2_BAR_BYTES);
     p.nst = 3;
-    p.nr2 = std::min(K2_MAX_R2, (avail - p.nst * static_cast<int>(p.stage_bytes)) / (box + 128));
+    p.nr2 = std::min(K2_MAX_R2, (avail - p.nst * static_cast<int>(p.stage_bytes)) / (box + 256));
     if (p.nr2 < 2) {
       p.nst = 2;
-      p.nr2 = std::min(K2_MAX_R2, (avail - p.nst * static_cast<int>(p.stage_bytes)) / (box + 128));
+      p.nr2 = std::min(K2_MAX_R2, (avail - p.nst * static_cast<int>(p.stage_bytes)) / (box + 256));
     }
     if (p.nr2 < 2 || p.nst > K2_MAX_ST) return cudaErrorNotSupported;
     p.off_r2 = static_cast<uint32_t>(p.nst) * p.stage_bytes;
-    p.off_wn = p.off_r2 + static_cast<uint32_t>(p.nr2 * box);
-    p.off_bar = p.off_wn + static_cast<uint32_t>(p.nr2) * 128u;
+    p.off_w1 = p.off_r2 + static_cast<uint32_t>(p.nr2 * box);
+    p.off_bar = p.off_w1 + static_cast<uint32_t>(p.nr2) * 256u;
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
     const size_t smem = p.off_bar + K2_BAR_BYTES + 1024;
