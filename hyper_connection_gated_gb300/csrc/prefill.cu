@@ -49,17 +49,28 @@ constexpr int BK = 64;    // K block: one 128-byte swizzle row of bf16
 constexpr uint32_t TILE_BYTES = BM * BK * 2;   // 16 KB
 
 // ===================================================================== K1
+// Shared memory holds two rings: R/y slots (the R and y tiles of one K block,
+// 32 KB, converted in place into the MMA's A operand) and weight slots (one
+// column block of the B tile: Wd rows, plus the inject rows in the last
+// block).  The R/y ring runs deeper because its tiles come from HBM; the
+// weights are L2-resident.
 constexpr int K1_CONV_WARPS = 8;
-constexpr int K1_THREADS = (K1_CONV_WARPS + 2) * 32;
-constexpr int K1_TMA_WARP = K1_CONV_WARPS;
-constexpr int K1_MMA_WARP = K1_CONV_WARPS + 1;
-constexpr int K1_MAXST = 4;
+constexpr int K1_RY_WARP = 8;     // TMA: R, y tiles and the K block's Wnorm values
+constexpr int K1_MMA_WARP = 9;    // MMAs of column block 0 (and the TMEM allocation)
+constexpr int K1_W_WARP = 10;     // TMA: weight column blocks
+constexpr int K1_MMA1_WARP = 11;  // MMAs of column block 1
+constexpr int K1_THREADS = 12 * 32;
+constexpr int K1_MAX_RY = 6;
+constexpr int K1_MAX_W = 8;
+constexpr uint32_t RY_BYTES = 2 * TILE_BYTES;
+constexpr uint32_t K1_BAR_BYTES = 512;
 constexpr int WI_ROWS = 16;   // inject rows in the MMA's B tile (HC real, rest zero-filled)
 
 struct K1Params {
   CUtensorMap tm_R;    // [M][K], box {64, 128}, 128B swizzle
   CUtensorMap tm_y;    // [M][HS], box {64, 128}, 128B swizzle
-  CUtensorMap tm_w;    // Wd [r][K], box {64, wbox_rows}, 128B swizzle
+  CUtensorMap tm_w0;   // Wd rows [0, wrows0): box {64, wrows0}, 128B swizzle
+  CUtensorMap tm_w1;   // Wd rows [wrows0, r): box {64, r - wrows0}, 128B swizzle
   CUtensorMap tm_wi;   // Wi [HC][K], box {64, 16} (128B swizzle) or {64, HC} (plain)
   const float* inj;
   int64_t ld_inj;
@@ -69,32 +80,15 @@ struct K1Params {
   float* sumsq;       // [M][HC * S] partial sums of R2^2
   int M, HS, K, r, np, fold;
   int S;              // K chunks per stream
-  int nkb, wbox_rows, nwbox, n1, n2;   // MMA column blocks: [0, n1) and [n1, n1 + n2)
-  int nst;                             // pipeline stages (2 or 3)
-  uint32_t stage_bytes, tmem_cols;
+  int nkb;
+  int n1, n2;         // MMA column blocks (B rows): [0, n1) and [n1, n1 + n2); n2 may be 0
+  int wrows0;         // Wd rows in column block 0 (the rest, and the inject rows, in block 1)
+  int nry, nw;        // ring depths
+  uint32_t w_slot, tmem_cols;
+  uint32_t off_w, off_wn, off_wic, off_bar, off_rowss, off_rowinj;
   int* err;
   uint64_t limit_ns;
 };
-
-struct K1Smem {
-  uint32_t stage, off_b, off_wi, off_wn, off_bar, off_rowss, off_rowinj, total;
-};
-
-// Stage: R tile, y tile, B tile (r rows of Wd, then the inject rows).  The K
-// blocks' Wnorm values (128 bytes each) sit in a small ring of their own.
-__host__ __device__ inline K1Smem k1_smem(int r, int HC, bool inj_mma, int nst) {
-  K1Smem s;
-  s.off_b = 2 * TILE_BYTES;
-  s.off_wi = s.off_b + r * 128;
-  const uint32_t wi_bytes = (inj_mma ? WI_ROWS : HC) * 128;
-  s.stage = (s.off_wi + wi_bytes + 1023) / 1024 * 1024;
-  s.off_wn = nst * s.stage;
-  s.off_bar = s.off_wn + K1_MAXST * 128;
-  s.off_rowss = s.off_bar + 128;
-  s.off_rowinj = s.off_rowss + BM * 4;
-  s.total = s.off_rowinj + (inj_mma ? 0 : BM * HC * 4);
-  return s;
-}
 
 template <int HCT, bool INJ_MMA>
 __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant__ K1Params p) {
@@ -102,8 +96,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int HC = HCT;
-  const K1Smem L = k1_smem(p.r, HC, INJ_MMA, p.nst);
-  const int NST = p.nst;
+  const int NRY = p.nry, NW = p.nw;
+  const int nh = p.n2 > 0 ? 2 : 1;   // weight column blocks per K block
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int chunk = blockIdx.x % p.S;
   const int s = (blockIdx.x / p.S) % HC;
@@ -113,26 +107,33 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   const int kb0 = chunk * p.nkb / p.S, kb1 = (chunk + 1) * p.nkb / p.S;
   const int nkb = kb1 - kb0;                       // K blocks of this CTA
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t bar = sbase + L.off_bar;
-  auto full = [&](int st) { return bar + 8u * st; };
-  auto conv = [&](int st) { return bar + 32u + 8u * st; };
-  auto freeb = [&](int st) { return bar + 64u + 8u * st; };
-  const uint32_t accb = bar + 96u;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.off_bar + 104);
-  float* rowss = reinterpret_cast<float*>(smem + L.off_rowss);
-  float* rowinj = reinterpret_cast<float*>(smem + L.off_rowinj);
+  const uint32_t bar = sbase + p.off_bar;
+  auto ryfull = [&](int st) { return bar + 8u * st; };
+  auto conv = [&](int st) { return bar + 48u + 8u * st; };
+  auto ryfree = [&](int st) { return bar + 96u + 8u * st; };
+  auto wfull = [&](int ws) { return bar + 144u + 8u * ws; };
+  auto wfree = [&](int ws) { return bar + 208u + 8u * ws; };
+  const uint32_t accb = bar + 272u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + p.off_bar + 280);
+  float* rowss = reinterpret_cast<float*>(smem + p.off_rowss);
+  float* rowinj = reinterpret_cast<float*>(smem + p.off_rowinj);
 
   if (tid == 0) {
     prefetch_tmap(&p.tm_R);
     prefetch_tmap(&p.tm_y);
-    prefetch_tmap(&p.tm_w);
+    prefetch_tmap(&p.tm_w0);
+    prefetch_tmap(&p.tm_w1);
     prefetch_tmap(&p.tm_wi);
-    for (int i = 0; i < NST; ++i) {
-      mbar_init(full(i), 1);
+    for (int i = 0; i < NRY; ++i) {
+      mbar_init(ryfull(i), 1);
       mbar_init(conv(i), K1_CONV_WARPS);
-      mbar_init(freeb(i), 1);
+      mbar_init(ryfree(i), nh);
     }
-    mbar_init(accb, 1);
+    for (int i = 0; i < NW; ++i) {
+      mbar_init(wfull(i), 1);
+      mbar_init(wfree(i), 1);
+    }
+    mbar_init(accb, nh);
     fence_mbar_init();
   }
   if (warp == K1_MMA_WARP) {
@@ -144,64 +145,98 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == K1_TMA_WARP) {
+  if (warp == K1_RY_WARP) {
     if (lane == 0) {
-      int last_issued[K1_MAXST] = {-1, -1, -1, -1};
       bool ok = true;
-      const uint32_t wi_tx = (INJ_MMA ? WI_ROWS : HC) * 128;
-      for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int st = kb % NST;
-        if (kb >= NST)
-          ok = mbar_wait_bounded(freeb(st), ((kb / NST) - 1) & 1, p.err, p.limit_ns);
+      int kb = 0;
+      const uint32_t wic_tx = INJ_MMA ? 0u : HC * 128u;
+      for (; kb < nkb && ok; ++kb) {
+        const int st = kb % NRY;
+        if (kb >= NRY) ok = mbar_wait_bounded(ryfree(st), ((kb / NRY) - 1) & 1, p.err, p.limit_ns);
         if (!ok) break;
-        const uint32_t sb = sbase + st * L.stage;
+        const uint32_t sb = sbase + st * RY_BYTES;
         const int kx = (kb0 + kb) * BK;           // column within the stream
-        mbar_arrive_expect_tx(full(st), 2 * TILE_BYTES + r * 128 + wi_tx + 128);
-        tma_load_2d(sb, &p.tm_R, s * HS + kx, m0, full(st));
-        tma_load_2d(sb + TILE_BYTES, &p.tm_y, kx, m0, full(st));
-        for (int bx = 0; bx < p.nwbox; ++bx)
-          tma_load_2d(sb + L.off_b + bx * p.wbox_rows * 128, &p.tm_w, s * HS + kx,
-                      bx * p.wbox_rows, full(st));
-        tma_load_2d(sb + L.off_wi, &p.tm_wi, s * HS + kx, 0, full(st));
-        bulk_g2s(sbase + L.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kx, 128,
-                 full(st));
-        last_issued[st] = kb;
+        mbar_arrive_expect_tx(ryfull(st), RY_BYTES + 128 + wic_tx);
+        tma_load_2d(sb, &p.tm_R, s * HS + kx, m0, ryfull(st));
+        tma_load_2d(sb + TILE_BYTES, &p.tm_y, kx, m0, ryfull(st));
+        bulk_g2s(sbase + p.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kx, 128,
+                 ryfull(st));
+        if constexpr (!INJ_MMA)
+          tma_load_2d(sbase + p.off_wic + st * HC * 128, &p.tm_wi, s * HS + kx, 0, ryfull(st));
       }
       // outstanding copies land before the CTA can leave
-      for (int st = 0; st < NST; ++st)
-        if (last_issued[st] >= 0)
-          mbar_wait_bounded(full(st), (last_issued[st] / NST) & 1, p.err, p.limit_ns);
+      for (int j = max(0, kb - NRY); j < kb; ++j)
+        mbar_wait_bounded(ryfull(j % NRY), (j / NRY) & 1, p.err, p.limit_ns);
     }
-  } else if (warp == K1_MMA_WARP) {
+  } else if (warp == K1_W_WARP) {
     if (lane == 0) {
-      const uint32_t id1 = idesc_bf16(BM, p.n1);
-      const uint32_t id2 = idesc_bf16(BM, p.n2 > 0 ? p.n2 : 16);
       bool ok = true;
-      for (int kb = 0; kb < nkb; ++kb) {
-        const int st = kb % NST;
-        ok = mbar_wait_bounded(conv(st), (kb / NST) & 1, p.err, p.limit_ns);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t sb = sbase + st * L.stage;
-#pragma unroll
-        for (int ks = 0; ks < BK / 16; ++ks) {
-          const uint64_t a_hi = desc_sw128(sb + ks * 32);
-          const uint64_t a_lo = desc_sw128(sb + TILE_BYTES + ks * 32);
-          const uint64_t b1 = desc_sw128(sb + L.off_b + ks * 32);
-          umma_bf16(tmem, a_hi, b1, id1, (kb | ks) != 0);
-          if (!p.fold) umma_bf16(tmem, a_lo, b1, id1, 1);
-          if (p.n2 > 0) {
-            const uint64_t b2 = desc_sw128(sb + L.off_b + p.n1 * 128 + ks * 32);
-            umma_bf16(tmem + p.n1, a_hi, b2, id2, (kb | ks) != 0);
-            if (!p.fold) umma_bf16(tmem + p.n1, a_lo, b2, id2, 1);
+      int g = 0;
+      const uint32_t bytes0 = p.n2 > 0 ? p.wrows0 * 128u
+                                       : r * 128u + (INJ_MMA ? WI_ROWS * 128u : 0u);
+      const uint32_t bytes1 = (r - p.wrows0) * 128u + (INJ_MMA ? WI_ROWS * 128u : 0u);
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int kx = s * HS + (kb0 + kb) * BK;
+        for (int hh = 0; hh < nh; ++hh, ++g) {
+          const int ws = g % NW;
+          if (g >= NW) ok = mbar_wait_bounded(wfree(ws), ((g / NW) - 1) & 1, p.err, p.limit_ns);
+          if (!ok) break;
+          const uint32_t wb = sbase + p.off_w + ws * p.w_slot;
+          if (hh == 0) {
+            mbar_arrive_expect_tx(wfull(ws), bytes0);
+            tma_load_2d(wb, &p.tm_w0, kx, 0, wfull(ws));
+            if (p.n2 == 0) {
+              if (r > p.wrows0) tma_load_2d(wb + p.wrows0 * 128, &p.tm_w1, kx, p.wrows0, wfull(ws));
+              if constexpr (INJ_MMA) tma_load_2d(wb + r * 128, &p.tm_wi, kx, 0, wfull(ws));
+            }
+          } else {
+            mbar_arrive_expect_tx(wfull(ws), bytes1);
+            tma_load_2d(wb, &p.tm_w1, kx, p.wrows0, wfull(ws));
+            if constexpr (INJ_MMA)
+              tma_load_2d(wb + (r - p.wrows0) * 128, &p.tm_wi, kx, 0, wfull(ws));
           }
         }
-        umma_commit(freeb(st));
       }
-      umma_commit(accb);
+      for (int j = max(0, g - NW); j < g; ++j)
+        mbar_wait_bounded(wfull(j % NW), (j / NW) & 1, p.err, p.limit_ns);
+    }
+  } else if (warp == K1_MMA_WARP || warp == K1_MMA1_WARP) {
+    // One warp per weight column block (two issuing threads keep the tensor
+    // pipe fed; the blocks write disjoint accumulator columns).  The whole
+    // warp walks the loop (every lane observes the barriers) and one elected
+    // lane issues; the vote keeps the warp together if a wait expires.
+    const int hh = warp == K1_MMA_WARP ? 0 : 1;
+    if (hh < nh) {
+      const uint32_t id = idesc_bf16(BM, hh ? p.n2 : p.n1);
+      const uint32_t d = tmem + (hh ? p.n1 : 0);
+      bool ok = true;
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int st = kb % NRY;
+        const int g = kb * nh + hh, ws = g % NW;
+        ok = __all_sync(0xffffffffu, mbar_wait_bounded(conv(st), (kb / NRY) & 1, p.err, p.limit_ns));
+        ok = ok && __all_sync(0xffffffffu, mbar_wait_bounded(wfull(ws), (g / NW) & 1, p.err, p.limit_ns));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t ab = sbase + st * RY_BYTES;
+        const uint64_t a_hi = desc_sw128(ab), a_lo = desc_sw128(ab + TILE_BYTES);
+        const uint64_t bd = desc_sw128(sbase + p.off_w + ws * p.w_slot);
+        if (elect_one()) {
+#pragma unroll
+          for (int ks = 0; ks < BK / 16; ++ks) {
+            umma_bf16(d, a_hi + 2u * ks, bd + 2u * ks, id, (kb | ks) != 0);
+            if (!p.fold) umma_bf16(d, a_lo + 2u * ks, bd + 2u * ks, id, 1);
+          }
+          umma_commit(wfree(ws));
+          umma_commit(ryfree(st));
+        }
+        __syncwarp();
+      }
+      // the accumulator is complete (or abandoned) once every issued MMA is
+      if (elect_one()) umma_commit(accb);
+      __syncwarp();
       mbar_wait_bounded(accb, 0, p.err, p.limit_ns);
     }
-  } else {
+  } else if (warp < K1_CONV_WARPS) {
     // ---------------- converters: warps 0-7.  Thread (warp w, lane l) owns
     // channel chunk l & 7 (8 channels) of every K block and the four rows
     // 4w + (l >> 3) + 32 pp, pp < 4.  In the 128-byte swizzled tile chunk c of
@@ -224,20 +259,20 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     }
     bool ok = true;
     for (int kb = 0; kb < nkb; ++kb) {
-      const int st = kb % NST;
-      ok = mbar_wait_bounded(full(st), (kb / NST) & 1, p.err, p.limit_ns);
+      const int st = kb % NRY;
+      ok = mbar_wait_bounded(ryfull(st), (kb / NRY) & 1, p.err, p.limit_ns);
       if (!ok) break;
-      unsigned char* sb = smem + st * L.stage;
+      unsigned char* sb = smem + st * RY_BYTES;
       const int col = (kb0 + kb) * BK + ch * 8;   // channel within the stream
       float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(smem + L.off_wn + st * 128 + ch * 16), f);
+      unpack8(*reinterpret_cast<const uint4*>(smem + p.off_wn + st * 128 + ch * 16), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] += 1.0f;
       float wi[INJ_MMA ? 1 : HC][8];
       if constexpr (!INJ_MMA) {
 #pragma unroll
         for (int j = 0; j < HC; ++j)
-          unpack8(*reinterpret_cast<const uint4*>(sb + L.off_wi + j * 128 + ch * 16), wi[j]);
+          unpack8(*reinterpret_cast<const uint4*>(smem + p.off_wic + (st * HC + j) * 128 + ch * 16), wi[j]);
       }
 #pragma unroll
       for (int pp = 0; pp < 4; ++pp) {
@@ -371,7 +406,7 @@ constexpr int RED_THREADS = 256;
 // of squares and its column's HC * S partial products together (a single
 // round trip to memory), forms rrms_s itself and writes its four outputs.
 template <int HC>
-__global__ void __launch_bounds__(RED_THREADS)
+__global__ void __launch_bounds__(RED_THREADS, 4)
     k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
                      float* __restrict__ rrms, float* __restrict__ lora,
                      float* __restrict__ inj_next, bf16_t* __restrict__ hh,
@@ -479,15 +514,6 @@ __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   if constexpr (ROWB == 128) return row * 128 + ((chunk ^ (row & 7)) << 4);
   else if constexpr (ROWB == 64) return row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4);
   else return row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4);
-}
-
-// One lane of the (converged) warp; used for the single-thread tcgen05 issue.
-__device__ __forceinline__ bool elect_one() {
-  uint32_t pred;
-  asm volatile(
-      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(pred));
-  return pred != 0;
 }
 
 template <int HCT>
@@ -802,11 +828,24 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const uint64_t dy[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(M)};
     const uint64_t sy[1] = {static_cast<uint64_t>(c.HS) * 2};
     if (!make_tmap_bf16(&p.tm_y, c.y, 2, dy, sy, bT, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
-    p.nwbox = c.r > 256 ? 2 : 1;
-    p.wbox_rows = c.r / p.nwbox;
+    // MMA column blocks over the B tile (r rows of Wd, then 16 inject rows
+    // when the inject products run on the tensor cores)
+    const int ntot = c.r + (inj_mma ? WI_ROWS : 0);
+    if (ntot <= 256) {
+      p.n1 = ntot;
+      p.n2 = 0;
+      p.wrows0 = c.r;
+    } else {
+      p.n1 = ((ntot / 2) + 15) / 16 * 16;
+      p.n2 = ntot - p.n1;
+      p.wrows0 = p.n1;
+    }
     const uint64_t dw[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(c.r)};
-    const uint32_t bw[2] = {BK, static_cast<uint32_t>(p.wbox_rows)};
-    if (!make_tmap_bf16(&p.tm_w, c.Wd, 2, dw, sR, bw, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    const uint32_t bw0[2] = {BK, static_cast<uint32_t>(p.wrows0)};
+    const uint32_t bw1[2] = {BK, static_cast<uint32_t>(p.n2 > 0 ? c.r - p.wrows0 : 16)};
+    if (!make_tmap_bf16(&p.tm_w0, c.Wd, 2, dw, sR, bw0, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_bf16(&p.tm_w1, c.Wd, 2, dw, sR, bw1, CU_TENSOR_MAP_SWIZZLE_128B))
+      return cudaErrorInvalidValue;
     const uint64_t di[2] = {static_cast<uint64_t>(c.K), static_cast<uint64_t>(c.HC)};
     const uint32_t bi[2] = {BK, static_cast<uint32_t>(inj_mma ? WI_ROWS : c.HC)};
     if (!make_tmap_bf16(&p.tm_wi, c.Wi, 2, di, sR, bi,
@@ -826,25 +865,29 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.fold = c.fold;
     p.S = S;
     p.nkb = nkb;
-    // MMA column blocks over the B tile (r rows of Wd, then 16 inject rows)
-    const int ntot = c.r + (inj_mma ? WI_ROWS : 0);
-    if (ntot <= 256) {
-      p.n1 = ntot;
-      p.n2 = 0;
-    } else {
-      p.n1 = ((ntot / 2) + 15) / 16 * 16;
-      p.n2 = ntot - p.n1;
+    // shared memory: [R/y ring | weight ring | Wnorm slices | Wi rows (CUDA-core
+    // inject) | barriers | row sums of squares | row inject sums]; the deepest
+    // rings that fit
+    p.w_slot = static_cast<uint32_t>((std::max(p.n1, p.n2) * 128 + 1023) / 1024 * 1024);
+    const int depths[5][2] = {{4, 4}, {4, 3}, {3, 3}, {3, 2}, {2, 2}};
+    size_t smem = 0;
+    for (const auto& dpt : depths) {
+      p.nry = dpt[0];
+      p.nw = dpt[1];
+      p.off_w = static_cast<uint32_t>(p.nry) * RY_BYTES;
+      p.off_wn = p.off_w + static_cast<uint32_t>(p.nw) * p.w_slot;
+      p.off_wic = p.off_wn + static_cast<uint32_t>(p.nry) * 128u;
+      p.off_bar = p.off_wic + (inj_mma ? 0u : static_cast<uint32_t>(p.nry * c.HC) * 128u);
+      p.off_rowss = p.off_bar + K1_BAR_BYTES;
+      p.off_rowinj = p.off_rowss + BM * 4;
+      smem = p.off_rowinj + (inj_mma ? 0u : static_cast<uint32_t>(BM * c.HC) * 4u) + 1024;
+      if (smem <= static_cast<size_t>(dev.smem_optin)) break;
     }
-    p.nst = 3;
-    while (p.nst > 2 && k1_smem(c.r, c.HC, inj_mma, p.nst).total + 1024 > static_cast<uint32_t>(dev.smem_optin))
-      --p.nst;
-    const K1Smem L = k1_smem(c.r, c.HC, inj_mma, p.nst);
-    p.stage_bytes = L.stage;
+    if (smem > static_cast<size_t>(dev.smem_optin) || p.nry > K1_MAX_RY || p.nw > K1_MAX_W)
+      return cudaErrorNotSupported;
     p.tmem_cols = pow2_cols(ntot);
     p.err = ws.err;
     p.limit_ns = 1000ull * 1000 * 1000;
-    const size_t smem = L.total + 1024;
-    if (smem > static_cast<size_t>(dev.smem_optin)) return cudaErrorNotSupported;
     cudaError_t e = cudaSuccess;
     const int grid = n_mt * c.HC * S;
 #define HCGR_K1(HCV)                                                                        \
