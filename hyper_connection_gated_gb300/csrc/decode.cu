@@ -471,13 +471,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       const bool valid = inj_row ? n < n_out : rt < g.rows_w;
       const int jn = n / g.Qn, qn = n - jn * g.Qn;
       uint32_t h0[8], l0[8], h1[8], l1[8];
-      tmem_ld8(tl + t * Nd + m0, h0);
-      tmem_ld8(tl + t * Nd + Nt + m0, l0);
-      if (two) {
-        tmem_ld8(tl + (g.ntd + t) * Nd + m0, h1);
-        tmem_ld8(tl + (g.ntd + t) * Nd + Nt + m0, l1);
-      }
-      tmem_ld_wait();
+      if (two)
+        tmem_ld8x4_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, tl + (g.ntd + t) * Nd + m0,
+                        tl + (g.ntd + t) * Nd + Nt + m0, h0, l0, h1, l1);
+      else
+        tmem_ld8x2_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, h0, l0);
       if (valid) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
@@ -690,9 +688,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         const int tu = item / nmc, m0 = (item - tu * nmc) * 8;
         const int i = tu * 128 + 32 * q4 + lane;               // row (stream, channel)
         uint32_t v0[8], v1[8];
-        tmem_ld8(tl + tu * Nu + m0, v0);
-        if (nub > 1) tmem_ld8(tl + (g.ntu + tu) * Nu + m0, v1);
-        tmem_ld_wait();
+        if (nub > 1) tmem_ld8x2_wait(tl + tu * Nu + m0, tl + (g.ntu + tu) * Nu + m0, v0, v1);
+        else tmem_ld8_wait(tl + tu * Nu + m0, v0);
         if (i < g.rows_u) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)

@@ -353,8 +353,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       float injv[HC];
       if constexpr (INJ_MMA) {
         uint32_t acc[16];
-        tmem_ld16(tl + r, acc);
-        tmem_ld_wait();
+        tmem_ld16_wait(tl + r, acc);
 #pragma unroll
         for (int j = 0; j < HC; ++j) injv[j] = __uint_as_float(acc[j]);
       } else {
@@ -371,8 +370,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       const int cols = r / 2;
       for (int c0 = 0; c0 < cols; c0 += 16) {
         uint32_t acc[16];
-        tmem_ld16(tl + half * cols + c0, acc);
-        tmem_ld_wait();
+        tmem_ld16_wait(tl + half * cols + c0, acc);
         if (v) {
 #pragma unroll
           for (int e = 0; e < 16; e += 4)
@@ -666,21 +664,15 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
       float2 acc[CPT / 2];
 #pragma unroll
       for (int e = 0; e < CPT / 2; ++e) acc[e] = make_float2(0.f, 0.f);
-      uint32_t gv[2][CPT];
-      if constexpr (CPT == 32) tmem_ld32(tbase, gv[0]);
-      else tmem_ld16(tbase, gv[0]);
+      uint32_t gv[CPT];
       bool ok = true;
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss) {
         const int q = (n + ss) % nr2;
         ok = __all_sync(0xffffffffu, mbar_wait_bounded(r2full(q), ((n + ss) / nr2) & 1, p.err, p.limit_ns));
-        tmem_ld_wait();
         if (!ok) break;
-        // the next stream's gates load while this one is processed
-        if (ss + 1 < HC) {
-          if constexpr (CPT == 32) tmem_ld32(tbase + (ss + 1) * NCU, gv[(ss + 1) & 1]);
-          else tmem_ld16(tbase + (ss + 1) * NCU, gv[(ss + 1) & 1]);
-        }
+        if constexpr (CPT == 32) tmem_ld32_wait(tbase + ss * NCU, gv);
+        else tmem_ld16_wait(tbase + ss * NCU, gv);
         const unsigned char* rb = smem + p.off_r2 + q * BOXB;
         const float* wb = reinterpret_cast<const float*>(smem + p.off_w1 + q * 256u) + half * CPT;
         const float2 rr2 = make_float2(rr[ss], rr[ss]);
@@ -696,8 +688,8 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
           for (int e = 0; e < 4; ++e) {
             // xn = R2 * rrms * (1 + Wnorm); sigmoid(G) = 1/2 + tanh(G / 2) / 2
             const float2 xn = __fmul2_rn(__fmul2_rn(make_float2(lo_bf16(rw[e]), hi_bf16(rw[e])), rr2), w[e]);
-            const float2 th = make_float2(tanh_approx(__uint_as_float(gv[ss & 1][8 * j + 2 * e])),
-                                          tanh_approx(__uint_as_float(gv[ss & 1][8 * j + 2 * e + 1])));
+            const float2 th = make_float2(tanh_approx(__uint_as_float(gv[8 * j + 2 * e])),
+                                          tanh_approx(__uint_as_float(gv[8 * j + 2 * e + 1])));
             const float2 sg = __ffma2_rn(th, make_float2(0.5f, 0.5f), make_float2(0.5f, 0.5f));
             acc[4 * j + e] = __ffma2_rn(sg, xn, acc[4 * j + e]);
           }
