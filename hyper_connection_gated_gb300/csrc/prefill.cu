@@ -400,6 +400,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // columns).
 constexpr int RED_THREADS = 256;
 
+// 1 / (1 + e^-u) with the fast exponential and division (a few ulp; the
+// result is rounded to bf16 next).  e^-u overflowing to +inf gives 0.
+__device__ __forceinline__ float sigmoid_fast(float u) { return __fdividef(1.0f, 1.0f + __expf(-u)); }
+
 // One thread per (token row, float4 column): it loads the row's partial sums
 // of squares and its column's HC * S partial products together (a single
 // round trip to memory), forms rrms_s itself and writes its four outputs.
@@ -409,7 +413,7 @@ __global__ void __launch_bounds__(RED_THREADS, 4)
                      float* __restrict__ rrms, float* __restrict__ lora,
                      float* __restrict__ inj_next, bf16_t* __restrict__ hh,
                      const bf16_t* __restrict__ Wnorm, float* __restrict__ w1, int M, int S,
-                     int r, int np, int HS, float eps) {
+                     int r, int np, int HS, float inv_hs, float eps) {
   const int tid = threadIdx.x;
   const int K = HC * HS;
   for (int k = blockIdx.x * RED_THREADS + tid; k < K; k += gridDim.x * RED_THREADS)
@@ -424,21 +428,33 @@ __global__ void __launch_bounds__(RED_THREADS, 4)
   const float* qrow = sumsq + static_cast<int64_t>(m) * ns;
   float4 a[HC];
   float q[HC];
+  if (S == 1) {
+    // one partial per stream: every load issues before any is used
 #pragma unroll
-  for (int ss = 0; ss < HC; ++ss) {
-    a[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
-    q[ss] = 0.f;
-    for (int c = 0; c < S; ++c) {
-      const float4 v = *reinterpret_cast<const float4*>(prow + (ss * S + c) * np);
-      a[ss].x += v.x; a[ss].y += v.y; a[ss].z += v.z; a[ss].w += v.w;
-      q[ss] += qrow[ss * S + c];
+    for (int ss = 0; ss < HC; ++ss) {
+      a[ss] = __ldcs(reinterpret_cast<const float4*>(prow + ss * np));
+      q[ss] = qrow[ss];
+    }
+  } else {
+#pragma unroll
+    for (int ss = 0; ss < HC; ++ss) {
+      a[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
+      q[ss] = 0.f;
+      for (int c = 0; c < S; ++c) {
+        const float4 v = __ldcs(reinterpret_cast<const float4*>(prow + (ss * S + c) * np));
+        a[ss].x += v.x; a[ss].y += v.y; a[ss].z += v.z; a[ss].w += v.w;
+        q[ss] += qrow[ss * S + c];
+      }
     }
   }
   const float inv_hc = 1.0f / static_cast<float>(HC);
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int ss = 0; ss < HC; ++ss) {
-    const float rs = 1.0f / sqrtf(q[ss] / static_cast<float>(HS) + eps);
+    // 1/sqrt by the hardware estimate and one Newton step (~1 ulp)
+    const float v = fmaf(q[ss], inv_hs, eps);
+    float rs = rsqrtf(v);
+    rs = rs * fmaf(-0.5f * v * rs, rs, 1.5f);
     if (n == 0) rrms[static_cast<int64_t>(m) * HC + ss] = rs;
     acc.x = fmaf(rs, a[ss].x, acc.x); acc.y = fmaf(rs, a[ss].y, acc.y);
     acc.z = fmaf(rs, a[ss].z, acc.z); acc.w = fmaf(rs, a[ss].w, acc.w);
@@ -447,8 +463,8 @@ __global__ void __launch_bounds__(RED_THREADS, 4)
     *reinterpret_cast<float4*>(lora + static_cast<int64_t>(m) * r + n) = acc;
     const float u0 = acc.x * inv_hc, u1 = acc.y * inv_hc, u2 = acc.z * inv_hc, u3 = acc.w * inv_hc;
     uint2 hv;
-    hv.x = pack2(0.5f * (u0 * sigmoidf_dev(u0)), 0.5f * (u1 * sigmoidf_dev(u1)));
-    hv.y = pack2(0.5f * (u2 * sigmoidf_dev(u2)), 0.5f * (u3 * sigmoidf_dev(u3)));
+    hv.x = pack2(0.5f * (u0 * sigmoid_fast(u0)), 0.5f * (u1 * sigmoid_fast(u1)));
+    hv.y = pack2(0.5f * (u2 * sigmoid_fast(u2)), 0.5f * (u3 * sigmoid_fast(u3)));
     *reinterpret_cast<uint2*>(hh + static_cast<int64_t>(m) * r + n) = hv;
   } else {
     const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
@@ -903,7 +919,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   case HCV:                                                                                  \
     k1_reduce_kernel<HCV><<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,     \
                                                           c.inj_next, h, c.Wnorm, w1, M, S,  \
-                                                          c.r, np, c.HS, c.eps);             \
+                                                          c.r, np, c.HS, 1.0f / c.HS, c.eps);\
     break;
     switch (c.HC) {
       HCGR_RED(1) HCGR_RED(2) HCGR_RED(3) HCGR_RED(4) HCGR_RED(5) HCGR_RED(6) HCGR_RED(7)
