@@ -308,6 +308,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // swizzled layout (16-byte unit u of row m of a chunk at (u ^ (m & 7)) * 16;
   // hi in rows m, lo in rows Nt + m)
   const int nu = g.nkc * 8;                                    // 16-byte units per row
+  const float inv_hc0 = 1.0f / static_cast<float>(HC);
 #pragma unroll 1
   for (int it = tid; it < Nt * nu; it += NT) {
     const int m = it / nu, un = it - m * nu;
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     float ss = 0.f;
     if (m < M && ch < nkv) {
       const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
-      const float iw = 2.0f * sigmoidf_dev(c.inj[m * c.ld_inj + s] / static_cast<float>(HC));
+      const float iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc0);
       float rv[8], yv[8], wv[8], a[8];
       unpack8(__ldg(reinterpret_cast<const uint4*>(c.R + kk)), rv);
       unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
@@ -399,7 +400,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     const int n_all = n_r + n_y + n_w;
 #pragma unroll 1
     for (int i = tid; i < n_iw; i += NT)
-      s_iw[i] = 2.0f * sigmoidf_dev(c.inj[(i / HC) * c.ld_inj + (i % HC)] / static_cast<float>(HC));
+      s_iw[i] = combine_weight(c.inj[(i / HC) * c.ld_inj + (i % HC)], inv_hc0);
 #pragma unroll 1
     for (int i0 = tid; i0 < n_all; i0 += XU * NT) {
       uint32_t v[XU];
@@ -545,7 +546,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     ok = __syncthreads_and(got);
     if (!ok) break;
     if (tid < HC) {
-      const float rr = 1.0f / sqrtf(s_red[tid * g.row + g.Qn] / static_cast<float>(HS) + c.eps);
+      const float rr = rsqrt_nr(fmaf(s_red[tid * g.row + g.Qn], __fdividef(1.0f, static_cast<float>(HS)), c.eps));
       s_rl[tid] = rr;
       if (jn == 0) c.rrms[m * HC + tid] = rr;
     }
@@ -571,7 +572,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       if (n0 < r) {   // r is even: n0 + 1 < r too
         const float u0 = v[0] * inv_hc, u1 = v[1] * inv_hc;
         st_relaxed_u32(gat + m * g.L2w + n0 / 2,
-                       pack2(u0 * sigmoidf_dev(u0), u1 * sigmoidf_dev(u1)));
+                       pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1)));
       }
     }
     if (jn == 0) {
@@ -694,7 +695,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll
           for (int e = 0; e < 8; ++e)
             if (m0 + e < M)
-              s_g[(m0 + e) * g.rows_u + i] = sigmoidf_dev(
+              s_g[(m0 + e) * g.rows_u + i] = sigmoid_fast(
                   __uint_as_float(v0[e]) + (nub > 1 ? __uint_as_float(v1[e]) : 0.f));
         }
       }

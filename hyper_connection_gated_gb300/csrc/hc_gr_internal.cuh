@@ -528,7 +528,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-__device__ __forceinline__ float sigmoidf_dev(float v) { return 1.0f / (1.0f + expf(-v)); }
+// 1 / (1 + e^-u) with the fast exponential and division (a few ulp);
+// e^-u overflowing to +inf gives 0.
+__device__ __forceinline__ float sigmoid_fast(float u) { return __fdividef(1.0f, 1.0f + __expf(-u)); }
+// COMBINE weight iw = 2 sigmoid(inj / HC), inv_hc = 1 / HC.  Decode and
+// prefill form it the same way, so their R2 agree bit for bit.
+__device__ __forceinline__ float combine_weight(float inj, float inv_hc) {
+  return 2.0f * sigmoid_fast(inj * inv_hc);
+}
+// 1 / sqrt(v): hardware estimate plus one Newton step (~1 ulp).
+__device__ __forceinline__ float rsqrt_nr(float v) {
+  const float y = rsqrtf(v);
+  return y * fmaf(-0.5f * v * y, y, 1.5f);
+}
 
 #endif  // __CUDACC__
 

@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     for (int pp = 0; pp < 4; ++pp) {
       const int m = m0 + rbase + 32 * pp;
       valid[pp] = m < p.M;
-      iw[pp] = valid[pp] ? 2.0f * sigmoidf_dev(p.inj[m * p.ld_inj + s] / static_cast<float>(HC)) : 0.f;
+      iw[pp] = valid[pp] ? combine_weight(p.inj[m * p.ld_inj + s], 1.0f / static_cast<float>(HC)) : 0.f;
       ss[pp] = 0.f;
 #pragma unroll
       for (int j = 0; j < HC; ++j) ij[pp][j] = 0.f;
@@ -400,9 +400,6 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // columns).
 constexpr int RED_THREADS = 256;
 
-// 1 / (1 + e^-u) with the fast exponential and division (a few ulp; the
-// result is rounded to bf16 next).  e^-u overflowing to +inf gives 0.
-__device__ __forceinline__ float sigmoid_fast(float u) { return __fdividef(1.0f, 1.0f + __expf(-u)); }
 
 // One thread per (token row, float4 column): it loads the row's partial sums
 // of squares and its column's HC * S partial products together (a single
@@ -451,10 +448,7 @@ __global__ void __launch_bounds__(RED_THREADS, 4)
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int ss = 0; ss < HC; ++ss) {
-    // 1/sqrt by the hardware estimate and one Newton step (~1 ulp)
-    const float v = fmaf(q[ss], inv_hs, eps);
-    float rs = rsqrtf(v);
-    rs = rs * fmaf(-0.5f * v * rs, rs, 1.5f);
+    const float rs = rsqrt_nr(fmaf(q[ss], inv_hs, eps));
     if (n == 0) rrms[static_cast<int64_t>(m) * HC + ss] = rs;
     acc.x = fmaf(rs, a[ss].x, acc.x); acc.y = fmaf(rs, a[ss].y, acc.y);
     acc.z = fmaf(rs, a[ss].z, acc.z); acc.w = fmaf(rs, a[ss].w, acc.w);
