@@ -262,10 +262,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     tma_load_3d(ubase + slot * g.slot_u, &p.tm_wu, q * 64, cp0, 0, full_u(slot));
   };
 
-  // Weight copies first (they do not depend on the previous kernel): thread
-  // 0 initialises the barriers, then lane 0 of warp w issues box w (down
-  // boxes first, then up chunks), so the issue latencies overlap; warp 15
-  // takes the call ticket and warp 3 allocates TMEM meanwhile.
+  // Down-weight copies first (they do not depend on the previous kernel):
+  // thread 0 initialises the barriers, then lane 0 of warp w issues down box
+  // w, so the issue latencies overlap; warp 15 takes the call ticket and warp
+  // 3 allocates TMEM meanwhile.
   const int pre_w = min(g.nsl_w, nbox), pre_u = min(g.nsl_u, nub);
   int issued_w = pre_w, issued_u = pre_u;   // kept by thread 0, which drains them
   if (tid == 0) {
@@ -284,8 +284,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         prefetch_tmap(&p.tm_w);
         issue_w(k);
       } else {
-        prefetch_tmap(&p.tm_wu);
-        issue_u(k - pre_w);
+        prefetch_tmap(&p.tm_wu);   // the up boxes are issued after COMBINE (step 2)
       }
     }
   } else if (warp == NW - 1 && lane == 1) {
@@ -303,6 +302,31 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   }
   // inputs and outputs may belong to the previous kernel in the stream
   grid_dep_wait();
+
+  // Inputs of this CTA's channel range for the final mix -- R, y, Wnorm in
+  // channel pairs, and inj (iw is formed from it later) -- copied
+  // asynchronously now, so that their latency hides behind COMBINE and the
+  // down MMAs.
+  {
+    const int np = nc / 2;
+    const int n_iw = M * HC, n_r = M * HC * np, n_y = M * np, n_w = HC * np;
+#pragma unroll 1
+    for (int i = tid; i < n_iw + n_r + n_y + n_w; i += NT) {
+      if (i < n_iw) {
+        cp_async4(s_iw + i, c.inj + (i / HC) * c.ld_inj + (i % HC));
+      } else if (i < n_iw + n_r) {
+        const int j = i - n_iw, row = j / np, cc = 2 * (j - row * np);   // row = m * HC + stream
+        const int m = row / HC, ss = row - m * HC;
+        cp_async4(s_x3r + row * g.nc_max + cc, c.R + static_cast<int64_t>(m) * K + ss * HS + cp0 + cc);
+      } else if (i < n_iw + n_r + n_y) {
+        const int j = i - n_iw - n_r, m = j / np, cc = 2 * (j - m * np);
+        cp_async4(s_x3y + m * g.nc_max + cc, c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
+      } else {
+        const int j = i - n_iw - n_r - n_y, ss = j / np, cc = 2 * (j - ss * np);
+        cp_async4(s_x3w + ss * g.nc_max + cc, c.Wnorm + ss * HS + cp0 + cc);
+      }
+    }
+  }
 
   // --- step 1: COMBINE on this CTA's slice, R2 stored, MMA operands in the
   // swizzled layout (16-byte unit u of row m of a chunk at (u ^ (m & 7)) * 16;
@@ -383,6 +407,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     if (!okm) *s_mma_ok = 0;
     umma_commit(barD);
   } else if (tid == 0) {
+    // the up-weight boxes: requested only now, so that the down boxes, which
+    // the next MMAs need, do not share this SM's copy bandwidth with them
+#pragma unroll 1
+    for (int q = 0; q < pre_u; ++q) issue_u(q);
     // ring refills: a slot is free once the MMAs that read it have completed
 #pragma unroll 1
     for (int i = pre_w; i < nbox; ++i) {
@@ -392,45 +420,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       ++issued_w;
     }
   }
-  // meanwhile: inputs of this CTA's channel range for the final mix (iw,
-  // and R, y, Wnorm in channel pairs, XU loads in flight per thread)
-  {
-    const int np = nc / 2;
-    const int n_iw = M * HC, n_r = M * HC * np, n_y = M * np, n_w = HC * np;
-    const int n_all = n_r + n_y + n_w;
+  // the final mix's inputs (copied since the prologue) have landed; iw from inj
+  cp_async_wait_all();
 #pragma unroll 1
-    for (int i = tid; i < n_iw; i += NT)
-      s_iw[i] = combine_weight(c.inj[(i / HC) * c.ld_inj + (i % HC)], inv_hc0);
-#pragma unroll 1
-    for (int i0 = tid; i0 < n_all; i0 += XU * NT) {
-      uint32_t v[XU];
-      uint32_t* dst[XU];
-#pragma unroll
-      for (int k = 0; k < XU; ++k) {
-        const int i = i0 + k * NT;
-        const unsigned int* src = nullptr;
-        dst[k] = nullptr;
-        if (i < n_r) {
-          const int row = i / np, cc = 2 * (i - row * np);     // row = m * HC + stream
-          const int m = row / HC, ss = row - m * HC;
-          src = reinterpret_cast<const unsigned int*>(c.R + static_cast<int64_t>(m) * K + ss * HS + cp0 + cc);
-          dst[k] = reinterpret_cast<uint32_t*>(s_x3r + row * g.nc_max + cc);
-        } else if (i < n_r + n_y) {
-          const int j = i - n_r, m = j / np, cc = 2 * (j - m * np);
-          src = reinterpret_cast<const unsigned int*>(c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
-          dst[k] = reinterpret_cast<uint32_t*>(s_x3y + m * g.nc_max + cc);
-        } else if (i < n_all) {
-          const int j = i - n_r - n_y, ss = j / np, cc = 2 * (j - ss * np);
-          src = reinterpret_cast<const unsigned int*>(c.Wnorm + ss * HS + cp0 + cc);
-          dst[k] = reinterpret_cast<uint32_t*>(s_x3w + ss * g.nc_max + cc);
-        }
-        v[k] = src ? __ldg(src) : 0u;
-      }
-#pragma unroll
-      for (int k = 0; k < XU; ++k)
-        if (dst[k]) *dst[k] = v[k];
-    }
-  }
+  for (int i = tid; i < M * HC; i += NT) s_iw[i] = combine_weight(s_iw[i], inv_hc0);
   // and the sum of squares, and the non-product words of this CTA's
   // piece of every reduce-scatter block ([Qn partials][sum of squares][3 pad
   // words], partials past n_out zero)

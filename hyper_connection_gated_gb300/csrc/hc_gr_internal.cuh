@@ -176,6 +176,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// 4-byte asynchronous copy global -> shared (cp.async, L1-allocating); the
+// copies of a thread complete at its next cp_async_wait_all().
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gsrc) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;"
+               ::"r"(smem_u32(smem_dst)), "l"(__cvta_generic_to_global(gsrc)) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // 1-D bulk async copy global -> shared, completion counted on an mbarrier.
 // src, dst 16-byte aligned; bytes a multiple of 16.
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
