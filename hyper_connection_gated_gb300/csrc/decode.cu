@@ -14,8 +14,8 @@
 //      every 128-row tile of the down/inject weight (TMA, 128-byte swizzle):
 //      D[n][m] = sum_{c in slice} W[n, s HS + c] a[m, c].  The hi and lo
 //      terms are stacked as the two halves of the MMA's N dimension (one MMA
-//      per weight tile and k-step), and two threads issue, each for alternate
-//      64-column chunks into its own accumulator copy.
+//      per weight tile and k-step), and one thread per row tile issues (the
+//      issues run side by side; each costs ~100 cycles).
 //      rrms_s is constant over stream s, so lora = sum_s rrms_s sum_{b in s}
 //      D_b is exact: the per-stream factor commutes out of the K-sum.
 //   3. Reduce-scatter: the M (r + HC) outputs are cut into blocks of Qn
@@ -57,6 +57,7 @@ constexpr int NT = 512;              // threads per CTA
 constexpr int NW = NT / 32;
 constexpr int MAX_SLOTS = 8;         // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
+constexpr int DOWN_ISSUERS = 8;      // threads that may issue the down MMAs (one per row tile)
 constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int HDR = 512;             // mbarriers, TMEM address, flags
 constexpr int SMEM_BUDGET = 220 * 1024;
@@ -159,8 +160,10 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     while (2 * g.R <= 32 && 2 * g.R * c.HC * g.nquad <= NT) g.R *= 2;
     g.ppr = (g.P + g.R - 1) / g.R;
     g.L2w = round_up(c.r / 2 + c.HC, 4);     // h pairs, then rrms, then pad words
-    // two accumulator copies (one per issuing thread) for each product
-    const int cols = std::max(2 * g.ntd * g.Nd, 2 * g.ntu * g.Nu);
+    // down: one accumulator per row tile (one issuing thread each); up: two
+    // accumulator copies (one per issuing thread)
+    if (g.ntd > DOWN_ISSUERS) return false;
+    const int cols = std::max(g.ntd * g.Nd, 2 * g.ntu * g.Nu);
     if (cols > 512) return false;
     g.tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
     // all weight tiles resident when they fit, else rings
@@ -271,7 +274,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   if (tid == 0) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
-    mbar_init(barD, 2);
+    mbar_init(barD, DOWN_ISSUERS);
     mbar_init(barG, 2);
     fence_mbar_init();
     *s_mma_ok = 1;
@@ -377,31 +380,31 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
 
-  // --- step 2: the down/inject products on the tensor cores.  Threads 32
-  // and 96 issue, for even and odd chunks, each into its own accumulator
-  // copy, when every box has its own slot; with a ring (whose slots the
-  // issuer hands back) thread 32 alone consumes the boxes, in order, and
-  // thread 0 refills.
+  // --- step 2: the down/inject products on the tensor cores.  When every
+  // box has its own slot, lane 0 of warp 2t + 1 issues the MMAs of row tile t
+  // (all chunks, one accumulator per tile): up to DOWN_ISSUERS threads issue
+  // side by side, each tcgen05.mma issue costing ~100 cycles.  With a ring
+  // (whose slots the issuer hands back) thread 32 alone consumes the boxes,
+  // in order, and thread 0 refills.  Every issuer thread commits barD.
   const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
-  const int nis = g.nsl_w >= nbox ? 2 : 1;          // issuing threads of the down step
-  if (tid == 32 || tid == 96) {
-    const int me = tid == 96 ? 1 : 0;
+  const bool ring = g.nsl_w < nbox;
+  if ((tid & 63) == 32 && (tid >> 6) < DOWN_ISSUERS) {
+    const int me = tid >> 6;
     const uint32_t idesc = idesc_bf16(128, Nd);
     bool okm = true;
 #pragma unroll 1
     for (int i = 0; i < nbox && okm; ++i) {
       const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
-      if (ch % nis != me) continue;
+      if (ring ? me != 0 : t != me) continue;
       const uint32_t ph = (i / g.nsl_w) & 1;
       okm = mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns);
       if (!okm) break;
       tc_fence_after();
       const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
-      const uint32_t d = tmem + (me * g.ntd + t) * Nd;
+      const uint32_t d = tmem + t * Nd;
 #pragma unroll 1
       for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc,
-                  (ch >= nis || ks) ? 1u : 0u);
+        umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc, (ch || ks) ? 1u : 0u);
       umma_commit(free_w(slot));
     }
     if (!okm) *s_mma_ok = 0;
@@ -455,7 +458,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     const int tr = 32 * q4 + lane;                             // row within a tile
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
     const int nmc = Nt / 8;                                    // 8-token chunks
-    const bool two = nis > 1 && nkv > 1;
 #pragma unroll 1
     for (int item = grp; item < g.ntd * nmc; item += NW / 4) {
       const int t = item / nmc, m0 = (item - t * nmc) * 8;
@@ -464,17 +466,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       const int n = inj_row ? r + (tr - g.wi_row) : rt;
       const bool valid = inj_row ? n < n_out : rt < g.rows_w;
       const int jn = n / g.Qn, qn = n - jn * g.Qn;
-      uint32_t h0[8], l0[8], h1[8], l1[8];
-      if (two)
-        tmem_ld8x4_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, tl + (g.ntd + t) * Nd + m0,
-                        tl + (g.ntd + t) * Nd + Nt + m0, h0, l0, h1, l1);
-      else
-        tmem_ld8x2_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, h0, l0);
+      uint32_t h0[8], l0[8];
+      tmem_ld8x2_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, h0, l0);
       if (valid) {
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          float v = __uint_as_float(h0[e]) + __uint_as_float(l0[e]);
-          if (two) v += __uint_as_float(h1[e]) + __uint_as_float(l1[e]);
+          const float v = __uint_as_float(h0[e]) + __uint_as_float(l0[e]);
           if (m0 + e < M)
             st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.G + b) * g.row + qn,
                            xword(v));
