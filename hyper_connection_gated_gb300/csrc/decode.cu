@@ -58,6 +58,7 @@ constexpr int NW = NT / 32;
 constexpr int MAX_SLOTS = 8;         // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
 constexpr int DOWN_ISSUERS = 8;      // threads that may issue the down MMAs (one per row tile)
+constexpr int UP_ISSUERS = 8;        // threads that may issue the gate MMAs (one per Wu chunk)
 constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int HDR = 512;             // mbarriers, TMEM address, flags
 constexpr int SMEM_BUDGET = 220 * 1024;
@@ -70,6 +71,7 @@ struct Geom {
   int nc_max, rows_u, ntu, nchunk_u, slot_u, nsl_u;                    // up weight
   int Qn, Jm, nred, row, nquad, R, ppr, L2w;                           // exchanges
   int tmem_cols;
+  int ncu;                        // gate-MMA issuers (accumulator copies)
   int off_rr, off_iw, off_x3r, off_x3y, off_x3w, off_ssum, off_ss1, off_rl, off_act, off_u,
       off_a;                      // (off_act: [nkc][Nd rows][128 B], hi rows then lo rows)
   int off_red, off_hb, off_g;            // region A once the down weights are consumed
@@ -160,12 +162,7 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     while (2 * g.R <= 32 && 2 * g.R * c.HC * g.nquad <= NT) g.R *= 2;
     g.ppr = (g.P + g.R - 1) / g.R;
     g.L2w = round_up(c.r / 2 + c.HC, 4);     // h pairs, then rrms, then pad words
-    // down: one accumulator per row tile (one issuing thread each); up: two
-    // accumulator copies (one per issuing thread)
-    if (g.ntd > DOWN_ISSUERS) return false;
-    const int cols = std::max(g.ntd * g.Nd, 2 * g.ntu * g.Nu);
-    if (cols > 512) return false;
-    g.tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+    if (g.ntd > DOWN_ISSUERS || g.nchunk_u > UP_ISSUERS) return false;
     // all weight tiles resident when they fit, else rings
     const int nbox = g.ntd * g.nkc;
     bool fits = false;
@@ -175,6 +172,14 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
       if (g.nsl_w > MAX_SLOTS || g.nsl_u > MAX_SLOTS) continue;
       fits = layout(c, g);
     }
+    // down: one accumulator per row tile (one issuing thread each); up: one
+    // accumulator copy per issuing thread -- a thread per Wu chunk when every
+    // chunk has its own slot and the copies fit, else two (the ring's two
+    // slots alternate between them)
+    g.ncu = g.nsl_u >= g.nchunk_u && g.nchunk_u * g.ntu * g.Nu <= 512 ? g.nchunk_u : 2;
+    const int cols = std::max(g.ntd * g.Nd, g.ncu * g.ntu * g.Nu);
+    if (cols > 512) fits = false;
+    g.tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
     // a kernel that allocates TMEM runs one CTA per SM
     if (fits && g.G <= dev.sms) return true;
   }
@@ -275,7 +280,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
     mbar_init(barD, DOWN_ISSUERS);
-    mbar_init(barG, 2);
+    mbar_init(barG, UP_ISSUERS);
     fence_mbar_init();
     *s_mma_ok = 1;
   }
@@ -630,18 +635,19 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     ok = __syncthreads_and(got);
   }
   // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
-  // channel) of this CTA's range; threads 32 and 96 take alternate chunks
-  // into their own accumulator copies (the ring has two slots or none, so
-  // each slot serves one issuer)
+  // channel) of this CTA's range; lane 0 of warp 2k + 1 (k < ncu) issues
+  // chunks k, k + ncu, .. into its own accumulator copy (with a ring, ncu = 2
+  // and each of its two slots serves one issuer).  Every candidate thread
+  // commits barG.
   const bool up_issued = ok && nc > 0;
   if (up_issued) {
-    if (tid == 32 || tid == 96) {
-      const int me = tid == 96 ? 1 : 0;
+    if ((tid & 63) == 32 && (tid >> 6) < UP_ISSUERS) {
+      const int me = tid >> 6;
       tc_fence_after();
       const uint32_t idesc = idesc_bf16(128, Nu);
       bool okm = true;
 #pragma unroll 1
-      for (int q = me; q < nub && okm; q += 2) {
+      for (int q = me; q < nub && okm && me < g.ncu; q += g.ncu) {
         const int slot = q % g.nsl_u;
         const uint32_t ph = (q / g.nsl_u) & 1;
         okm = mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns);
@@ -653,7 +659,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll 1
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
-                      desc_sw128(bq + ks * 32), idesc, (q > 1 || ks) ? 1u : 0u);
+                      desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
         umma_commit(free_u(slot));
       }
       if (!okm) *s_mma_ok = 0;
@@ -678,15 +684,28 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       for (int item = grp; item < g.ntu * nmc; item += NW / 4) {
         const int tu = item / nmc, m0 = (item - tu * nmc) * 8;
         const int i = tu * 128 + 32 * q4 + lane;               // row (stream, channel)
-        uint32_t v0[8], v1[8];
-        if (nub > 1) tmem_ld8x2_wait(tl + tu * Nu + m0, tl + (g.ntu + tu) * Nu + m0, v0, v1);
-        else tmem_ld8_wait(tl + tu * Nu + m0, v0);
+        // sum of the issuers' accumulator copies that hold a chunk
+        const int ncopy = min(g.ncu, nub);
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) v[e] = 0.f;
+#pragma unroll 1
+        for (int k = 0; k < ncopy; k += 2) {
+          uint32_t v0[8], v1[8];
+          if (k + 1 < ncopy) {
+            tmem_ld8x2_wait(tl + (k * g.ntu + tu) * Nu + m0, tl + ((k + 1) * g.ntu + tu) * Nu + m0, v0, v1);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(v0[e]) + __uint_as_float(v1[e]);
+          } else {
+            tmem_ld8_wait(tl + (k * g.ntu + tu) * Nu + m0, v0);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(v0[e]);
+          }
+        }
         if (i < g.rows_u) {
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            if (m0 + e < M)
-              s_g[(m0 + e) * g.rows_u + i] = sigmoid_fast(
-                  __uint_as_float(v0[e]) + (nub > 1 ? __uint_as_float(v1[e]) : 0.f));
+            if (m0 + e < M) s_g[(m0 + e) * g.rows_u + i] = sigmoid_fast(v[e]);
         }
       }
       __syncthreads();
