@@ -281,25 +281,45 @@ def run_ours(args, rank, world):
     tokens_per_step = sum(SWEEP)
     value = tokens_per_step * args.steps * world / (ms / 1e3)
 
-    # e2e through the public API: pinned host inputs in, all outputs back
-    host_in = {M: {k: v[:M].cpu().pin_memory() for k, v in (("R", base["R"]), ("y", base["y"]),
-                                                             ("inj", base["inj"]))}
-               for M in SWEEP}
-    dev_in = {M: {k: torch.empty_like(v, device="cuda") for k, v in host_in[M].items()} for M in SWEEP}
-    host_out = {M: {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs[M][0].items()}
-                for M in SWEEP}
-    h2d = sum(t.numel() * t.element_size() for M in SWEEP for t in host_in[M].values())
-    d2h = sum(t.numel() * t.element_size() for M in SWEEP for t in host_out[M].values())
+    # e2e through the public API: each step copies all of its inputs in with
+    # one host->device copy from a pinned staging buffer and all of its
+    # outputs back with one device->host copy (views carve the buffers)
+    def carve(specs):
+        offs, total = [], 0
+        for shape, dtype in specs:
+            nbytes = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+            offs.append((total, nbytes, shape, dtype))
+            total += (nbytes + 255) // 256 * 256
+        return offs, total
+
+    def views(buf, offs):
+        return [buf[o:o + n].view(dt).view(shape) for o, n, shape, dt in offs]
+
+    in_keys = ("R", "y", "inj")
+    out_keys = tuple(outs[SWEEP[0]][0].keys())
+    in_offs, in_total = carve([(tuple(base[k][:M].shape), base[k].dtype) for M in SWEEP for k in in_keys])
+    out_offs, out_total = carve([(tuple(outs[M][0][k].shape), outs[M][0][k].dtype)
+                                 for M in SWEEP for k in out_keys])
+    host_in_buf = torch.empty(in_total, dtype=torch.uint8).pin_memory()
+    dev_in_buf = torch.empty(in_total, dtype=torch.uint8, device="cuda")
+    host_out_buf = torch.empty(out_total, dtype=torch.uint8).pin_memory()
+    dev_out_buf = torch.empty(out_total, dtype=torch.uint8, device="cuda")
+    hv, dv, dov = views(host_in_buf, in_offs), views(dev_in_buf, in_offs), views(dev_out_buf, out_offs)
+    dev_in, dev_out = {}, {}
+    for i, M in enumerate(SWEEP):
+        for j, k in enumerate(in_keys):
+            hv[i * len(in_keys) + j].copy_(base[k][:M].cpu())
+        dev_in[M] = {k: dv[i * len(in_keys) + j] for j, k in enumerate(in_keys)}
+        dev_out[M] = {k: dov[i * len(out_keys) + j] for j, k in enumerate(out_keys)}
+    h2d, d2h = sum(n for _, n, _, _ in in_offs), sum(n for _, n, _, _ in out_offs)
 
     def e2e_step(j):
         s = sets[j]
+        dev_in_buf.copy_(host_in_buf, non_blocking=True)
         for M in SWEEP:
-            for k, v in host_in[M].items():
-                dev_in[M][k].copy_(v, non_blocking=True)
-            o = op.forward(dev_in[M]["R"], dev_in[M]["y"], dev_in[M]["inj"], s["Wnorm"], s["Wu"],
-                           Wd=s["Wd"], Wi=s["Wi"], out=outs[M][j])
-            for k, v in o.items():
-                host_out[M][k].copy_(v, non_blocking=True)
+            op.forward(dev_in[M]["R"], dev_in[M]["y"], dev_in[M]["inj"], s["Wnorm"], s["Wu"],
+                       Wd=s["Wd"], Wi=s["Wi"], out=dev_out[M])
+        host_out_buf.copy_(dev_out_buf, non_blocking=True)
         torch.cuda.current_stream().synchronize()
 
     with torch.cuda.stream(stream):
