@@ -108,12 +108,6 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
 __device__ __forceinline__ float lo_bf16(uint32_t p) { return __uint_as_float(p << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t p) { return __uint_as_float(p & 0xffff0000u); }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
-
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
@@ -279,22 +273,6 @@ __device__ __forceinline__ void tmem_ld8x2_wait(uint32_t t0, uint32_t t1, uint32
       : "r"(t0), "r"(t1)
       : "memory");
 }
-__device__ __forceinline__ void tmem_ld8x4_wait(uint32_t t0, uint32_t t1, uint32_t t2, uint32_t t3, uint32_t* v0, uint32_t* v1, uint32_t* v2, uint32_t* v3) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%32];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%8,%9,%10,%11,%12,%13,%14,%15}, [%33];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%16,%17,%18,%19,%20,%21,%22,%23}, [%34];\n"
-      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%24,%25,%26,%27,%28,%29,%30,%31}, [%35];\n"
-      "tcgen05.wait::ld.sync.aligned;"
-      : "=r"(v0[0]), "=r"(v0[1]), "=r"(v0[2]), "=r"(v0[3]), "=r"(v0[4]), "=r"(v0[5]),
-        "=r"(v0[6]), "=r"(v0[7]), "=r"(v1[0]), "=r"(v1[1]), "=r"(v1[2]), "=r"(v1[3]),
-        "=r"(v1[4]), "=r"(v1[5]), "=r"(v1[6]), "=r"(v1[7]), "=r"(v2[0]), "=r"(v2[1]),
-        "=r"(v2[2]), "=r"(v2[3]), "=r"(v2[4]), "=r"(v2[5]), "=r"(v2[6]), "=r"(v2[7]),
-        "=r"(v3[0]), "=r"(v3[1]), "=r"(v3[2]), "=r"(v3[3]), "=r"(v3[4]), "=r"(v3[5]),
-        "=r"(v3[6]), "=r"(v3[7])
-      : "r"(t0), "r"(t1), "r"(t2), "r"(t3)
-      : "memory");
-}
 __device__ __forceinline__ void tmem_ld16_wait(uint32_t t0, uint32_t* v) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n"
@@ -340,120 +318,19 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N) {
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
-// Named barrier that also ANDs a predicate over its participants.
-__device__ __forceinline__ bool named_bar_and(int id, int nthreads, bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n"
-      " bar.red.and.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r) : "r"(pred ? 1u : 0u), "r"(id), "r"(nthreads) : "memory");
-  return r != 0;
-}
 // Hardware tanh approximation (one MUFU operation).
 __device__ __forceinline__ float tanh_approx(float x) {
   float t;
   asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
   return t;
 }
-// sigmoid(x) = (1 + tanh(x / 2)) / 2.
-__device__ __forceinline__ float sigmoid_tanh(float x) { return fmaf(0.5f, tanh_approx(0.5f * x), 0.5f); }
 
-// Tiled TMA store shared -> global (bulk-group completion); rows and columns
-// outside the tensor are not written.
-__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, uint32_t src) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
-      ::"l"(tmap), "r"(x), "r"(y), "r"(src) : "memory");
-}
-__device__ __forceinline__ void bulk_commit() {
-  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-// Wait until at most N committed bulk groups still read shared memory.
-template <int N>
-__device__ __forceinline__ void bulk_wait_read() {
-  asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
-}
-template <int N>
-__device__ __forceinline__ void bulk_wait() {
-  asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
-}
-
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void st_release_u32(unsigned* p, unsigned v) {
-  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 __device__ __forceinline__ void st_relaxed_u32(unsigned* p, unsigned v) {
   asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ unsigned atom_add_acq_rel_u32(unsigned* p, unsigned v) {
-  unsigned old;
-  asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-               : "memory");
-  return old;
-}
-
-__device__ __forceinline__ unsigned long long atom_add_release_u64(unsigned long long* p,
-                                                                  unsigned long long v) {
-  unsigned long long old;
-  asm volatile("atom.add.release.gpu.global.u64 %0, [%1], %2;" : "=l"(old) : "l"(p), "l"(v)
-               : "memory");
-  return old;
-}
-__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
 }
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
-__device__ __forceinline__ void fence_acq_rel_gpu() {
-  asm volatile("fence.acq_rel.gpu;" ::: "memory");
-}
-
-// Grid-wide barrier for a cooperative launch of `nblocks` CTAs.  `cnt` is a
-// 64-bit counter used only by grids of exactly this size, so it is a multiple
-// of nblocks whenever a barrier begins: an arriving CTA adds 1 (release, so
-// everything the CTA wrote before the CTA barrier is published), derives the
-// barrier's target from the value it saw, polls with relaxed loads and ends
-// with one acquire fence.  Returns false (all threads of the CTA) when the
-// wait expired or another CTA reported an error; the CTA must then leave.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* cnt, unsigned nblocks, int* err,
-                                             uint64_t limit_ns, int* s_flag) {
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int ok = 1;
-    const unsigned long long old = atom_add_release_u64(cnt, 1ull);
-    const unsigned long long target = (old / nblocks + 1) * nblocks;
-    const long long t0 = clock64();
-    uint32_t it = 0;
-    while (ld_relaxed_u64(cnt) < target) {
-      if ((++it & 31u) == 0) {
-        if (*((volatile int*)err) != DEV_OK) { ok = 0; break; }
-        if (clock64() - t0 > wait_limit_cycles(limit_ns)) {
-          atomicCAS(err, DEV_OK, DEV_TIMEOUT);
-          ok = 0;
-          break;
-        }
-      }
-    }
-    fence_acq_rel_gpu();
-    *s_flag = ok;
-  }
-  __syncthreads();
-  return *s_flag != 0;
-}
-
 // Exchange words: 0xffffffff marks an empty word; a value never equals it.
 constexpr uint32_t XEMPTY = 0xffffffffu;
 
@@ -505,37 +382,6 @@ __device__ __forceinline__ void grid_dep_wait() {
 }
 __device__ __forceinline__ void grid_dep_launch() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-}
-
-// Warp-level bf16 MMA (D += A * B, fp32 accumulate).  Fragment layouts (g =
-// lane / 4, t = lane % 4): A rows g and g+8, column pairs 2t and 2t+8; B
-// column g, row pairs 2t and 2t+8; D rows g, g+8 and columns 2t, 2t+1.
-__device__ __forceinline__ void mma_16816(float* d, uint32_t a0, uint32_t a1, uint32_t a2,
-                                          uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
-      " {%8,%9}, {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_1688(float* d, uint32_t a0, uint32_t a1, uint32_t b0) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6},"
-      " {%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(a1), "r"(b0));
-}
-
-// Orders this thread's earlier generic-proxy accesses (and those it has
-// acquired) before its later async-proxy (TMA / bulk copy) accesses.
-__device__ __forceinline__ void fence_proxy_async_global() {
-  asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  return v;
 }
 
 // 1 / (1 + e^-u) with the fast exponential and division (a few ulp);
