@@ -76,8 +76,8 @@ struct K1Params {
   int64_t ld_inj;
   bf16_t* R2;
   const bf16_t* Wnorm;
-  float* part;        // [M][HC * S][np]: lora columns, then the HC inject columns
-  float* sumsq;       // [M][HC * S] partial sums of R2^2
+  float* part;        // [tile][HC * S][np][128 rows]: lora columns, then the HC inject columns
+  float* sumsq;       // [tile][HC * S][128 rows] partial sums of R2^2
   int M, HS, K, r, np, fold;
   int S;              // K chunks per stream
   int nkb;
@@ -345,10 +345,11 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     tc_fence_after();
     const int q = warp & 3, half = warp >> 2;
     const int erow = 32 * q + lane;
-    const int em = m0 + erow;
-    const bool v = em < p.M;
     const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q) << 16);
-    float* dst = p.part + (static_cast<int64_t>(v ? em : 0) * (HC * p.S) + pid) * p.np;
+    // column-major within the tile: consecutive threads (rows) write
+    // consecutive words, one 128-byte line per warp and column
+    const int64_t tp = static_cast<int64_t>(m0 / BM) * (HC * p.S) + pid;
+    float* dst = p.part + tp * p.np * BM + erow;
     if (ok && half == 0) {
       float injv[HC];
       if constexpr (INJ_MMA) {
@@ -360,24 +361,17 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 #pragma unroll
         for (int j = 0; j < HC; ++j) injv[j] = rowinj[erow * HC + j];
       }
-      if (v) {
-        p.sumsq[static_cast<int64_t>(em) * (HC * p.S) + pid] = rowss[erow];
+      p.sumsq[tp * BM + erow] = rowss[erow];
 #pragma unroll
-        for (int j = 0; j < HC; ++j) dst[r + j] = injv[j];
-      }
+      for (int j = 0; j < HC; ++j) dst[(r + j) * BM] = injv[j];
     }
     if (ok) {
       const int cols = r / 2;
       for (int c0 = 0; c0 < cols; c0 += 16) {
         uint32_t acc[16];
         tmem_ld16_wait(tl + half * cols + c0, acc);
-        if (v) {
 #pragma unroll
-          for (int e = 0; e < 16; e += 4)
-            *reinterpret_cast<float4*>(dst + half * cols + c0 + e) =
-                make_float4(__uint_as_float(acc[e]), __uint_as_float(acc[e + 1]),
-                            __uint_as_float(acc[e + 2]), __uint_as_float(acc[e + 3]));
-        }
+        for (int e = 0; e < 16; ++e) dst[(half * cols + c0 + e) * BM] = __uint_as_float(acc[e]);
       }
     }
   }
@@ -395,76 +389,103 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // partial products), and the up-GEMM operand hh = bf16(SiLU(lora / HC) / 2):
 // the halving is exact and makes K2's accumulator hold G / 2, the argument of
 // tanh in sigmoid(G) = (1 + tanh(G / 2)) / 2.  The grid also writes
-// w1 = 1 + Wnorm in fp32 for K2's epilogue.  Columns go in float4s (np is a
-// multiple of 4 and r of 8, so a float4 never straddles lora and the inject
-// columns).
+// w1 = 1 + Wnorm in fp32 for K2's epilogue.  A block takes a 128-row tile
+// x 16 columns: it reads the column-major partials 512 contiguous bytes per
+// column and stream, and transposes through shared memory to write the
+// row-major outputs in 64-byte row runs.
 constexpr int RED_THREADS = 256;
+constexpr int RED_COLS = 16;          // columns per block (a block covers a whole 128-row tile)
 
-
-// One thread per (token row, float4 column): it loads the row's partial sums
-// of squares and its column's HC * S partial products together (a single
-// round trip to memory), forms rrms_s itself and writes its four outputs.
 template <int HC>
-__global__ void __launch_bounds__(RED_THREADS, 4)
+__global__ void __launch_bounds__(RED_THREADS)
     k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
                      float* __restrict__ rrms, float* __restrict__ lora,
                      float* __restrict__ inj_next, bf16_t* __restrict__ hh,
                      const bf16_t* __restrict__ Wnorm, float* __restrict__ w1, int M, int S,
                      int r, int np, int HS, float inv_hs, float eps) {
+  __shared__ float s_acc[RED_COLS][BM + 1];
   const int tid = threadIdx.x;
+  const int bid = blockIdx.y * gridDim.x + blockIdx.x;
   const int K = HC * HS;
-  for (int k = blockIdx.x * RED_THREADS + tid; k < K; k += gridDim.x * RED_THREADS)
+  for (int k = bid * RED_THREADS + tid; k < K; k += gridDim.x * gridDim.y * RED_THREADS)
     w1[k] = 1.0f + bf16_to_f32(Wnorm[k]);
-  const int np4 = np / 4;
-  const int64_t idx = static_cast<int64_t>(blockIdx.x) * RED_THREADS + tid;
-  if (idx >= static_cast<int64_t>(M) * np4) return;
-  const int m = static_cast<int>(idx / np4);
-  const int n = static_cast<int>(idx % np4) * 4;
+  const int tile = blockIdx.y, n0 = blockIdx.x * RED_COLS;
+  const int rr = tid & (BM - 1), cw = tid >> 7;        // row within the tile; column phase 0/1
   const int ns = HC * S;
-  const float* prow = part + static_cast<int64_t>(m) * ns * np + n;
-  const float* qrow = sumsq + static_cast<int64_t>(m) * ns;
-  float4 a[HC];
+  const int64_t tb = static_cast<int64_t>(tile) * ns;
+  // the row's partial sums of squares and the columns' partial products:
+  // with one K chunk per stream (the usual case) every load issues before
+  // any is used
   float q[HC];
+  float pv[RED_COLS / 2][HC];
   if (S == 1) {
-    // one partial per stream: every load issues before any is used
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss) {
-      a[ss] = __ldcs(reinterpret_cast<const float4*>(prow + ss * np));
-      q[ss] = qrow[ss];
+    for (int ss = 0; ss < HC; ++ss) q[ss] = sumsq[(tb + ss) * BM + rr];
+#pragma unroll
+    for (int j = 0; j < RED_COLS / 2; ++j) {
+      const int n = min(n0 + cw + 2 * j, np - 1);
+#pragma unroll
+      for (int ss = 0; ss < HC; ++ss) pv[j][ss] = part[((tb + ss) * np + n) * BM + rr];
     }
   } else {
+    // K chunk by K chunk, each chunk's loads all in flight together
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss) {
-      a[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
-      q[ss] = 0.f;
-      for (int c = 0; c < S; ++c) {
-        const float4 v = __ldcs(reinterpret_cast<const float4*>(prow + (ss * S + c) * np));
-        a[ss].x += v.x; a[ss].y += v.y; a[ss].z += v.z; a[ss].w += v.w;
-        q[ss] += qrow[ss * S + c];
+    for (int ss = 0; ss < HC; ++ss) q[ss] = 0.f;
+#pragma unroll
+    for (int j = 0; j < RED_COLS / 2; ++j)
+#pragma unroll
+      for (int ss = 0; ss < HC; ++ss) pv[j][ss] = 0.f;
+    for (int c = 0; c < S; ++c) {
+      float qc[HC], vc[RED_COLS / 2][HC];
+#pragma unroll
+      for (int ss = 0; ss < HC; ++ss) qc[ss] = sumsq[(tb + ss * S + c) * BM + rr];
+#pragma unroll
+      for (int j = 0; j < RED_COLS / 2; ++j) {
+        const int n = min(n0 + cw + 2 * j, np - 1);
+#pragma unroll
+        for (int ss = 0; ss < HC; ++ss) vc[j][ss] = part[((tb + ss * S + c) * np + n) * BM + rr];
       }
+#pragma unroll
+      for (int ss = 0; ss < HC; ++ss) q[ss] += qc[ss];
+#pragma unroll
+      for (int j = 0; j < RED_COLS / 2; ++j)
+#pragma unroll
+        for (int ss = 0; ss < HC; ++ss) pv[j][ss] += vc[j][ss];
     }
   }
-  const float inv_hc = 1.0f / static_cast<float>(HC);
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float rs[HC];
 #pragma unroll
-  for (int ss = 0; ss < HC; ++ss) {
-    const float rs = rsqrt_nr(fmaf(q[ss], inv_hs, eps));
-    if (n == 0) rrms[static_cast<int64_t>(m) * HC + ss] = rs;
-    acc.x = fmaf(rs, a[ss].x, acc.x); acc.y = fmaf(rs, a[ss].y, acc.y);
-    acc.z = fmaf(rs, a[ss].z, acc.z); acc.w = fmaf(rs, a[ss].w, acc.w);
+  for (int ss = 0; ss < HC; ++ss) rs[ss] = rsqrt_nr(fmaf(q[ss], inv_hs, eps));
+  const int m_row = tile * BM + rr;
+  if (blockIdx.x == 0 && cw == 0 && m_row < M) {
+#pragma unroll
+    for (int ss = 0; ss < HC; ++ss) rrms[static_cast<int64_t>(m_row) * HC + ss] = rs[ss];
   }
-  if (n < r) {
-    *reinterpret_cast<float4*>(lora + static_cast<int64_t>(m) * r + n) = acc;
-    const float u0 = acc.x * inv_hc, u1 = acc.y * inv_hc, u2 = acc.z * inv_hc, u3 = acc.w * inv_hc;
-    uint2 hv;
-    hv.x = pack2(0.5f * (u0 * sigmoid_fast(u0)), 0.5f * (u1 * sigmoid_fast(u1)));
-    hv.y = pack2(0.5f * (u2 * sigmoid_fast(u2)), 0.5f * (u3 * sigmoid_fast(u3)));
-    *reinterpret_cast<uint2*>(hh + static_cast<int64_t>(m) * r + n) = hv;
-  } else {
-    const float vals[4] = {acc.x, acc.y, acc.z, acc.w};
+  // columns n0 + cw + 2j: four warps read a column's 128 rows (512 contiguous bytes)
 #pragma unroll
-    for (int e = 0; e < 4; ++e)
-      if (n + e - r < HC) inj_next[static_cast<int64_t>(m) * HC + (n + e - r)] = vals[e];
+  for (int j = 0; j < RED_COLS / 2; ++j) {
+    float acc = 0.f;
+#pragma unroll
+    for (int ss = 0; ss < HC; ++ss) acc = fmaf(rs[ss], pv[j][ss], acc);
+    s_acc[cw + 2 * j][rr] = acc;
+  }
+  __syncthreads();
+  // rows out: 16 consecutive columns of a row per 16 lanes
+  const float inv_hc = 1.0f / static_cast<float>(HC);
+  const int cn = tid & (RED_COLS - 1), n = n0 + cn;
+#pragma unroll
+  for (int j = 0; j < BM * RED_COLS / RED_THREADS; ++j) {
+    const int rw = (tid >> 4) + (RED_THREADS / RED_COLS) * j;
+    const int m = tile * BM + rw;
+    if (m >= M || n >= np) continue;
+    const float v = s_acc[cn][rw];
+    if (n < r) {
+      lora[static_cast<int64_t>(m) * r + n] = v;
+      const float u = v * inv_hc;
+      hh[static_cast<int64_t>(m) * r + n] = f32_to_bf16(0.5f * (u * sigmoid_fast(u)));
+    } else if (n - r < HC) {
+      inj_next[static_cast<int64_t>(m) * HC + (n - r)] = v;
+    }
   }
 }
 
@@ -788,9 +809,11 @@ int k1_np(int r, int HC) { return (r + HC + 3) / 4 * 4; }
 size_t prefill_ws_bytes(int64_t max_M, int HC, int HS, int r) {
   // the largest partial buffer over M <= max_M: split-K only for small M,
   // where HC * S * M stays below a few hundred tiles of rows
-  size_t part = static_cast<size_t>(HC) * max_M * k1_np(r, HC);
+  // rows padded to whole 128-token tiles
+  const size_t Mp = static_cast<size_t>((max_M + BM - 1) / BM) * BM;
+  size_t part = static_cast<size_t>(HC) * Mp * k1_np(r, HC);
   part = std::max(part, static_cast<size_t>(2 * MAX_GRID) * BM * k1_np(r, HC));
-  const size_t sumsq = std::max(static_cast<size_t>(HC) * max_M, static_cast<size_t>(2 * MAX_GRID) * BM);
+  const size_t sumsq = std::max(static_cast<size_t>(HC) * Mp, static_cast<size_t>(2 * MAX_GRID) * BM);
   const size_t h = static_cast<size_t>(max_M) * r * 2;
   const size_t w1 = static_cast<size_t>(HC) * HS;
   return part * 4 + 256 + sumsq * 4 + 256 + h + 256 + w1 * 4 + 256;
@@ -805,15 +828,16 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   const int nkb = c.HS / BK;
   const int S = k1_chunks(n_mt, c.HC, nkb, dev.sms);
   const int np = k1_np(c.r, c.HC);
-  const size_t part_floats = static_cast<size_t>(c.HC) * S * M * np;
-  if (part_floats > std::max(static_cast<size_t>(c.HC) * M * np,
+  const size_t Mp = static_cast<size_t>(n_mt) * BM;
+  const size_t part_floats = static_cast<size_t>(c.HC) * S * Mp * np;
+  if (part_floats > std::max(static_cast<size_t>(c.HC) * Mp * np,
                              static_cast<size_t>(2 * MAX_GRID) * BM * np))
     return cudaErrorNotSupported;
   // workspace carve-up (sized by prefill_ws_bytes for max_M)
   float* part = ws.k1_part;
   float* sumsq = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(part) +
                                           (part_floats * 4 + 255) / 256 * 256);
-  const size_t sumsq_floats = static_cast<size_t>(c.HC) * S * M;
+  const size_t sumsq_floats = static_cast<size_t>(c.HC) * S * Mp;
   bf16_t* h = reinterpret_cast<bf16_t*>(reinterpret_cast<unsigned char*>(sumsq) +
                                         (sumsq_floats * 4 + 255) / 256 * 256);
   float* w1 = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(h) +
@@ -907,8 +931,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   }
   // ---------------- reduce
   {
-    const int64_t items = static_cast<int64_t>(M) * (np / 4);
-    const unsigned grid = static_cast<unsigned>((items + RED_THREADS - 1) / RED_THREADS);
+    const dim3 grid((np + RED_COLS - 1) / RED_COLS, n_mt);
 #define HCGR_RED(HCV)                                                                        \
   case HCV:                                                                                  \
     k1_reduce_kernel<HCV><<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,     \
