@@ -390,9 +390,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // the halving is exact and makes K2's accumulator hold G / 2, the argument of
 // tanh in sigmoid(G) = (1 + tanh(G / 2)) / 2.  The grid also writes
 // w1 = 1 + Wnorm in fp32 for K2's epilogue.  A block takes a 128-row tile
-// x 16 columns: it reads the column-major partials 512 contiguous bytes per
-// column and stream, and transposes through shared memory to write the
-// row-major outputs in 64-byte row runs.
+// x 16 columns: it reads the column-major partials in float4s, 512
+// contiguous bytes per warp, column and stream, and transposes through shared
+// memory to write the row-major outputs in 64-byte row runs.
 constexpr int RED_THREADS = 256;
 constexpr int RED_COLS = 16;          // columns per block (a block covers a whole 128-row tile)
 
@@ -410,64 +410,73 @@ __global__ void __launch_bounds__(RED_THREADS)
   for (int k = bid * RED_THREADS + tid; k < K; k += gridDim.x * gridDim.y * RED_THREADS)
     w1[k] = 1.0f + bf16_to_f32(Wnorm[k]);
   const int tile = blockIdx.y, n0 = blockIdx.x * RED_COLS;
-  const int rr = tid & (BM - 1), cw = tid >> 7;        // row within the tile; column phase 0/1
+  // thread = (4 consecutive rows, 2 columns): rows 4 (tid % 32) .., columns
+  // n0 + tid / 32 and n0 + tid / 32 + 8; a warp reads 512 contiguous bytes
+  // per column and stream
+  const int r4 = (tid & 31) * 4, cw = tid >> 5;
+  constexpr int NCOL = RED_COLS / 8;
   const int ns = HC * S;
   const int64_t tb = static_cast<int64_t>(tile) * ns;
-  // the row's partial sums of squares and the columns' partial products:
+  float4 q[HC];
+  float4 pv[NCOL][HC];
   // with one K chunk per stream (the usual case) every load issues before
-  // any is used
-  float q[HC];
-  float pv[RED_COLS / 2][HC];
-  if (S == 1) {
+  // any is used; otherwise chunk by chunk
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss) q[ss] = sumsq[(tb + ss) * BM + rr];
+  for (int ss = 0; ss < HC; ++ss) q[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < RED_COLS / 2; ++j) {
-      const int n = min(n0 + cw + 2 * j, np - 1);
+  for (int j = 0; j < NCOL; ++j)
 #pragma unroll
-      for (int ss = 0; ss < HC; ++ss) pv[j][ss] = part[((tb + ss) * np + n) * BM + rr];
+    for (int ss = 0; ss < HC; ++ss) pv[j][ss] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int c = 0; c < S; ++c) {
+    float4 qc[HC], vc[NCOL][HC];
+#pragma unroll
+    for (int ss = 0; ss < HC; ++ss)
+      qc[ss] = *reinterpret_cast<const float4*>(sumsq + (tb + ss * S + c) * BM + r4);
+#pragma unroll
+    for (int j = 0; j < NCOL; ++j) {
+      const int n = min(n0 + cw + 8 * j, np - 1);
+#pragma unroll
+      for (int ss = 0; ss < HC; ++ss)
+        vc[j][ss] = *reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4);
     }
-  } else {
-    // K chunk by K chunk, each chunk's loads all in flight together
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss) q[ss] = 0.f;
+    for (int ss = 0; ss < HC; ++ss) {
+      q[ss].x += qc[ss].x; q[ss].y += qc[ss].y; q[ss].z += qc[ss].z; q[ss].w += qc[ss].w;
+    }
 #pragma unroll
-    for (int j = 0; j < RED_COLS / 2; ++j)
+    for (int j = 0; j < NCOL; ++j)
 #pragma unroll
-      for (int ss = 0; ss < HC; ++ss) pv[j][ss] = 0.f;
-    for (int c = 0; c < S; ++c) {
-      float qc[HC], vc[RED_COLS / 2][HC];
-#pragma unroll
-      for (int ss = 0; ss < HC; ++ss) qc[ss] = sumsq[(tb + ss * S + c) * BM + rr];
-#pragma unroll
-      for (int j = 0; j < RED_COLS / 2; ++j) {
-        const int n = min(n0 + cw + 2 * j, np - 1);
-#pragma unroll
-        for (int ss = 0; ss < HC; ++ss) vc[j][ss] = part[((tb + ss * S + c) * np + n) * BM + rr];
+      for (int ss = 0; ss < HC; ++ss) {
+        pv[j][ss].x += vc[j][ss].x; pv[j][ss].y += vc[j][ss].y;
+        pv[j][ss].z += vc[j][ss].z; pv[j][ss].w += vc[j][ss].w;
       }
+  }
+  float4 rs[HC];
 #pragma unroll
-      for (int ss = 0; ss < HC; ++ss) q[ss] += qc[ss];
+  for (int ss = 0; ss < HC; ++ss)
+    rs[ss] = make_float4(rsqrt_nr(fmaf(q[ss].x, inv_hs, eps)), rsqrt_nr(fmaf(q[ss].y, inv_hs, eps)),
+                         rsqrt_nr(fmaf(q[ss].z, inv_hs, eps)), rsqrt_nr(fmaf(q[ss].w, inv_hs, eps)));
+  if (blockIdx.x == 0 && cw == 0) {
 #pragma unroll
-      for (int j = 0; j < RED_COLS / 2; ++j)
+    for (int e = 0; e < 4; ++e) {
+      const int m = tile * BM + r4 + e;
+      if (m < M) {
 #pragma unroll
-        for (int ss = 0; ss < HC; ++ss) pv[j][ss] += vc[j][ss];
+        for (int ss = 0; ss < HC; ++ss)
+          rrms[static_cast<int64_t>(m) * HC + ss] = e == 0 ? rs[ss].x : e == 1 ? rs[ss].y : e == 2 ? rs[ss].z : rs[ss].w;
+      }
     }
   }
-  float rs[HC];
 #pragma unroll
-  for (int ss = 0; ss < HC; ++ss) rs[ss] = rsqrt_nr(fmaf(q[ss], inv_hs, eps));
-  const int m_row = tile * BM + rr;
-  if (blockIdx.x == 0 && cw == 0 && m_row < M) {
+  for (int j = 0; j < NCOL; ++j) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss) rrms[static_cast<int64_t>(m_row) * HC + ss] = rs[ss];
-  }
-  // columns n0 + cw + 2j: four warps read a column's 128 rows (512 contiguous bytes)
-#pragma unroll
-  for (int j = 0; j < RED_COLS / 2; ++j) {
-    float acc = 0.f;
-#pragma unroll
-    for (int ss = 0; ss < HC; ++ss) acc = fmaf(rs[ss], pv[j][ss], acc);
-    s_acc[cw + 2 * j][rr] = acc;
+    for (int ss = 0; ss < HC; ++ss) {
+      acc.x = fmaf(rs[ss].x, pv[j][ss].x, acc.x); acc.y = fmaf(rs[ss].y, pv[j][ss].y, acc.y);
+      acc.z = fmaf(rs[ss].z, pv[j][ss].z, acc.z); acc.w = fmaf(rs[ss].w, pv[j][ss].w, acc.w);
+    }
+    float* dstc = &s_acc[cw + 8 * j][r4];
+    dstc[0] = acc.x; dstc[1] = acc.y; dstc[2] = acc.z; dstc[3] = acc.w;
   }
   __syncthreads();
   // rows out: 16 consecutive columns of a row per 16 lanes
