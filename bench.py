@@ -45,8 +45,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # were taken on: if those changed since, roofline.traffic is null.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "6232d6677320b5828a4468685e40a251e5d2e47e615e90ae06a6277eddc517b7",
-    "bytes": {2: 13336832, 4: 13389312, 8: 13494784, 16: 13698304, 32: 14152448},
+    "sources_sha256": "40b65a25d5c1b1ed7b367fb67aef16ef0f3139ec69e9b8d2000c11a4a3baba47",
+    "bytes": {2: 13336832, 4: 13389568, 8: 13494784, 16: 13698816, 32: 14124800},
 }
 
 
@@ -484,6 +484,87 @@ def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
     return res
 
 
+WIDE_MS = (1, 8, 64, 1024, 8192)
+
+
+def wide_sweep(Ms=WIDE_MS, reps: int = 5):
+    """Per-M latency of the wide shape (HC=8, HS=4096, r=512; heavy-tailed R,
+    y x10): decode path for M <= 32, prefill above, chosen by the library's
+    dispatcher.  Graph replay; weight+input sets rotate over more than twice
+    the L2 where one set fits in it."""
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import HcGatedResidual, inputs
+
+    sh = inputs.WIDE
+    K = sh.HC * sh.HS
+    w_bytes = 2 * (sh.r + sh.HC) * K + 2 * K * sh.r + 2 * K
+    a_bytes = 2 * K + 2 * sh.HS + 4 * sh.HC + 2 * K + 4 * sh.HC + 4 * sh.HC + 4 * sh.r + 2 * sh.HS
+    dev = torch.cuda.current_device()
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = {k: bf(v) for k, v in inputs.weights(sh).items()}
+    base_rows = 1024
+    a = inputs.activations(base_rows, sh)
+    R0, y0, inj0 = bf(a["R"]), bf(a["y"]), torch.from_numpy(a["inj"]).cuda()
+    hbm, _, _ = peaks()
+    res = {}
+    stream = torch.cuda.Stream()
+    for M in Ms:
+        per_set = w_bytes + M * a_bytes
+        nsets = int(min(4, max(1, np.ceil(2.0 * l2 / per_set))))
+        reps_rows = (M + base_rows - 1) // base_rows
+        R = R0.repeat(reps_rows, 1, 1)[:M].contiguous()
+        y = y0.repeat(reps_rows, 1)[:M].contiguous()
+        inj = inj0.repeat(reps_rows, 1)[:M].contiguous()
+        op = HcGatedResidual(max_M=M, HC=sh.HC, HS=sh.HS, r=sh.r)
+        sets = [(R, y, inj, w) if j == 0 else
+                (R.clone(), y.clone(), inj.clone(), {k: v.clone() for k, v in w.items()})
+                for j in range(nsets)]
+        outs = [{"R2": torch.empty_like(R), "rrms": torch.empty((M, sh.HC), device="cuda"),
+                 "inj_next": torch.empty((M, sh.HC), device="cuda"),
+                 "x": torch.empty((M, sh.HS), dtype=torch.bfloat16, device="cuda"),
+                 "lora": torch.empty((M, sh.r), device="cuda")} for _ in range(nsets)]
+
+        def call(j):
+            Rj, yj, ij, wj = sets[j]
+            op.forward(Rj, yj, ij, wj["Wnorm"], wj["Wu"], Wd=wj["Wd"], Wi=wj["Wi"], out=outs[j])
+
+        for j in range(nsets):
+            call(j)
+        op.check()
+        g = torch.cuda.CUDAGraph()
+        calls = max(nsets, 2)
+        with torch.cuda.graph(g, stream=stream):
+            for j in range(calls):
+                call(j % nsets)
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for _ in range(2):
+                g.replay()
+            samples = []
+            for _ in range(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                e1.synchronize()
+                samples.append(e0.elapsed_time(e1) * 1e3 / calls)
+        us = statistics.median(samples)
+        roof_us = per_set / hbm / 1e3
+        res[str(M)] = {"us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us,
+                       "roofline_frac": roof_us / us, "path": "decode" if M <= 32 else "prefill",
+                       "l2": f"{nsets} rotating sets" if nsets > 1 else "inputs > L2"}
+        op.close()
+        del sets, outs, R, y, inj
+        torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["auto", "decode", "prefill"], default=None,
@@ -528,6 +609,7 @@ def main():
     line = run_ours(args, rank, world)
     if rank == 0 and not args.no_prefill_sweep:
         line["prefill_sweep_us"] = prefill_sweep()
+        line["wide_sweep_us"] = wide_sweep()
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline()
         print(json.dumps(line))
