@@ -166,11 +166,23 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     // all weight tiles resident when they fit, else rings
     const int nbox = g.ntd * g.nkc;
     bool fits = false;
-    for (int ring = 0; ring < 2 && !fits; ++ring) {
-      g.nsl_w = ring ? std::min(nbox, 4) : nbox;
-      g.nsl_u = ring ? std::min(g.nchunk_u, 2) : g.nchunk_u;
-      if (g.nsl_w > MAX_SLOTS || g.nsl_u > MAX_SLOTS) continue;
-      fits = layout(c, g);
+    // With rings the weight streams are bound by the bytes in flight per SM,
+    // so the rings take what the budget allows: the up ring first (its
+    // refills sit on the critical path after the exchanges; a ring of fewer
+    // slots than chunks alternates its slots between two issuers, so it has
+    // an even count), then the down ring (at least four slots if possible).
+    g.nsl_w = nbox;
+    g.nsl_u = g.nchunk_u;
+    fits = g.nsl_w <= MAX_SLOTS && g.nsl_u <= MAX_SLOTS && layout(c, g);
+    for (int wmin = std::min(nbox, 4); wmin >= 2 && !fits; wmin -= 2) {
+      for (int u = std::min(g.nchunk_u, MAX_SLOTS); u >= 2 && !fits; --u) {
+        if (u < g.nchunk_u && (u & 1)) continue;
+        g.nsl_u = u;
+        for (int w = std::min(nbox, MAX_SLOTS); w >= wmin && !fits; --w) {
+          g.nsl_w = w;
+          fits = layout(c, g);
+        }
+      }
     }
     // down: one accumulator per row tile (one issuing thread each); up: one
     // accumulator copy per issuing thread -- a thread per Wu chunk when every
