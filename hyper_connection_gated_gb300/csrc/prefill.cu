@@ -807,7 +807,9 @@ static_assert(k2_ncu(4) * 4 == 256 && k2_ncu(8) * 8 == 256 && k2_ncu(1) * 8 <= 5
 // when there are few token tiles, at least two K blocks per chunk.
 int k1_chunks(int n_mt, int HC, int nkb, int sms) {
   if (HC * n_mt >= sms) return 1;
-  const int want = (sms + HC * n_mt / 2) / (HC * n_mt);
+  // as many chunks as still fit one wave (a second, nearly empty wave costs
+  // a whole CTA time)
+  const int want = sms / (HC * n_mt);
   return std::max(1, std::min(want, nkb / 2));
 }
 
