@@ -31,6 +31,7 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 SWEEP = (2, 4, 8, 16, 32)
+LAT_MS = (1,) + SWEEP      # per-M latency table: the single-token call as well
 HC, HS, R_LOW = 4, 2560, 320
 K_DIM = HC * HS
 METRIC = "HC gated-residual µs/call & tokens/s vs M (HC4,HS2560,r320 bf16); % roofline"
@@ -45,8 +46,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # were taken on: if those changed since, roofline.traffic is null.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "40b65a25d5c1b1ed7b367fb67aef16ef0f3139ec69e9b8d2000c11a4a3baba47",
-    "bytes": {2: 13336832, 4: 13389568, 8: 13494784, 16: 13698816, 32: 14124800},
+    "sources_sha256": "4525dd2f469fb05c8a7e079c55dcefed09c9deaaa6e98a46896ab1210bd1e902",
+    "bytes": {2: 13337344, 4: 13398528, 8: 13494528, 16: 13697792, 32: 14125056},
 }
 
 
@@ -60,6 +61,14 @@ def decode_traffic_per_launch():
     if h.hexdigest() != DECODE_TRAFFIC["sources_sha256"]:
         return None
     return sum(DECODE_TRAFFIC["bytes"][M] for M in SWEEP) / len(SWEEP)
+
+
+def roofline_us(nbytes: float, flops: float, hbm_gbs: float, tflops: float):
+    """Roofline time of one call (µs) and its bound: the larger of the HBM
+    time for the algorithmic bytes and the tensor time for the flops."""
+    t_hbm = nbytes / hbm_gbs / 1e3
+    t_tc = flops / tflops / 1e6
+    return (t_hbm, "hbm") if t_hbm >= t_tc else (t_tc, "tensor")
 
 
 def peaks():
@@ -199,7 +208,7 @@ def run_ours(args, rank, world):
     sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
     op = HcGatedResidual(max_M=max(SWEEP))
     outs = {M: [op.forward(s["R"][:M], s["y"][:M], s["inj"][:M], s["Wnorm"], s["Wu"],
-                           Wd=s["Wd"], Wi=s["Wi"]) for s in sets] for M in SWEEP}
+                           Wd=s["Wd"], Wi=s["Wi"]) for s in sets] for M in LAT_MS}
     op.check()
 
     def prepared(M, j, pdl):
@@ -216,7 +225,7 @@ def run_ours(args, rank, world):
 
     # pdl: each call may start its weight copies while the previous call in
     # the stream finishes (the library's programmatic-dependent-launch mode)
-    args_tab = {(M, j, pdl): prepared(M, j, pdl) for M in SWEEP for j in range(nsets)
+    args_tab = {(M, j, pdl): prepared(M, j, pdl) for M in LAT_MS for j in range(nsets)
                 for pdl in (True, False)}
     stream = torch.cuda.Stream()
 
@@ -230,13 +239,13 @@ def run_ours(args, rank, world):
 
     step_graphs = [capture([args_tab[(M, j, True)] for M in SWEEP]) for j in range(nsets)]
     per_m_graphs = {(M, pdl): capture([args_tab[(M, j, pdl)] for j in range(nsets)])
-                    for M in SWEEP for pdl in (True, False)}
+                    for M in LAT_MS for pdl in (True, False)}
     torch.cuda.synchronize()
 
     # per-M latency (graph replay, nsets calls per replay), both launch modes
     per_m, per_m_plain = {}, {}
     with torch.cuda.stream(stream):
-        for M in SWEEP:
+        for M in LAT_MS:
             for pdl, dst in ((True, per_m), (False, per_m_plain)):
                 gr = per_m_graphs[(M, pdl)]
                 for _ in range(3):
@@ -323,9 +332,18 @@ def run_ours(args, rank, world):
     ev_comp = [torch.cuda.Event() for _ in range(2)]
     ev_out = [torch.cuda.Event() for _ in range(2)]
 
+    # one prepared call per buffer set, weight set and M: the loop below makes
+    # one C-ABI call per forward, with no per-call Python validation
+    e2e_args = {(bsel, j, M): op.prepare(dev_in[bsel][M]["R"], dev_in[bsel][M]["y"],
+                                         dev_in[bsel][M]["inj"], sets[j]["Wnorm"], sets[j]["Wu"],
+                                         Wd=sets[j]["Wd"], Wi=sets[j]["Wi"], out=dev_out[bsel][M],
+                                         pdl=True)[0]
+                for bsel in range(2) for j in range(nsets) for M in SWEEP}
+    sh = stream.cuda_stream
+
     def e2e_run(nsteps):
         for i in range(nsteps):
-            bsel, s = i % 2, sets[i % nsets]
+            bsel, j = i % 2, i % nsets
             with torch.cuda.stream(h2d_s):
                 if i >= 2:
                     h2d_s.wait_event(ev_comp[bsel])      # step i-2 has read this buffer
@@ -334,11 +352,9 @@ def run_ours(args, rank, world):
             stream.wait_event(ev_in[bsel])
             if i >= 2:
                 stream.wait_event(ev_out[bsel])          # step i-2's outputs are home
-            with torch.cuda.stream(stream):
-                for M in SWEEP:
-                    op.forward(dev_in[bsel][M]["R"], dev_in[bsel][M]["y"], dev_in[bsel][M]["inj"],
-                               s["Wnorm"], s["Wu"], Wd=s["Wd"], Wi=s["Wi"], out=dev_out[bsel][M])
-                ev_comp[bsel].record(stream)
+            for M in SWEEP:
+                op.launch(e2e_args[(bsel, j, M)], sh)
+            ev_comp[bsel].record(stream)
             with torch.cuda.stream(d2h_s):
                 d2h_s.wait_event(ev_comp[bsel])
                 host_out_buf[bsel].copy_(dev_out_buf[bsel], non_blocking=True)
@@ -370,7 +386,8 @@ def run_ours(args, rank, world):
                    "timing": "CUDA graph replay, CUDA events on the launching stream",
                    "launch": "programmatic dependent launch (hc_gr_args.pdl = 1): a call's "
                              "weight copies overlap the previous call's tail",
-                   "e2e": "public forward(); per step one pinned host->device copy of all inputs and "
+                   "e2e": "public prepare() once per buffer set, then launch() (one C-ABI call) per "
+                          "forward; per step one pinned host->device copy of all inputs and "
                           "one device->host copy of all outputs, on their own streams and double-"
                           "buffered (step i+1's copy-in and step i's copy-back overlap step i's "
                           "compute); the host waits for every step's outputs, one step behind",
@@ -384,10 +401,10 @@ def run_ours(args, rank, world):
                      "algorithmic_bytes_per_launch": alg_bytes / len(SWEEP),
                      "kernel": "decode_kernel (per launch, mean over the sweep: weights + activations)",
                      "peak_source": peak_src},
-        "per_M_us": {str(M): per_m[M] for M in SWEEP},
-        "per_M_us_plain_launch": {str(M): per_m_plain[M] for M in SWEEP},
+        "per_M_us": {str(M): per_m[M] for M in LAT_MS},
+        "per_M_us_plain_launch": {str(M): per_m_plain[M] for M in LAT_MS},
         "per_M_roofline_frac": {str(M): (WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN) / hbm / 1e3
-                                / per_m[M] for M in SWEEP},
+                                / per_m[M] for M in LAT_MS},
     }
     return line
 
@@ -448,7 +465,7 @@ def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
     Wdi[:R_LOW] = w["Wd"]
     Wdi[R_LOW:R_LOW + HC] = w["Wi"]
     Wdi_f = (Wdi.float() * (1.0 + w["Wnorm"].float())[None, :]).to(torch.bfloat16)
-    hbm, _, _ = peaks()
+    hbm, tflops, _ = peaks()
     res = {}
     stream = torch.cuda.Stream()
     for M in Ms:
@@ -498,9 +515,9 @@ def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
                     e1.synchronize()
                     samples.append(e0.elapsed_time(e1) * 1e3 / calls)
             us = statistics.median(samples)
-            roof_us = per_set / hbm / 1e3
+            roof_us, bound = roofline_us(per_set, M * FLOPS_PER_TOKEN, hbm, tflops)
             res.setdefault(str(M), {})[name] = {
-                "us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us,
+                "us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us, "bound": bound,
                 "roofline_frac": roof_us / us, "spread": (max(samples) - min(samples)) / us,
                 "l2": f"{nsets} rotating sets" if nsets > 1 else "inputs > L2"}
             del sets, outs
@@ -537,7 +554,8 @@ def wide_sweep(Ms=WIDE_MS, reps: int = 5):
     base_rows = 1024
     a = inputs.activations(base_rows, sh)
     R0, y0, inj0 = bf(a["R"]), bf(a["y"]), torch.from_numpy(a["inj"]).cuda()
-    hbm, _, _ = peaks()
+    flops_tok = 2 * K * (sh.r + sh.HC + sh.r)
+    hbm, tflops, _ = peaks()
     res = {}
     stream = torch.cuda.Stream()
     for M in Ms:
@@ -581,8 +599,8 @@ def wide_sweep(Ms=WIDE_MS, reps: int = 5):
                 e1.synchronize()
                 samples.append(e0.elapsed_time(e1) * 1e3 / calls)
         us = statistics.median(samples)
-        roof_us = per_set / hbm / 1e3
-        res[str(M)] = {"us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us,
+        roof_us, bound = roofline_us(per_set, M * flops_tok, hbm, tflops)
+        res[str(M)] = {"us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us, "bound": bound,
                        "roofline_frac": roof_us / us, "path": "decode" if M <= 32 else "prefill",
                        "l2": f"{nsets} rotating sets" if nsets > 1 else "inputs > L2"}
         op.close()

@@ -8,6 +8,10 @@ outputs when the caller does not pass them, and forwards raw pointers.
     op = HcGatedResidual(max_M=4096)           # HC=4, HS=2560, r=320
     out = op.forward(R, y, inj, Wnorm, Wu, Wd=Wd, Wi=Wi)
     out["x"], out["R2"], out["rrms"], out["inj_next"], out["lora"]
+
+    # fixed buffers, many calls: validate once, then one C call per step
+    args, out = op.prepare(R, y, inj, Wnorm, Wu, Wd=Wd, Wi=Wi, pdl=True)
+    op.launch(args, torch.cuda.current_stream().cuda_stream)
 """
 from __future__ import annotations
 
@@ -42,15 +46,19 @@ class HcGatedResidual:
         self.max_M, self.HC, self.HS, self.r = max_M, HC, HS, r
 
     # ------------------------------------------------------------------ calls
-    def forward(self, R, y, inj, Wnorm, Wu, Wd=None, Wi=None, Wdi=None, fold_w=False,
+    def prepare(self, R, y, inj, Wnorm, Wu, Wd=None, Wi=None, Wdi=None, fold_w=False,
                 eps: float = 1e-6, out: dict | None = None, want_lora: bool = True,
-                stream=None, force_path: int = PATH_AUTO, debug_fault: int = 0,
-                pdl: bool = False, check: bool = False) -> dict:
-        """Runs the whole forward pass; returns the output tensors.
+                force_path: int = PATH_AUTO, debug_fault: int = 0,
+                pdl: bool = False) -> tuple["_native.Args", dict]:
+        """Validates one call's tensors once and returns (args, out).
 
         R [M, HC, HS] bf16, y [M, HS] bf16, inj [M, HC] fp32 (rows may be
         strided), Wnorm [K] bf16, Wu [K, r] bf16, and either Wd [r, K] + Wi
         [HC, K] or a merged Wdi [n_pad, K] (fold_w: (1 + Wnorm) folded in).
+        out holds R2, rrms, inj_next, x (and lora); they are allocated here
+        when not given.  `launch(args)` then runs the call on these buffers
+        as often as needed (a serving loop with fixed buffers), with none of
+        the per-call checks of `forward`; the caller keeps every tensor alive.
         pdl: let the decode kernel start its weight copies before the
         previous kernel on the stream has finished (that kernel must not
         write the weights).
@@ -94,10 +102,28 @@ class HcGatedResidual:
                                          out["inj_next"].data_ptr(), out["x"].data_ptr())
         a.lora = out["lora"].data_ptr() if out.get("lora") is not None else None
         a.force_path, a.debug_fault, a.pdl = force_path, debug_fault, 1 if pdl else 0
-        s = stream if stream is not None else torch.cuda.current_stream(dev)
-        st = self._lib.hc_gr_forward_ex(self._h, ctypes.byref(a), ctypes.c_void_p(s.cuda_stream))
+        return a, out
+
+    def launch(self, args: "_native.Args", stream_handle: int) -> None:
+        """Runs a prepared call on a raw stream handle (`stream.cuda_stream`);
+        raises on a rejected call."""
+        st = self._lib.hc_gr_forward_ex(self._h, ctypes.byref(args), ctypes.c_void_p(stream_handle))
         if st != OK:
             raise HcGrError(st, self._error_text(st))
+
+    def forward(self, R, y, inj, Wnorm, Wu, Wd=None, Wi=None, Wdi=None, fold_w=False,
+                eps: float = 1e-6, out: dict | None = None, want_lora: bool = True,
+                stream=None, force_path: int = PATH_AUTO, debug_fault: int = 0,
+                pdl: bool = False, check: bool = False) -> dict:
+        """Runs the whole forward pass; returns the output tensors (arguments
+        as in `prepare`, on `stream` or the current stream)."""
+        import torch
+
+        a, out = self.prepare(R, y, inj, Wnorm, Wu, Wd=Wd, Wi=Wi, Wdi=Wdi, fold_w=fold_w, eps=eps,
+                              out=out, want_lora=want_lora, force_path=force_path,
+                              debug_fault=debug_fault, pdl=pdl)
+        s = stream if stream is not None else torch.cuda.current_stream(R.device)
+        self.launch(a, s.cuda_stream)
         if check:
             self.check(s)
         return out

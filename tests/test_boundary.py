@@ -147,3 +147,31 @@ def test_lora_optional(env):
                      want_lora=False, check=True)
     assert "lora" not in out
     tl.assert_parity(out, tl.oracle_ref(case))
+
+
+def test_prepared_call_repeats_bit_identically(env):
+    # prepare() validates once; launch() reruns the same call on the same
+    # buffers, and every run gives the result forward() gives
+    torch, case, d, op = env
+    ref = op.forward(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"],
+                     check=True)
+    args, out = op.prepare(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"],
+                           pdl=True)
+    h = torch.cuda.current_stream().cuda_stream
+    for _ in range(3):
+        for t in out.values():
+            t.fill_(float("nan"))
+        op.launch(args, h)
+        op.check()
+        for k in ref:
+            assert torch.equal(out[k].view(torch.uint8), ref[k].view(torch.uint8)), k
+    tl.assert_parity(out, tl.oracle_ref(case))
+
+
+def test_prepared_call_rejects_like_forward(env):
+    torch, case, d, op = env
+    args, _ = op.prepare(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"])
+    args.eps = 0.0
+    with pytest.raises(HcGrError) as ei:
+        op.launch(args, torch.cuda.current_stream().cuda_stream)
+    assert ei.value.status == ERR_INVALID_ARG
