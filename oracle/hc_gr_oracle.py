@@ -144,7 +144,8 @@ def merge_weight(Wd, Wi, Wnorm, n_pad, fold):
 
 def forward(R, y, inj, Wnorm, Wu, eps, Wd=None, Wi=None, Wdi=None,
             fold_w=False):
-    """The whole per-token path, in the page's order.
+    """The whole per-token path, in the page's order: (COMBINE), then the
+    mix of the combined residual.
 
     Either (Wd, Wi) or a merged Wdi is given.  With fold_w the given
     projection weights already carry (1 + Wnorm) in their columns.
@@ -152,11 +153,23 @@ def forward(R, y, inj, Wnorm, Wu, eps, Wd=None, Wi=None, Wdi=None,
     """
     R = np.asarray(R, np.float64)
     y = np.asarray(y, np.float64)
-    M, HC, HS = R.shape
+    R2, _ = combine(R, y, inj)
+    out = mix(R2, Wnorm, Wu, eps, Wd=Wd, Wi=Wi, Wdi=Wdi, fold_w=fold_w)
+    out["R2"] = R2
+    return out
+
+
+def mix(R2, Wnorm, Wu, eps, Wd=None, Wi=None, Wdi=None, fold_w=False):
+    """Every step after (COMBINE) -- (N), (G1), (INJ), (G2), (MIX) -- on an
+    already-combined residual R2 [M, HC, HS] (the page's mix entry point).
+
+    Weights as in forward.  Returns rrms, xn, lora, inj_next, h, G, x.
+    """
+    R2 = np.asarray(R2, np.float64)
+    M, HC, HS = R2.shape
     r = np.asarray(Wu).shape[1]
     if Wdi is not None:
         Wd, Wi = split_merged(Wdi, r, HC)
-    R2, _ = combine(R, y, inj)
     rrms = grouped_rrms(R2, eps)
     xn = normalise(R2, rrms, Wnorm)
     if fold_w:
@@ -168,5 +181,5 @@ def forward(R, y, inj, Wnorm, Wu, eps, Wd=None, Wi=None, Wdi=None,
     h = silu_h(lora, HC)
     G = up_gate(h, Wu)
     x = gated_mean(G, xn, HC)
-    return {"R2": R2, "rrms": rrms, "xn": xn, "lora": lora,
+    return {"rrms": rrms, "xn": xn, "lora": lora,
             "inj_next": inj_next, "h": h, "G": G, "x": x}

@@ -272,6 +272,36 @@ def test_batch_invariance():
         np.testing.assert_allclose(one[k][0], full[k][3], rtol=1e-14, atol=1e-15)
 
 
+def test_mix_is_the_path_with_nothing_injected():
+    # The mix entry point runs (N) onwards on R as the combined residual.
+    # With y = 0, COMBINE leaves every bf16 R unchanged whatever inj is
+    # (R + 0 * iw = R), so the whole path must give the same outputs.
+    rng = np.random.default_rng(16)
+    c = _case(rng, 4, 4, 16, 8)
+    m = oracle.mix(c["R"], c["Wnorm"], c["Wu"], c["eps"], Wd=c["Wd"], Wi=c["Wi"])
+    f = oracle.forward(**dict(c, y=np.zeros_like(c["y"])))
+    np.testing.assert_array_equal(f["R2"], c["R"])
+    for k in ("rrms", "lora", "inj_next", "h", "G", "x"):
+        np.testing.assert_array_equal(m[k], f[k])
+    assert "R2" not in m
+
+
+def test_mix_constant_rows_closed_form():
+    # Mix alone on constant streams a_s with Wnorm = 0 and Wu = 0:
+    # x[c] = (1/2) mean_s a_s / sqrt(a_s^2 + eps), lora[n] = HS sum_s xn_s for
+    # all-ones Wd rows -- the closed form of (N), (G1), (G2) and (MIX).
+    HC, HS, r, eps = 4, 8, 4, 1e-6
+    a = np.array([1.5, -0.25, 2.0, -4.0])
+    R = np.broadcast_to(a[None, :, None], (2, HC, HS)).copy()
+    out = oracle.mix(R, np.zeros(HC * HS), np.zeros((HC * HS, r)), eps,
+                     Wd=np.ones((r, HC * HS)), Wi=np.ones((HC, HC * HS)))
+    xs = a / np.sqrt(a * a + eps)
+    np.testing.assert_allclose(out["rrms"], np.broadcast_to(1.0 / np.sqrt(a * a + eps), (2, HC)),
+                               rtol=1e-15)
+    np.testing.assert_allclose(out["x"], np.full((2, HS), 0.5 * xs.mean()), rtol=1e-14)
+    np.testing.assert_allclose(out["lora"], np.full((2, r), HS * xs.sum()), rtol=1e-14)
+
+
 def test_fold_equivalence_exact_weights():
     # Folding (1 + Wnorm) into the weight columns is the same product when the
     # fold is kept in float64; the mix still sees (1 + Wnorm).
