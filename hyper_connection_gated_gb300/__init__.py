@@ -55,8 +55,9 @@ class HcGatedResidual:
         R [M, HC, HS] bf16, y [M, HS] bf16, inj [M, HC] fp32 (rows may be
         strided), Wnorm [K] bf16, Wu [K, r] bf16, and either Wd [r, K] + Wi
         [HC, K] or a merged Wdi [n_pad, K] (fold_w: (1 + Wnorm) folded in).
-        out holds R2, rrms, inj_next, x (and lora); they are allocated here
-        when not given.  `launch(args)` then runs the call on these buffers
+        y = inj = None is the mix alone: R is the combined residual and no R2
+        is produced.  out holds R2, rrms, inj_next, x (and lora); they are
+        allocated here when not given.  `launch(args)` then runs the call on these buffers
         as often as needed (a serving loop with fixed buffers), with none of
         the per-call checks of `forward`; the caller keeps every tensor alive.
         pdl: let the decode kernel start its weight copies before the
@@ -68,38 +69,46 @@ class HcGatedResidual:
         M, HC, HS = R.shape
         r = Wu.shape[1]
         dev = R.device
+        mix_only = y is None and inj is None
         for name, t in (("R", R), ("y", y), ("Wnorm", Wnorm), ("Wu", Wu), ("Wd", Wd),
                         ("Wi", Wi), ("Wdi", Wdi)):
             if t is None:
                 continue
             if t.dtype != torch.bfloat16 or t.device != dev or not t.is_contiguous():
                 raise HcGrError(ERR_INVALID_ARG, f"{name} must be a contiguous bf16 tensor on {dev}")
-        if inj.dtype != torch.float32 or inj.device != dev or inj.stride(1) != 1:
-            raise HcGrError(ERR_INVALID_ARG, "inj must be fp32 on the same device, unit column stride")
-        if tuple(y.shape) != (M, HS) or tuple(inj.shape) != (M, HC) or Wnorm.numel() != HC * HS \
-                or tuple(Wu.shape) != (HC * HS, r):
+        if not mix_only:
+            if y is None or inj is None:
+                raise HcGrError(ERR_INVALID_ARG, "y and inj are both given or both None (mix only)")
+            if inj.dtype != torch.float32 or inj.device != dev or inj.stride(1) != 1:
+                raise HcGrError(ERR_INVALID_ARG, "inj must be fp32 on the same device, unit column stride")
+            if tuple(y.shape) != (M, HS) or tuple(inj.shape) != (M, HC):
+                raise HcGrError(ERR_INVALID_ARG, "shape mismatch")
+        if Wnorm.numel() != HC * HS or tuple(Wu.shape) != (HC * HS, r):
             raise HcGrError(ERR_INVALID_ARG, "shape mismatch")
         if out is None:
-            out = {
-                "R2": torch.empty_like(R),
+            out = {} if mix_only else {"R2": torch.empty_like(R)}
+            out.update({
                 "rrms": torch.empty((M, HC), dtype=torch.float32, device=dev),
                 "inj_next": torch.empty((M, HC), dtype=torch.float32, device=dev),
                 "x": torch.empty((M, HS), dtype=torch.bfloat16, device=dev),
-            }
+            })
             if want_lora:
                 out["lora"] = torch.empty((M, r), dtype=torch.float32, device=dev)
         a = _native.Args()
         a.M, a.HC, a.HS, a.r, a.eps = M, HC, HS, r, eps
-        a.R, a.y, a.inj = R.data_ptr(), y.data_ptr(), inj.data_ptr()
-        a.ld_inj = inj.stride(0) if M > 1 else HC
+        a.R = R.data_ptr()
+        if not mix_only:
+            a.y, a.inj = y.data_ptr(), inj.data_ptr()
+            a.ld_inj = inj.stride(0) if M > 1 else HC
         a.Wnorm, a.Wu = Wnorm.data_ptr(), Wu.data_ptr()
         if Wdi is not None:
             a.Wdi, a.n_pad = Wdi.data_ptr(), Wdi.shape[0]
         else:
             a.Wd, a.Wi = Wd.data_ptr(), Wi.data_ptr()
         a.fold_w = 1 if fold_w else 0
-        a.R2, a.rrms, a.inj_next, a.x = (out["R2"].data_ptr(), out["rrms"].data_ptr(),
-                                         out["inj_next"].data_ptr(), out["x"].data_ptr())
+        if not mix_only:
+            a.R2 = out["R2"].data_ptr()
+        a.rrms, a.inj_next, a.x = out["rrms"].data_ptr(), out["inj_next"].data_ptr(), out["x"].data_ptr()
         a.lora = out["lora"].data_ptr() if out.get("lora") is not None else None
         a.force_path, a.debug_fault, a.pdl = force_path, debug_fault, 1 if pdl else 0
         return a, out
@@ -126,6 +135,41 @@ class HcGatedResidual:
         self.launch(a, s.cuda_stream)
         if check:
             self.check(s)
+        return out
+
+    def mix(self, R, Wnorm, Wu, Wd=None, Wi=None, Wdi=None, fold_w=False, eps: float = 1e-6,
+            out: dict | None = None, want_lora: bool = True, stream=None,
+            force_path: int = PATH_AUTO, pdl: bool = False, check: bool = False) -> dict:
+        """Every step after COMBINE on R taken as the combined residual
+        (R2 = R): returns rrms, inj_next, x (and lora); no R2."""
+        return self.forward(R, None, None, Wnorm, Wu, Wd=Wd, Wi=Wi, Wdi=Wdi, fold_w=fold_w,
+                            eps=eps, out=out, want_lora=want_lora, stream=stream,
+                            force_path=force_path, pdl=pdl, check=check)
+
+    def combine(self, R, y, inj, out=None, stream=None):
+        """COMBINE alone: returns R2 = bf16(R + y * 2 sigmoid(inj / HC)).
+        inj may be a row-strided view (unit column stride)."""
+        import torch
+
+        M, HC, HS = R.shape
+        dev = R.device
+        for name, t in (("R", R), ("y", y)):
+            if t.dtype != torch.bfloat16 or t.device != dev or not t.is_contiguous():
+                raise HcGrError(ERR_INVALID_ARG, f"{name} must be a contiguous bf16 tensor on {dev}")
+        if inj.dtype != torch.float32 or inj.device != dev or inj.stride(1) != 1:
+            raise HcGrError(ERR_INVALID_ARG, "inj must be fp32 on the same device, unit column stride")
+        if tuple(y.shape) != (M, HS) or tuple(inj.shape) != (M, HC):
+            raise HcGrError(ERR_INVALID_ARG, "shape mismatch")
+        if out is None:
+            out = torch.empty_like(R)
+        elif out.dtype != torch.bfloat16 or out.shape != R.shape or not out.is_contiguous():
+            raise HcGrError(ERR_INVALID_ARG, "out must be a contiguous bf16 tensor shaped like R")
+        s = stream if stream is not None else torch.cuda.current_stream(dev)
+        st = self._lib.hc_gr_combine(self._h, M, HC, HS, R.data_ptr(), y.data_ptr(), inj.data_ptr(),
+                                     inj.stride(0) if M > 1 else HC, out.data_ptr(),
+                                     ctypes.c_void_p(s.cuda_stream))
+        if st != OK:
+            raise HcGrError(st, self._error_text(st))
         return out
 
     def forward_raw(self, args: "_native.Args", stream_handle: int) -> int:

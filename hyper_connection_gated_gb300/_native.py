@@ -16,7 +16,8 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ALIAS, ERR_CUDA, ERR_TIMEOUT = range(6
 PATH_AUTO, PATH_DECODE, PATH_PREFILL = range(3)
 
 EXPORTS = ("hc_gr_create", "hc_gr_forward", "hc_gr_forward_ex", "hc_gr_check",
-           "hc_gr_destroy", "hc_gr_strerror", "hc_gr_last_cuda_error", "hc_gr_forward_noalloc")
+           "hc_gr_destroy", "hc_gr_strerror", "hc_gr_last_cuda_error", "hc_gr_forward_noalloc",
+           "hc_gr_combine", "hc_gr_mix")
 
 _vp = ctypes.c_void_p
 _fp = ctypes.c_void_p   # float* passed as an address
@@ -69,6 +70,12 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_gr_forward_noalloc.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float] + [_vp] * 12 + [_vp]
     lib.hc_gr_forward_noalloc.restype = ctypes.c_int
+    lib.hc_gr_combine.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
+                                  ctypes.c_int64, _vp, _vp]
+    lib.hc_gr_combine.restype = ctypes.c_int
+    lib.hc_gr_mix.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_float] + [_vp] * 9 + [_vp]
+    lib.hc_gr_mix.restype = ctypes.c_int
     return lib
 
 

@@ -327,9 +327,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // channel pairs, and inj (iw is formed from it later) -- copied
   // asynchronously now, so that their latency hides behind COMBINE and the
   // down MMAs.
+  const bool has_y = c.y != nullptr;   // false: mix only, R2 = R
   {
     const int np = nc / 2;
-    const int n_iw = M * HC, n_r = M * HC * np, n_y = M * np, n_w = HC * np;
+    const int n_iw = has_y ? M * HC : 0, n_r = M * HC * np, n_y = has_y ? M * np : 0, n_w = HC * np;
 #pragma unroll 1
     for (int i = tid; i < n_iw + n_r + n_y + n_w; i += NT) {
       if (i < n_iw) {
@@ -361,15 +362,18 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     float ss = 0.f;
     if (m < M && ch < nkv) {
       const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
-      const float iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc0);
-      float rv[8], yv[8], wv[8], a[8];
+      float rv[8], yv[8] = {}, wv[8], a[8];
+      float iw = 0.f;
       unpack8(__ldg(reinterpret_cast<const uint4*>(c.R + kk)), rv);
-      unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
+      if (has_y) {
+        iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc0);
+        unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
+      }
       unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + k0 + un * 8)), wv);
       uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const float r2 = bf16_to_f32(f32_to_bf16(fmaf(yv[i], iw, rv[i])));
+        const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(yv[i], iw, rv[i]))) : rv[i];
         ss = fmaf(r2, r2, ss);
         rv[i] = r2;
         a[i] = c.fold ? r2 : r2 * (1.0f + wv[i]);
@@ -382,7 +386,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         ph[i] = pack2(h0, h1);
         pl[i] = pack2(a[2 * i] - h0, a[2 * i + 1] - h1);
       }
-      *reinterpret_cast<uint4*>(c.R2 + kk) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+      if (c.R2) *reinterpret_cast<uint4*>(c.R2 + kk) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
       hv = make_uint4(ph[0], ph[1], ph[2], ph[3]);
       lv = make_uint4(pl[0], pl[1], pl[2], pl[3]);
     }
@@ -443,7 +447,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // the final mix's inputs (copied since the prologue) have landed; iw from inj
   cp_async_wait_all();
 #pragma unroll 1
-  for (int i = tid; i < M * HC; i += NT) s_iw[i] = combine_weight(s_iw[i], inv_hc0);
+  for (int i = tid; i < M * HC; i += NT) s_iw[i] = has_y ? combine_weight(s_iw[i], inv_hc0) : 0.f;
   // and the sum of squares, and the non-product words of this CTA's
   // piece of every reduce-scatter block ([Qn partials][sum of squares][3 pad
   // words], partials past n_out zero)
@@ -729,8 +733,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll 1
         for (int ss = 0; ss < HC; ++ss) {
           const float rv = bf16_to_f32(s_x3r[(m * HC + ss) * g.nc_max + cc]);
-          const float yv = bf16_to_f32(s_x3y[m * g.nc_max + cc]);
-          const float r2 = bf16_to_f32(f32_to_bf16(fmaf(yv, s_iw[m * HC + ss], rv)));
+          const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(bf16_to_f32(s_x3y[m * g.nc_max + cc]),
+                                                                s_iw[m * HC + ss], rv)))
+                                 : rv;
           const float xn = r2 * s_rr[m * HC + ss] * (1.0f + bf16_to_f32(s_x3w[ss * g.nc_max + cc]));
           sum = fmaf(s_g[m * g.rows_u + ss * g.nc_max + cc], xn, sum);
         }

@@ -46,9 +46,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 struct Range {
   uintptr_t lo, hi;  // [lo, hi)
 };
-Range span(const void* p, int64_t bytes) {
+Range span(const void* p, int64_t bytes) {   // NULL: the empty range
   const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
-  return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+  return p ? Range{lo, lo + static_cast<uintptr_t>(bytes)} : Range{0, 0};
 }
 bool overlap(const Range& a, const Range& b) {
   return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo;
@@ -176,8 +176,10 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
   const int64_t ld_inj = a->ld_inj == 0 ? HC : a->ld_inj;
   if (ld_inj < HC) return HC_GR_ERR_INVALID_ARG;
   const bool merged = a->Wdi != nullptr;
-  if (!a->R || !a->y || !a->inj || !a->Wnorm || !a->Wu || !a->R2 || !a->rrms ||
-      !a->inj_next || !a->x)
+  // y, inj and R2 all NULL: the mix alone (R is the combined residual)
+  const bool mix_only = !a->y && !a->inj && !a->R2;
+  if (!mix_only && (!a->y || !a->inj || !a->R2)) return HC_GR_ERR_INVALID_ARG;
+  if (!a->R || !a->Wnorm || !a->Wu || !a->rrms || !a->inj_next || !a->x)
     return HC_GR_ERR_INVALID_ARG;
   if (!merged && (!a->Wd || !a->Wi)) return HC_GR_ERR_INVALID_ARG;
   const void* p16[] = {a->R, a->y, a->Wnorm, a->Wu, a->R2, a->x, a->lora,
@@ -258,6 +260,50 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
   if (e == cudaErrorNotSupported) return HC_GR_ERR_UNSUPPORTED;
   if (e != cudaSuccess) return cuda_fail(h, e);
   return HC_GR_OK;
+}
+
+int hc_gr_combine(hc_gr_handle h, int64_t M, int HC, int HS, const void* R, const void* y,
+                  const float* inj, int64_t ld_inj, void* R2, struct CUstream_st* stream) {
+  if (!h || !R || !y || !inj || !R2) return HC_GR_ERR_INVALID_ARG;
+  if (M < 1 || HC < 1 || HS < 1) return HC_GR_ERR_INVALID_ARG;
+  if (ld_inj == 0) ld_inj = HC;
+  if (ld_inj < HC) return HC_GR_ERR_INVALID_ARG;
+  if (!aligned(R, 16) || !aligned(y, 16) || !aligned(R2, 16) || !aligned(inj, 4))
+    return HC_GR_ERR_INVALID_ARG;
+  if (HS % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
+  const int64_t K = static_cast<int64_t>(HC) * HS;
+  const Range out = span(R2, M * K * 2);
+  if (overlap(out, span(R, M * K * 2)) || overlap(out, span(y, M * HS * 2)) ||
+      overlap(out, span(inj, ((M - 1) * ld_inj + HC) * 4)))
+    return HC_GR_ERR_ALIAS;
+  DeviceGuard guard(h->dev.id);
+  const cudaError_t e = hcgr::launch_combine(
+      M, HC, HS, static_cast<const hcgr::bf16_t*>(R), static_cast<const hcgr::bf16_t*>(y), inj,
+      ld_inj, static_cast<hcgr::bf16_t*>(R2), h->dev, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(h, e);
+  return HC_GR_OK;
+}
+
+int hc_gr_mix(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps, const void* R,
+              const void* Wnorm, const void* Wd, const void* Wi, const void* Wu, float* rrms,
+              float* inj_next, void* x, float* lora, struct CUstream_st* stream) {
+  hc_gr_args a;
+  std::memset(&a, 0, sizeof(a));
+  a.M = M;
+  a.HC = HC;
+  a.HS = HS;
+  a.r = r;
+  a.eps = eps;
+  a.R = R;
+  a.Wnorm = Wnorm;
+  a.Wd = Wd;
+  a.Wi = Wi;
+  a.Wu = Wu;
+  a.rrms = rrms;
+  a.inj_next = inj_next;
+  a.x = x;
+  a.lora = lora;
+  return hc_gr_forward_ex(h, &a, stream);
 }
 
 int hc_gr_forward(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps, const void* R,

@@ -37,7 +37,7 @@ struct Call {
   int HC, HS, r, K, n_out;
   float eps;
   const bf16_t* R;
-  const bf16_t* y;
+  const bf16_t* y;    // NULL: mix only -- R holds the combined streams (R2 = R), inj unused
   const float* inj;
   int64_t ld_inj;
   const bf16_t* Wnorm;
@@ -45,7 +45,7 @@ struct Call {
   const bf16_t* Wi;   // row j < HC of the inject weight:   Wi + j * K
   int fold;
   const bf16_t* Wu;
-  bf16_t* R2;
+  bf16_t* R2;         // NULL (mix only): not stored
   float* rrms;
   float* inj_next;
   bf16_t* x;
@@ -70,6 +70,11 @@ size_t decode_xred_words(const Device& dev, int64_t M, int HC, int HS, int r);
 size_t decode_xgat_words(int n_out_max);
 cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
                           cudaStream_t stream);
+
+// COMBINE alone: R2 = bf16(R + y * 2 sigmoid(inj / HC)), one streaming kernel.
+cudaError_t launch_combine(int64_t M, int HC, int HS, const bf16_t* R, const bf16_t* y,
+                           const float* inj, int64_t ld_inj, bf16_t* R2, const Device& dev,
+                           cudaStream_t stream);
 
 // Prefill path: tcgen05 tensor-core kernels.
 cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev,

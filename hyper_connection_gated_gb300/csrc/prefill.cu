@@ -36,6 +36,7 @@
 //   per-stream slots; epilogue warps read a row's gates stream by stream,
 //   apply sigmoid, rebuild xn from R2, rrms and 1 + Wnorm and store
 //   x = (1/HC) * sum_s G * xn.
+#include <cstring>
 #include <algorithm>
 
 #include "hc_gr_internal.cuh"
@@ -68,17 +69,18 @@ constexpr int WI_ROWS = 16;   // inject rows in the MMA's B tile (HC real, rest 
 
 struct K1Params {
   CUtensorMap tm_R;    // [M][K], box {64, 128}, 128B swizzle
-  CUtensorMap tm_y;    // [M][HS], box {64, 128}, 128B swizzle
+  CUtensorMap tm_y;    // [M][HS], box {64, 128}, 128B swizzle (unused when !has_y)
   CUtensorMap tm_w0;   // Wd rows [0, wrows0): box {64, wrows0}, 128B swizzle
   CUtensorMap tm_w1;   // Wd rows [wrows0, r): box {64, r - wrows0}, 128B swizzle
   CUtensorMap tm_wi;   // Wi [HC][K], box {64, 16} (128B swizzle) or {64, HC} (plain)
   const float* inj;
   int64_t ld_inj;
-  bf16_t* R2;
+  bf16_t* R2;         // NULL: R2 not stored (mix only)
   const bf16_t* Wnorm;
   float* part;        // [tile][HC * S][np][128 rows]: lora columns, then the HC inject columns
   float* sumsq;       // [tile][HC * S][128 rows] partial sums of R2^2
   int M, HS, K, r, np, fold;
+  int has_y;          // 0: mix only -- R is already the combined residual, y and inj unused
   int S;              // K chunks per stream
   int nkb;
   int n1, n2;         // MMA column blocks (B rows): [0, n1) and [n1, n1 + n2); n2 may be 0
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 
   if (tid == 0) {
     prefetch_tmap(&p.tm_R);
-    prefetch_tmap(&p.tm_y);
+    if (p.has_y) prefetch_tmap(&p.tm_y);
     prefetch_tmap(&p.tm_w0);
     prefetch_tmap(&p.tm_w1);
     prefetch_tmap(&p.tm_wi);
@@ -156,9 +158,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
         if (!ok) break;
         const uint32_t sb = sbase + st * RY_BYTES;
         const int kx = (kb0 + kb) * BK;           // column within the stream
-        mbar_arrive_expect_tx(ryfull(st), RY_BYTES + 128 + wic_tx);
+        mbar_arrive_expect_tx(ryfull(st), (p.has_y ? RY_BYTES : TILE_BYTES) + 128 + wic_tx);
         tma_load_2d(sb, &p.tm_R, s * HS + kx, m0, ryfull(st));
-        tma_load_2d(sb + TILE_BYTES, &p.tm_y, kx, m0, ryfull(st));
+        if (p.has_y) tma_load_2d(sb + TILE_BYTES, &p.tm_y, kx, m0, ryfull(st));
         bulk_g2s(sbase + p.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kx, 128,
                  ryfull(st));
         if constexpr (!INJ_MMA)
@@ -252,7 +254,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     for (int pp = 0; pp < 4; ++pp) {
       const int m = m0 + rbase + 32 * pp;
       valid[pp] = m < p.M;
-      iw[pp] = valid[pp] ? combine_weight(p.inj[m * p.ld_inj + s], 1.0f / static_cast<float>(HC)) : 0.f;
+      iw[pp] = valid[pp] && p.has_y ? combine_weight(p.inj[m * p.ld_inj + s], 1.0f / static_cast<float>(HC))
+                                    : 0.f;
       ss[pp] = 0.f;
 #pragma unroll
       for (int j = 0; j < HC; ++j) ij[pp][j] = 0.f;
@@ -278,13 +281,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       for (int pp = 0; pp < 4; ++pp) {
         const int row = rbase + 32 * pp;
         const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-        float rv[8], yv[8], a[8];
-        unpack8(*reinterpret_cast<const uint4*>(sb + off), rv);
-        unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
+        float rv[8], yv[8] = {}, a[8];
+        const uint4 rraw = *reinterpret_cast<const uint4*>(sb + off);
+        const uint32_t rw[4] = {rraw.x, rraw.y, rraw.z, rraw.w};
+        unpack8(rraw, rv);
+        if (p.has_y) unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
         uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pr[e] = pack2(fmaf(yv[2 * e], iw[pp], rv[2 * e]), fmaf(yv[2 * e + 1], iw[pp], rv[2 * e + 1]));
+          pr[e] = p.has_y ? pack2(fmaf(yv[2 * e], iw[pp], rv[2 * e]), fmaf(yv[2 * e + 1], iw[pp], rv[2 * e + 1]))
+                          : rw[e];
           const float r0 = lo_bf16(pr[e]), r1 = hi_bf16(pr[e]);
           ss[pp] = fmaf(r0, r0, ss[pp]);
           ss[pp] = fmaf(r1, r1, ss[pp]);
@@ -293,7 +299,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
           ph[e] = pack2(a[2 * e], a[2 * e + 1]);
           pl[e] = pack2(a[2 * e] - lo_bf16(ph[e]), a[2 * e + 1] - hi_bf16(ph[e]));
         }
-        if (valid[pp])
+        if (valid[pp] && p.R2)
           *reinterpret_cast<uint4*>(p.R2 + static_cast<int64_t>(m0 + row) * p.K +
                                     static_cast<int64_t>(s) * HS + col) =
               make_uint4(pr[0], pr[1], pr[2], pr[3]);
@@ -864,7 +870,12 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     if (!make_tmap_bf16(&p.tm_R, c.R, 2, dR, sR, bT, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
     const uint64_t dy[2] = {static_cast<uint64_t>(c.HS), static_cast<uint64_t>(M)};
     const uint64_t sy[1] = {static_cast<uint64_t>(c.HS) * 2};
-    if (!make_tmap_bf16(&p.tm_y, c.y, 2, dy, sy, bT, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    if (c.y) {
+      if (!make_tmap_bf16(&p.tm_y, c.y, 2, dy, sy, bT, CU_TENSOR_MAP_SWIZZLE_128B)) return cudaErrorInvalidValue;
+    } else {
+      std::memset(&p.tm_y, 0, sizeof(p.tm_y));
+    }
+    p.has_y = c.y != nullptr;
     // MMA column blocks over the B tile (r rows of Wd, then 16 inject rows
     // when the inject products run on the tensor cores)
     const int ntot = c.r + (inj_mma ? WI_ROWS : 0);
@@ -978,7 +989,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const CUtensorMapSwizzle sw = ncu == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
     if (!make_tmap_bf16(&p.tm_h, h, 2, dh, sh, bh, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_tmap_bf16(&p.tm_wu, c.Wu, 3, du, su, bu, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_bf16(&p.tm_r2, c.R2, 2, dr, sr, br, sw) ||
+        !make_tmap_bf16(&p.tm_r2, c.R2 ? c.R2 : c.R, 2, dr, sr, br, sw) ||   // mix only: R2 = R
         !make_tmap(&p.tm_w1, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w1, 2, dn, sn, bn))
       return cudaErrorInvalidValue;
     p.rrms = c.rrms;

@@ -136,8 +136,35 @@ int hc_gr_forward(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps,
                   struct CUstream_st* stream);
 
 /* Same operation with every option: a merged (optionally folded) weight, a
- * strided inj and a forced path. */
+ * strided inj and a forced path.  With y, inj and R2 all NULL the call is
+ * the mix alone (see hc_gr_mix); NULL in only some of them is INVALID_ARG. */
 int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* stream);
+
+/* COMBINE alone (the page's combine-only entry point, "Behavior and intent";
+ * the formula of the (COMBINE) bullet): R2 = bf16(R + y * 2 sigmoid(inj /
+ * HC)) for M tokens, nothing else.  For layers that apply COMBINE apart from
+ * the mix.  R2 is bit-identical to the R2 hc_gr_forward stores for the same
+ * inputs.
+ *   R, R2 [M, HC, HS] bf16 (16-byte aligned), y [M, HS] bf16 (16-byte
+ *   aligned), inj [M, HC] fp32 with row stride ld_inj >= HC floats (0 means
+ *   HC; 4-byte aligned), so the strided inj_next of a previous call can be
+ *   passed as it is.  Any M >= 1 and HC >= 1; HS a multiple of 8
+ *   (UNSUPPORTED otherwise).  The handle supplies the device and keeps the
+ *   last CUDA error; its workspace is not used and its size limits do not
+ *   apply.  R2 must not overlap R, y or inj (ALIAS).  One kernel launch,
+ *   asynchronous on `stream`. */
+int hc_gr_combine(hc_gr_handle h, int64_t M, int HC, int HS, const void* R, const void* y,
+                  const float* inj, int64_t ld_inj, void* R2, struct CUstream_st* stream);
+
+/* The mix alone (the page's mix entry point, "Behavior and intent"): every
+ * step after COMBINE -- (N), (G1), (INJ), (G2), (MIX) -- with R taken as
+ * the already-combined streams (R2 = R; nothing is injected and R2 is not
+ * written).  Outputs rrms, inj_next, x and lora (may be NULL) as in
+ * hc_gr_forward, the same limits, layouts and paths.  Equivalent to
+ * hc_gr_forward_ex with y = inj = R2 = NULL. */
+int hc_gr_mix(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps, const void* R,
+              const void* Wnorm, const void* Wd, const void* Wi, const void* Wu, float* rrms,
+              float* inj_next, void* x, float* lora, struct CUstream_st* stream);
 
 /* Waits for `stream`, then returns the device status recorded by the
  * handle's kernels since the last check (HC_GR_OK or HC_GR_ERR_TIMEOUT).

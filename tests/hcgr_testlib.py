@@ -64,6 +64,18 @@ def oracle_ref(case: dict, rows=None, Wdi_bits=None, fold_w=False) -> dict:
     return oracle.forward(**kw)
 
 
+def oracle_mix_ref(case: dict, rows=None, Wdi_bits=None, fold_w=False) -> dict:
+    """fp64 oracle of the mix alone, with the case's R as the combined residual."""
+    sel = slice(None) if rows is None else np.asarray(rows)
+    kw = dict(Wnorm=f64(case, "Wnorm"), Wu=f64(case, "Wu"), eps=case["shape"].eps)
+    if Wdi_bits is not None:
+        kw["Wdi"] = inputs.bf16_bits_to_f64(Wdi_bits)
+        kw["fold_w"] = fold_w
+    else:
+        kw["Wd"], kw["Wi"] = f64(case, "Wd"), f64(case, "Wi")
+    return oracle.mix(inputs.bf16_bits_to_f64(case["R"][sel]), **kw)
+
+
 def to_f64(t) -> np.ndarray:
     import torch
 
@@ -76,6 +88,8 @@ def parity_report(got: dict, ref: dict, rows=None) -> dict:
     rep = {}
     M = ref["x"].shape[0]
     for k in ("R2", "x"):
+        if k not in got or k not in ref:      # the mix alone produces no R2
+            continue
         g = to_f64(got[k])[sel].reshape(M, -1)
         o = ref[k].reshape(M, -1)
         rep[k] = float(np.max(np.abs(g - o) / (TOL_BF16 * (1.0 + np.abs(o)))))
