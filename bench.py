@@ -46,8 +46,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # were taken on: if those changed since, roofline.traffic is null.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "4525dd2f469fb05c8a7e079c55dcefed09c9deaaa6e98a46896ab1210bd1e902",
-    "bytes": {2: 13337344, 4: 13398528, 8: 13494528, 16: 13697792, 32: 14125056},
+    "sources_sha256": "2344b0152f5eae78caa75f5952bf04076da5fcd77648e1b9b7eb1bba2307c171",
+    "bytes": {2: 13339648, 4: 13391872, 8: 13496320, 16: 13698304, 32: 14127104},
 }
 
 
@@ -426,9 +426,14 @@ def run_case(args):
     a = inputs.activations(M, shape, distinct_rows=4096)
     R, y, inj = bf(a["R"]), bf(a["y"]), torch.from_numpy(a["inj"]).cuda()
     op = HcGatedResidual(max_M=M, HC=shape.HC, HS=shape.HS, r=shape.r)
-    path = {"auto": 0, "decode": 1, "prefill": 2}[args.case]
     for _ in range(args.calls):
-        op.forward(R, y, inj, w["Wnorm"], w["Wu"], Wd=w["Wd"], Wi=w["Wi"], force_path=path)
+        if args.case == "combine":
+            op.combine(R, y, inj)
+        elif args.case == "mix":
+            op.mix(R, w["Wnorm"], w["Wu"], Wd=w["Wd"], Wi=w["Wi"])
+        else:
+            path = {"auto": 0, "decode": 1, "prefill": 2}[args.case]
+            op.forward(R, y, inj, w["Wnorm"], w["Wu"], Wd=w["Wd"], Wi=w["Wi"], force_path=path)
     op.check()
     torch.cuda.synchronize()
     print(f"case ok: {args.case} M={M} calls={args.calls}")
@@ -609,9 +614,98 @@ def wide_sweep(Ms=WIDE_MS, reps: int = 5):
     return res
 
 
+ENTRY_MS = {"combine": (32, 512, 8192, 65536), "mix": (2, 32, 512, 8192)}
+
+
+def entry_sweep(reps: int = 5):
+    """Per-M latency of the combine-only and mix-only entry points at the
+    default shape (graph replay; sets rotate over more than twice the L2
+    where one set fits in it).  combine: R, y, inj in and R2 out, no weights;
+    mix: the fused path without y, inj and the R2 store."""
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import HcGatedResidual, inputs
+
+    dev = torch.cuda.current_device()
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+    comb_tok = 2 * K_DIM + 2 * HS + 4 * HC + 2 * K_DIM
+    mix_tok = 2 * K_DIM + 4 * HC + 4 * HC + 4 * R_LOW + 2 * HS
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = {k: bf(v) for k, v in inputs.weights().items()}
+    base_rows = 1024
+    a = inputs.activations(base_rows)
+    R0, y0, inj0 = bf(a["R"]), bf(a["y"]), torch.from_numpy(a["inj"]).cuda()
+    hbm, tflops, _ = peaks()
+    res = {}
+    stream = torch.cuda.Stream()
+    for kind, Ms in ENTRY_MS.items():
+        res[kind] = {}
+        for M in Ms:
+            per_set = M * comb_tok if kind == "combine" else WEIGHT_BYTES + M * mix_tok
+            nsets = int(min(256, max(1, np.ceil(2.0 * l2 / per_set))))
+            reps_rows = (M + base_rows - 1) // base_rows
+            R = R0.repeat(reps_rows, 1, 1)[:M].contiguous()
+            y = y0.repeat(reps_rows, 1)[:M].contiguous()
+            inj = inj0.repeat(reps_rows, 1)[:M].contiguous()
+            op = HcGatedResidual(max_M=M)
+            sets = [(R, y, inj, w) if j == 0 else
+                    (R.clone(), y.clone(), inj.clone(),
+                     w if kind == "combine" else {k: v.clone() for k, v in w.items()})
+                    for j in range(nsets)]
+            if kind == "combine":
+                outs = [torch.empty_like(R) for _ in range(nsets)]
+            else:
+                outs = [{"rrms": torch.empty((M, HC), device="cuda"),
+                         "inj_next": torch.empty((M, HC), device="cuda"),
+                         "x": torch.empty((M, HS), dtype=torch.bfloat16, device="cuda"),
+                         "lora": torch.empty((M, R_LOW), device="cuda")} for _ in range(nsets)]
+
+            def call(j):
+                Rj, yj, ij, wj = sets[j]
+                if kind == "combine":
+                    op.combine(Rj, yj, ij, out=outs[j])
+                else:
+                    op.mix(Rj, wj["Wnorm"], wj["Wu"], Wd=wj["Wd"], Wi=wj["Wi"], out=outs[j])
+
+            for j in range(nsets):
+                call(j)
+            op.check()
+            g = torch.cuda.CUDAGraph()
+            calls = max(nsets, 2)
+            with torch.cuda.graph(g, stream=stream):
+                for j in range(calls):
+                    call(j % nsets)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                for _ in range(2):
+                    g.replay()
+                samples = []
+                for _ in range(reps):
+                    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    e0.record(stream)
+                    g.replay()
+                    e1.record(stream)
+                    e1.synchronize()
+                    samples.append(e0.elapsed_time(e1) * 1e3 / calls)
+            us = statistics.median(samples)
+            flops = 0 if kind == "combine" else M * FLOPS_PER_TOKEN
+            roof_us, bound = roofline_us(per_set, flops, hbm, tflops)
+            res[kind][str(M)] = {"us": us, "tokens_per_s": M / (us * 1e-6), "roofline_us": roof_us,
+                                 "bound": bound, "roofline_frac": roof_us / us,
+                                 "l2": f"{nsets} rotating sets" if nsets > 1 else "inputs > L2"}
+            op.close()
+            del sets, outs, R, y, inj
+            torch.cuda.empty_cache()
+    return res
+
+
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--case", choices=["auto", "decode", "prefill"], default=None,
+    ap.add_argument("--case", choices=["auto", "decode", "prefill", "combine", "mix"], default=None,
                     help="only run --calls forward calls of one shape (for profiling)")
     ap.add_argument("--M", type=int, default=32)
     ap.add_argument("--calls", type=int, default=3)
@@ -654,6 +748,7 @@ def main():
     if rank == 0 and not args.no_prefill_sweep:
         line["prefill_sweep_us"] = prefill_sweep()
         line["wide_sweep_us"] = wide_sweep()
+        line["entry_points_us"] = entry_sweep()
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline()
         print(json.dumps(line))
