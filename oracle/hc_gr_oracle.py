@@ -20,7 +20,8 @@ Readings taken where the page leaves a step open:
     argument (the page writes both "h = SiLU(lora / HC)" and "lora
     (pre-SiLU)").
   * eps sits inside the square root, added to the mean of squares.
-  * Wnorm has K entries, one per (stream, channel).
+  * Wnorm has K entries, one per (stream, channel), or HS entries shared by
+    every stream (norm_weight).
   * With a folded weight W' = bf16(W * (1 + Wnorm)), the projections read
     R2 * rrms against W'; the mix still uses the full xn with (1 + Wnorm).
 
@@ -81,10 +82,23 @@ def grouped_rrms(R2, eps):
     return 1.0 / np.sqrt(ms + eps)
 
 
+def norm_weight(Wnorm, HC, HS):
+    """The norm weight as [HC, HS]: a full-width weight has K = HC * HS
+    entries, one per (stream, channel); an [HS] weight is one per channel,
+    shared by every stream (the page's default next to its "full-width norm
+    weights" variant)."""
+    w = np.asarray(Wnorm, np.float64).reshape(-1)
+    if w.size == HC * HS:
+        return w.reshape(HC, HS)
+    if w.size == HS:
+        return np.broadcast_to(w[None, :], (HC, HS))
+    raise ValueError("Wnorm must have HC * HS or HS entries")
+
+
 def normalise(R2, rrms, Wnorm):
     """(N) xn[s, c] = R2[s, c] * rrms_s * (1 + Wnorm[s, c]), flattened to K."""
     M, HC, HS = R2.shape
-    w = np.asarray(Wnorm, np.float64).reshape(HC, HS)
+    w = norm_weight(Wnorm, HC, HS)
     xn = R2 * rrms[:, :, None] * (1.0 + w)[None]
     return xn.reshape(M, HC * HS)
 
@@ -138,7 +152,7 @@ def merge_weight(Wd, Wi, Wnorm, n_pad, fold):
     W[:r] = Wd
     W[r:r + HC] = Wi
     if fold:
-        W[:r + HC] *= (1.0 + np.asarray(Wnorm, np.float64))[None, :]
+        W[:r + HC] *= (1.0 + norm_weight(Wnorm, HC, K // HC).reshape(K))[None, :]
     return W
 
 

@@ -302,6 +302,30 @@ def test_mix_constant_rows_closed_form():
     np.testing.assert_allclose(out["lora"], np.full((2, r), HS * xs.sum()), rtol=1e-14)
 
 
+def test_broadcast_norm_weight_is_the_tiled_full_width_one():
+    # An [HS] norm weight acts on every stream alike: the same outputs as the
+    # K-entry weight that repeats it HC times, and a stream permutation of
+    # R no longer needs a matching permutation of Wnorm.
+    rng = np.random.default_rng(17)
+    M, HC, HS, r = 3, 4, 16, 8
+    c = _case(rng, M, HC, HS, r)
+    w_hs = _rand(rng, HS, scale=0.1)
+    a = oracle.forward(**dict(c, Wnorm=w_hs))
+    b = oracle.forward(**dict(c, Wnorm=np.tile(w_hs, HC)))
+    for k in ("R2", "rrms", "xn", "lora", "inj_next", "x"):
+        np.testing.assert_array_equal(a[k], b[k])
+    xn = a["xn"].reshape(M, HC, HS)
+    R2 = a["R2"]
+    for s_ in range(HC):
+        np.testing.assert_allclose(xn[:, s_], R2[:, s_] * a["rrms"][:, s_, None] * (1.0 + w_hs),
+                                   rtol=1e-15)
+    Wf = oracle.merge_weight(c["Wd"], c["Wi"], w_hs, n_pad=12, fold=True)
+    np.testing.assert_array_equal(Wf, oracle.merge_weight(c["Wd"], c["Wi"], np.tile(w_hs, HC), 12,
+                                                          fold=True))
+    with pytest.raises(ValueError):
+        oracle.forward(**dict(c, Wnorm=np.zeros(HS + 1)))
+
+
 def test_fold_equivalence_exact_weights():
     # Folding (1 + Wnorm) into the weight columns is the same product when the
     # fold is kept in float64; the mix still sees (1 + Wnorm).
