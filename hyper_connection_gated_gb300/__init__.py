@@ -53,7 +53,8 @@ class HcGatedResidual:
         """Validates one call's tensors once and returns (args, out).
 
         R [M, HC, HS] bf16, y [M, HS] bf16, inj [M, HC] fp32 (rows may be
-        strided), Wnorm [K] bf16, Wu [K, r] bf16, and either Wd [r, K] + Wi
+        strided), Wnorm [K] bf16 (or [HS]: one norm weight per channel,
+        shared by every stream), Wu [K, r] bf16, and either Wd [r, K] + Wi
         [HC, K] or a merged Wdi [n_pad, K] (fold_w: (1 + Wnorm) folded in).
         y = inj = None is the mix alone: R is the combined residual and no R2
         is produced.  out holds R2, rrms, inj_next, x (and lora); they are
@@ -83,7 +84,7 @@ class HcGatedResidual:
                 raise HcGrError(ERR_INVALID_ARG, "inj must be fp32 on the same device, unit column stride")
             if tuple(y.shape) != (M, HS) or tuple(inj.shape) != (M, HC):
                 raise HcGrError(ERR_INVALID_ARG, "shape mismatch")
-        if Wnorm.numel() != HC * HS or tuple(Wu.shape) != (HC * HS, r):
+        if Wnorm.numel() not in (HC * HS, HS) or tuple(Wu.shape) != (HC * HS, r):
             raise HcGrError(ERR_INVALID_ARG, "shape mismatch")
         if out is None:
             out = {} if mix_only else {"R2": torch.empty_like(R)}
@@ -101,6 +102,7 @@ class HcGatedResidual:
             a.y, a.inj = y.data_ptr(), inj.data_ptr()
             a.ld_inj = inj.stride(0) if M > 1 else HC
         a.Wnorm, a.Wu = Wnorm.data_ptr(), Wu.data_ptr()
+        a.wnorm_hs = 1 if Wnorm.numel() != HC * HS else 0
         if Wdi is not None:
             a.Wdi, a.n_pad = Wdi.data_ptr(), Wdi.shape[0]
         else:

@@ -36,6 +36,7 @@ class Args(ctypes.Structure):
         ("Wu", _vp), ("R2", _vp), ("rrms", _fp), ("inj_next", _fp), ("x", _vp), ("lora", _fp),
         ("force_path", ctypes.c_int32), ("debug_fault", ctypes.c_int32),
         ("pdl", ctypes.c_int32),
+        ("wnorm_hs", ctypes.c_int32),
     ]
 
 

@@ -344,7 +344,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         cp_async4(s_x3y + m * g.nc_max + cc, c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
       } else {
         const int j = i - n_iw - n_r - n_y, ss = j / np, cc = 2 * (j - ss * np);
-        cp_async4(s_x3w + ss * g.nc_max + cc, c.Wnorm + ss * HS + cp0 + cc);
+        cp_async4(s_x3w + ss * g.nc_max + cc, c.Wnorm + ss * c.ld_wnorm + cp0 + cc);
       }
     }
   }
@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc0);
         unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
       }
-      unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + k0 + un * 8)), wv);
+      unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + s * c.ld_wnorm + c0 + un * 8)), wv);
       uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {

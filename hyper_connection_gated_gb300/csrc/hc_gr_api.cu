@@ -200,7 +200,8 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
                         span(a->inj_next, M * HC * 4), span(a->x, M * HS * 2),
                         a->lora ? span(a->lora, M * r * 4) : Range{0, 0}};
   const Range ins[] = {span(a->R, M * K * 2), span(a->y, M * HS * 2),
-                       span(a->inj, ((M - 1) * ld_inj + HC) * 4), span(a->Wnorm, K * 2),
+                       span(a->inj, ((M - 1) * ld_inj + HC) * 4),
+                       span(a->Wnorm, (a->wnorm_hs ? HS : K) * 2),
                        span(a->Wu, K * r * 2),
                        merged ? span(a->Wdi, static_cast<int64_t>(a->n_pad) * K * 2)
                               : span(a->Wd, static_cast<int64_t>(r) * K * 2),
@@ -226,6 +227,7 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
   c.inj = a->inj;
   c.ld_inj = ld_inj;
   c.Wnorm = static_cast<const bf16_t*>(a->Wnorm);
+  c.ld_wnorm = a->wnorm_hs ? 0 : HS;
   if (merged) {
     c.Wd = static_cast<const bf16_t*>(a->Wdi);
     c.Wi = c.Wd + static_cast<int64_t>(r) * K;

@@ -41,6 +41,7 @@ struct Call {
   const float* inj;
   int64_t ld_inj;
   const bf16_t* Wnorm;
+  int64_t ld_wnorm;   // entries between two streams' Wnorm slices: HS, or 0 (one [HS] slice shared)
   const bf16_t* Wd;   // row n < r of the projection weight: Wd + n * K
   const bf16_t* Wi;   // row j < HC of the inject weight:   Wi + j * K
   int fold;

@@ -145,6 +145,7 @@ extern "C" int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps
   c.inj = inj;
   c.ld_inj = HC;
   c.Wnorm = static_cast<const bf16_t*>(Wnorm);
+  c.ld_wnorm = HS;
   c.Wd = static_cast<const bf16_t*>(Wd);
   c.Wi = static_cast<const bf16_t*>(Wi);
   c.fold = 0;

@@ -38,6 +38,7 @@
 //   x = (1/HC) * sum_s G * xn.
 #include <cstring>
 #include <algorithm>
+#include <type_traits>
 
 #include "hc_gr_internal.cuh"
 #include "tmap.h"
@@ -77,6 +78,7 @@ struct K1Params {
   int64_t ld_inj;
   bf16_t* R2;         // NULL: R2 not stored (mix only)
   const bf16_t* Wnorm;
+  int64_t ld_wnorm;   // HS, or 0 when one [HS] Wnorm is shared by every stream
   float* part;        // [tile][HC * S][np][128 rows]: lora columns, then the HC inject columns
   float* sumsq;       // [tile][HC * S][128 rows] partial sums of R2^2
   int M, HS, K, r, np, fold;
@@ -161,7 +163,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
         mbar_arrive_expect_tx(ryfull(st), (p.has_y ? RY_BYTES : TILE_BYTES) + 128 + wic_tx);
         tma_load_2d(sb, &p.tm_R, s * HS + kx, m0, ryfull(st));
         if (p.has_y) tma_load_2d(sb + TILE_BYTES, &p.tm_y, kx, m0, ryfull(st));
-        bulk_g2s(sbase + p.off_wn + st * 128, p.Wnorm + static_cast<int64_t>(s) * HS + kx, 128,
+        bulk_g2s(sbase + p.off_wn + st * 128, p.Wnorm + s * p.ld_wnorm + kx, 128,
                  ryfull(st));
         if constexpr (!INJ_MMA)
           tma_load_2d(sbase + p.off_wic + st * HC * 128, &p.tm_wi, s * HS + kx, 0, ryfull(st));
@@ -260,18 +262,21 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 #pragma unroll
       for (int j = 0; j < HC; ++j) ij[pp][j] = 0.f;
     }
-    bool ok = true;
+    // The K-block loop in two copies, with COMBINE (y injected) and without
+    // (mix only: R is R2), so the call-uniform choice stays out of the
+    // per-element code.
+    auto convert = [&](auto has_y_c) -> bool {
+    constexpr bool HY = decltype(has_y_c)::value;
     for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % NRY;
-      ok = mbar_wait_bounded(ryfull(st), (kb / NRY) & 1, p.err, p.limit_ns);
-      if (!ok) break;
+      if (!mbar_wait_bounded(ryfull(st), (kb / NRY) & 1, p.err, p.limit_ns)) return false;
       unsigned char* sb = smem + st * RY_BYTES;
       const int col = (kb0 + kb) * BK + ch * 8;   // channel within the stream
       float f[8];
       unpack8(*reinterpret_cast<const uint4*>(smem + p.off_wn + st * 128 + ch * 16), f);
 #pragma unroll
       for (int e = 0; e < 8; ++e) f[e] += 1.0f;
-      float wi[INJ_MMA ? 1 : HC][8];
+      [[maybe_unused]] float wi[INJ_MMA ? 1 : HC][8];
       if constexpr (!INJ_MMA) {
 #pragma unroll
         for (int j = 0; j < HC; ++j)
@@ -281,16 +286,18 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       for (int pp = 0; pp < 4; ++pp) {
         const int row = rbase + 32 * pp;
         const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-        float rv[8], yv[8] = {}, a[8];
+        float rv[8], yv[8], a[8];
         const uint4 rraw = *reinterpret_cast<const uint4*>(sb + off);
         const uint32_t rw[4] = {rraw.x, rraw.y, rraw.z, rraw.w};
         unpack8(rraw, rv);
-        if (p.has_y) unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
+        if constexpr (HY) unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
         uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          pr[e] = p.has_y ? pack2(fmaf(yv[2 * e], iw[pp], rv[2 * e]), fmaf(yv[2 * e + 1], iw[pp], rv[2 * e + 1]))
-                          : rw[e];
+          if constexpr (HY)
+            pr[e] = pack2(fmaf(yv[2 * e], iw[pp], rv[2 * e]), fmaf(yv[2 * e + 1], iw[pp], rv[2 * e + 1]));
+          else
+            pr[e] = rw[e];
           const float r0 = lo_bf16(pr[e]), r1 = hi_bf16(pr[e]);
           ss[pp] = fmaf(r0, r0, ss[pp]);
           ss[pp] = fmaf(r1, r1, ss[pp]);
@@ -299,7 +306,7 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
           ph[e] = pack2(a[2 * e], a[2 * e + 1]);
           pl[e] = pack2(a[2 * e] - lo_bf16(ph[e]), a[2 * e + 1] - hi_bf16(ph[e]));
         }
-        if (valid[pp] && p.R2)
+        if (HY && valid[pp])
           *reinterpret_cast<uint4*>(p.R2 + static_cast<int64_t>(m0 + row) * p.K +
                                     static_cast<int64_t>(s) * HS + col) =
               make_uint4(pr[0], pr[1], pr[2], pr[3]);
@@ -323,6 +330,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       __syncwarp();
       if (lane == 0) mbar_arrive(conv(st));
     }
+    return true;
+    };
+    bool ok = p.has_y ? convert(std::true_type{}) : convert(std::false_type{});
     // per-row totals: the 8 lanes of a row hold its 8 channel chunks
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
@@ -407,14 +417,14 @@ __global__ void __launch_bounds__(RED_THREADS)
     k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
                      float* __restrict__ rrms, float* __restrict__ lora,
                      float* __restrict__ inj_next, bf16_t* __restrict__ hh,
-                     const bf16_t* __restrict__ Wnorm, float* __restrict__ w1, int M, int S,
-                     int r, int np, int HS, float inv_hs, float eps) {
+                     const bf16_t* __restrict__ Wnorm, int ld_wnorm, float* __restrict__ w1,
+                     int M, int S, int r, int np, int HS, float inv_hs, float eps) {
   __shared__ float s_acc[RED_COLS][BM + 1];
   const int tid = threadIdx.x;
   const int bid = blockIdx.y * gridDim.x + blockIdx.x;
   const int K = HC * HS;
   for (int k = bid * RED_THREADS + tid; k < K; k += gridDim.x * gridDim.y * RED_THREADS)
-    w1[k] = 1.0f + bf16_to_f32(Wnorm[k]);
+    w1[k] = 1.0f + bf16_to_f32(Wnorm[(k / HS) * ld_wnorm + k % HS]);
   const int tile = blockIdx.y, n0 = blockIdx.x * RED_COLS;
   // thread = (4 consecutive rows, 2 columns): rows 4 (tid % 32) .., columns
   // n0 + tid / 32 and n0 + tid / 32 + 8; a warp reads 512 contiguous bytes
@@ -903,6 +913,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     p.ld_inj = c.ld_inj;
     p.R2 = c.R2;
     p.Wnorm = c.Wnorm;
+    p.ld_wnorm = c.ld_wnorm;
     p.part = part;
     p.sumsq = sumsq;
     p.M = M;
@@ -957,7 +968,8 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
 #define HCGR_RED(HCV)                                                                        \
   case HCV:                                                                                  \
     k1_reduce_kernel<HCV><<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,     \
-                                                          c.inj_next, h, c.Wnorm, w1, M, S,  \
+                                                          c.inj_next, h, c.Wnorm,            \
+                                                          static_cast<int>(c.ld_wnorm), w1, M, S,  \
                                                           c.r, np, c.HS, 1.0f / c.HS, c.eps);\
     break;
     switch (c.HC) {

@@ -24,7 +24,8 @@
  *   R, R2      [M, HC, HS] bf16        y, x      [M, HS] bf16
  *   inj        [M, HC] fp32 (row stride ld_inj >= HC in hc_gr_forward_ex)
  *   rrms, inj_next [M, HC] fp32        lora      [M, r] fp32
- *   Wnorm      [K] bf16                Wd        [r, K] bf16
+ *   Wnorm      [K] bf16 (or [HS], shared by the streams: hc_gr_args.wnorm_hs)
+ *                                      Wd        [r, K] bf16
  *   Wi         [HC, K] bf16            Wu        [K, r] bf16
  *   Wdi        [n_pad, K] bf16 merged down/inject weight: rows 0..r-1 = Wd,
  *              rows r..r+HC-1 = Wi, rows r+HC..n_pad-1 are never read.  With
@@ -116,6 +117,10 @@ typedef struct hc_gr_args {
                           not write them; activations are read and outputs
                           written only after it has finished.  0: plain stream
                           order.  The prefill kernels ignore it. */
+  int32_t wnorm_hs;    /* 1: Wnorm has HS entries, one per channel, shared by
+                          every stream (xn[s, c] = R2[s, c] rrms[s]
+                          (1 + Wnorm[c])); 0: the full-width [K] layout.  A
+                          folded Wdi then carries (1 + Wnorm[k mod HS]). */
 } hc_gr_args;
 
 /* Creates a handle bound to `device` and allocates its workspace for calls
