@@ -262,20 +262,32 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 #pragma unroll
       for (int j = 0; j < HC; ++j) ij[pp][j] = 0.f;
     }
-    // The K-block loop in two copies, with COMBINE (y injected) and without
-    // (mix only: R is R2), so the call-uniform choice stays out of the
-    // per-element code.
-    auto convert = [&](auto has_y_c) -> bool {
+    // The K-block loop in four copies -- with COMBINE (y injected) or without
+    // (mix only: R is R2), for a folded weight (the operand is R2 itself) or
+    // an unfolded one (the hi/lo split of R2 * (1 + Wnorm)) -- so that
+    // call-uniform choices stay out of the per-element code.  Element pairs
+    // go through the paired fp32 instructions (FFMA2 / FMUL2); each lane is
+    // an ordinary round-to-nearest fma or multiply, so R2 is the same as
+    // with scalar fmaf.
+    float2 ss2[4];
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) ss2[pp] = make_float2(0.f, 0.f);
+    auto convert = [&](auto has_y_c, auto fold_c) -> bool {
     constexpr bool HY = decltype(has_y_c)::value;
+    constexpr bool FOLD = decltype(fold_c)::value;
     for (int kb = 0; kb < nkb; ++kb) {
       const int st = kb % NRY;
       if (!mbar_wait_bounded(ryfull(st), (kb / NRY) & 1, p.err, p.limit_ns)) return false;
       unsigned char* sb = smem + st * RY_BYTES;
       const int col = (kb0 + kb) * BK + ch * 8;   // channel within the stream
-      float f[8];
-      unpack8(*reinterpret_cast<const uint4*>(smem + p.off_wn + st * 128 + ch * 16), f);
+      float2 f2[4];
+      if constexpr (!FOLD) {
+        const uint4 wn = *reinterpret_cast<const uint4*>(smem + p.off_wn + st * 128 + ch * 16);
+        const uint32_t ww[4] = {wn.x, wn.y, wn.z, wn.w};
 #pragma unroll
-      for (int e = 0; e < 8; ++e) f[e] += 1.0f;
+        for (int e = 0; e < 4; ++e)
+          f2[e] = __fadd2_rn(make_float2(lo_bf16(ww[e]), hi_bf16(ww[e])), make_float2(1.f, 1.f));
+      }
       [[maybe_unused]] float wi[INJ_MMA ? 1 : HC][8];
       if constexpr (!INJ_MMA) {
 #pragma unroll
@@ -286,31 +298,47 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
       for (int pp = 0; pp < 4; ++pp) {
         const int row = rbase + 32 * pp;
         const uint32_t off = row * 128 + ((ch ^ (row & 7)) << 4);
-        float rv[8], yv[8], a[8];
         const uint4 rraw = *reinterpret_cast<const uint4*>(sb + off);
         const uint32_t rw[4] = {rraw.x, rraw.y, rraw.z, rraw.w};
-        unpack8(rraw, rv);
-        if constexpr (HY) unpack8(*reinterpret_cast<const uint4*>(sb + TILE_BYTES + off), yv);
         uint32_t pr[4], ph[4], pl[4];
+        [[maybe_unused]] float a[8];
+        if constexpr (HY) {
+          const uint4 yraw = *reinterpret_cast<const uint4*>(sb + TILE_BYTES + off);
+          const uint32_t yw[4] = {yraw.x, yraw.y, yraw.z, yraw.w};
+          const float2 iw2 = make_float2(iw[pp], iw[pp]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 v = __ffma2_rn(make_float2(lo_bf16(yw[e]), hi_bf16(yw[e])), iw2,
+                                        make_float2(lo_bf16(rw[e]), hi_bf16(rw[e])));
+            pr[e] = pack2(v.x, v.y);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) pr[e] = rw[e];
+        }
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          if constexpr (HY)
-            pr[e] = pack2(fmaf(yv[2 * e], iw[pp], rv[2 * e]), fmaf(yv[2 * e + 1], iw[pp], rv[2 * e + 1]));
-          else
-            pr[e] = rw[e];
-          const float r0 = lo_bf16(pr[e]), r1 = hi_bf16(pr[e]);
-          ss[pp] = fmaf(r0, r0, ss[pp]);
-          ss[pp] = fmaf(r1, r1, ss[pp]);
-          a[2 * e] = p.fold ? r0 : r0 * f[2 * e];
-          a[2 * e + 1] = p.fold ? r1 : r1 * f[2 * e + 1];
-          ph[e] = pack2(a[2 * e], a[2 * e + 1]);
-          pl[e] = pack2(a[2 * e] - lo_bf16(ph[e]), a[2 * e + 1] - hi_bf16(ph[e]));
+          const float2 r2 = make_float2(lo_bf16(pr[e]), hi_bf16(pr[e]));
+          ss2[pp] = __ffma2_rn(r2, r2, ss2[pp]);
+          if constexpr (FOLD) {
+            a[2 * e] = r2.x;
+            a[2 * e + 1] = r2.y;
+          } else {
+            const float2 av = __fmul2_rn(r2, f2[e]);
+            ph[e] = pack2(av.x, av.y);
+            // a - bf16(a) is exact in fp32, so the fma with -1 is exact too
+            const float2 lo = __ffma2_rn(make_float2(lo_bf16(ph[e]), hi_bf16(ph[e])),
+                                         make_float2(-1.f, -1.f), av);
+            pl[e] = pack2(lo.x, lo.y);
+            a[2 * e] = av.x;
+            a[2 * e + 1] = av.y;
+          }
         }
         if (HY && valid[pp])
           *reinterpret_cast<uint4*>(p.R2 + static_cast<int64_t>(m0 + row) * p.K +
                                     static_cast<int64_t>(s) * HS + col) =
               make_uint4(pr[0], pr[1], pr[2], pr[3]);
-        if (p.fold) {
+        if constexpr (FOLD) {
           *reinterpret_cast<uint4*>(sb + off) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
         } else {
           *reinterpret_cast<uint4*>(sb + off) = make_uint4(ph[0], ph[1], ph[2], ph[3]);
@@ -332,7 +360,12 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
     }
     return true;
     };
-    bool ok = p.has_y ? convert(std::true_type{}) : convert(std::false_type{});
+    using T_ = std::true_type;
+    using F_ = std::false_type;
+    bool ok = p.has_y ? (p.fold ? convert(T_{}, T_{}) : convert(T_{}, F_{}))
+                      : (p.fold ? convert(F_{}, T_{}) : convert(F_{}, F_{}));
+#pragma unroll
+    for (int pp = 0; pp < 4; ++pp) ss[pp] = ss2[pp].x + ss2[pp].y;
     // per-row totals: the 8 lanes of a row hold its 8 channel chunks
 #pragma unroll
     for (int pp = 0; pp < 4; ++pp) {
