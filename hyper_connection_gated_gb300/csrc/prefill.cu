@@ -439,14 +439,16 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // the halving is exact and makes K2's accumulator hold G / 2, the argument of
 // tanh in sigmoid(G) = (1 + tanh(G / 2)) / 2.  The grid also writes
 // w1 = 1 + Wnorm in fp32 for K2's epilogue.  A block takes a 128-row tile
-// x 16 columns: it reads the column-major partials in float4s, 512
+// x RED_COLS columns: it reads the column-major partials in float4s, 512
 // contiguous bytes per warp, column and stream, and transposes through shared
-// memory to write the row-major outputs in 64-byte row runs.
+// memory to write the row-major outputs in 32-byte row runs.  Eight columns
+// a block keep a thread at one column (64 registers at HC <= 4: four blocks
+// an SM), so more loads are in flight per SM than with 16.
 constexpr int RED_THREADS = 256;
-constexpr int RED_COLS = 16;          // columns per block (a block covers a whole 128-row tile)
+constexpr int RED_COLS = 8;           // columns per block (a block covers a whole 128-row tile)
 
 template <int HC>
-__global__ void __launch_bounds__(RED_THREADS)
+__global__ void __launch_bounds__(RED_THREADS, HC <= 4 ? 4 : 2)
     k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
                      float* __restrict__ rrms, float* __restrict__ lora,
                      float* __restrict__ inj_next, bf16_t* __restrict__ hh,
@@ -459,9 +461,9 @@ __global__ void __launch_bounds__(RED_THREADS)
   for (int k = bid * RED_THREADS + tid; k < K; k += gridDim.x * gridDim.y * RED_THREADS)
     w1[k] = 1.0f + bf16_to_f32(Wnorm[(k / HS) * ld_wnorm + k % HS]);
   const int tile = blockIdx.y, n0 = blockIdx.x * RED_COLS;
-  // thread = (4 consecutive rows, 2 columns): rows 4 (tid % 32) .., columns
-  // n0 + tid / 32 and n0 + tid / 32 + 8; a warp reads 512 contiguous bytes
-  // per column and stream
+  // thread = (4 consecutive rows, RED_COLS / 8 columns): rows 4 (tid % 32) ..,
+  // columns n0 + tid / 32 + 8 j; a warp reads 512 contiguous bytes per column
+  // and stream
   const int r4 = (tid & 31) * 4, cw = tid >> 5;
   constexpr int NCOL = RED_COLS / 8;
   const int ns = HC * S;
@@ -470,12 +472,25 @@ __global__ void __launch_bounds__(RED_THREADS)
   float4 pv[NCOL][HC];
   // with one K chunk per stream (the usual case) every load issues before
   // any is used; otherwise chunk by chunk
+  if (S == 1) {
+#pragma unroll
+    for (int ss = 0; ss < HC; ++ss)
+      q[ss] = *reinterpret_cast<const float4*>(sumsq + (tb + ss) * BM + r4);
+#pragma unroll
+    for (int j = 0; j < NCOL; ++j) {
+      const int n = min(n0 + cw + 8 * j, np - 1);
+#pragma unroll
+      for (int ss = 0; ss < HC; ++ss)
+        pv[j][ss] = *reinterpret_cast<const float4*>(part + ((tb + ss) * np + n) * BM + r4);
+    }
+  } else {
 #pragma unroll
   for (int ss = 0; ss < HC; ++ss) q[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < NCOL; ++j)
 #pragma unroll
     for (int ss = 0; ss < HC; ++ss) pv[j][ss] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
   for (int c = 0; c < S; ++c) {
     float4 qc[HC], vc[NCOL][HC];
 #pragma unroll
@@ -499,6 +514,7 @@ __global__ void __launch_bounds__(RED_THREADS)
         pv[j][ss].x += vc[j][ss].x; pv[j][ss].y += vc[j][ss].y;
         pv[j][ss].z += vc[j][ss].z; pv[j][ss].w += vc[j][ss].w;
       }
+  }
   }
   float4 rs[HC];
 #pragma unroll
@@ -528,12 +544,12 @@ __global__ void __launch_bounds__(RED_THREADS)
     dstc[0] = acc.x; dstc[1] = acc.y; dstc[2] = acc.z; dstc[3] = acc.w;
   }
   __syncthreads();
-  // rows out: 16 consecutive columns of a row per 16 lanes
+  // rows out: RED_COLS consecutive columns of a row per RED_COLS lanes
   const float inv_hc = 1.0f / static_cast<float>(HC);
   const int cn = tid & (RED_COLS - 1), n = n0 + cn;
 #pragma unroll
   for (int j = 0; j < BM * RED_COLS / RED_THREADS; ++j) {
-    const int rw = (tid >> 4) + (RED_THREADS / RED_COLS) * j;
+    const int rw = tid / RED_COLS + (RED_THREADS / RED_COLS) * j;
     const int m = tile * BM + rw;
     if (m >= M || n >= np) continue;
     const float v = s_acc[cn][rw];
