@@ -63,6 +63,24 @@ def decode_traffic_per_launch():
     return sum(DECODE_TRAFFIC["bytes"][M] for M in SWEEP) / len(SWEEP)
 
 
+def max_over_ranks(value: float, world: int, device="cuda") -> float:
+    """The largest of one float over all ranks (the slowest rank's time); the
+    value itself on one rank."""
+    if world <= 1:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(units_per_step: float, steps: int, world: int, seconds: float) -> float:
+    """Whole-job units per second: every rank processes units_per_step per
+    step (replicas, weak scaling), timed by the slowest rank."""
+    return units_per_step * steps * world / seconds
+
+
 def roofline_us(nbytes: float, flops: float, hbm_gbs: float, tflops: float):
     """Roofline time of one call (µs) and its bound: the larger of the HBM
     time for the algorithmic bytes and the tensor time for the flops."""
@@ -283,12 +301,10 @@ def run_ours(args, rank, world):
     ms = e0.elapsed_time(e1)
     if world > 1:
         torch.distributed.barrier()
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world)
     op.check(stream)
     tokens_per_step = sum(SWEEP)
-    value = tokens_per_step * args.steps * world / (ms / 1e3)
+    value = job_throughput(tokens_per_step, args.steps, world, ms / 1e3)
 
     # e2e through the public API: each step copies all of its inputs in with
     # one host->device copy from a pinned staging buffer and all of its
@@ -365,10 +381,12 @@ def run_ours(args, rank, world):
         torch.cuda.synchronize()
 
     e2e_run(args.warmup)
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     e2e_run(args.steps)
-    e2e_s = time.perf_counter() - t0
-    e2e_value = tokens_per_step * args.steps * world / e2e_s
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e_value = job_throughput(tokens_per_step, args.steps, world, e2e_s)
 
     hbm, bf16_peak, peak_src = peaks()
     alg_bytes = sum(WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN for M in SWEEP)
