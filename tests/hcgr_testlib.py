@@ -101,6 +101,9 @@ def parity_report(got: dict, ref: dict, rows=None) -> dict:
         g = to_f64(got[k])[sel]
         o = ref[k]
         scale = np.maximum(np.abs(o), np.sqrt(np.mean(o * o, axis=1, keepdims=True)))
+        # an all-zero reference row (a zero token) leaves no scale: only an
+        # exact zero passes there
+        scale = np.maximum(scale, np.finfo(np.float64).tiny)
         rep[k] = float(np.max(np.abs(g - o) / (TOL_F32 * scale)))
     for k in got:
         if got[k] is not None and not np.all(np.isfinite(to_f64(got[k])[sel])):
