@@ -447,8 +447,8 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 constexpr int RED_THREADS = 256;
 constexpr int RED_COLS = 8;           // columns per block (a block covers a whole 128-row tile)
 
-template <int HC>
-__global__ void __launch_bounds__(RED_THREADS, HC <= 4 ? 4 : 2)
+template <int HC, int CB>
+__global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
     k1_reduce_kernel(const float* __restrict__ part, const float* __restrict__ sumsq,
                      float* __restrict__ rrms, float* __restrict__ lora,
                      float* __restrict__ inj_next, bf16_t* __restrict__ hh,
@@ -471,7 +471,10 @@ __global__ void __launch_bounds__(RED_THREADS, HC <= 4 ? 4 : 2)
   float4 q[HC];
   float4 pv[NCOL][HC];
   // with one K chunk per stream (the usual case) every load issues before
-  // any is used; otherwise chunk by chunk
+  // any is used; with K chunks, the chunks' loads issue CB at a time (their
+  // sums are still added in chunk order).  CB = 2 halves the chain of
+  // dependent loads a thread waits through, at half the resident blocks, so
+  // the host picks it only when the grid fits one wave either way.
   if (S == 1) {
 #pragma unroll
     for (int ss = 0; ss < HC; ++ss)
@@ -491,29 +494,38 @@ __global__ void __launch_bounds__(RED_THREADS, HC <= 4 ? 4 : 2)
 #pragma unroll
     for (int ss = 0; ss < HC; ++ss) pv[j][ss] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-  for (int c = 0; c < S; ++c) {
-    float4 qc[HC], vc[NCOL][HC];
+  for (int c0 = 0; c0 < S; c0 += CB) {
+    float4 qc[CB][HC], vc[CB][NCOL][HC];
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss)
-      qc[ss] = *reinterpret_cast<const float4*>(sumsq + (tb + ss * S + c) * BM + r4);
-#pragma unroll
-    for (int j = 0; j < NCOL; ++j) {
-      const int n = min(n0 + cw + 8 * j, np - 1);
+    for (int u = 0; u < CB; ++u) {
+      const int c = min(c0 + u, S - 1);
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss)
-        vc[j][ss] = *reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4);
-    }
+        qc[u][ss] = *reinterpret_cast<const float4*>(sumsq + (tb + ss * S + c) * BM + r4);
 #pragma unroll
-    for (int ss = 0; ss < HC; ++ss) {
-      q[ss].x += qc[ss].x; q[ss].y += qc[ss].y; q[ss].z += qc[ss].z; q[ss].w += qc[ss].w;
-    }
+      for (int j = 0; j < NCOL; ++j) {
+        const int n = min(n0 + cw + 8 * j, np - 1);
 #pragma unroll
-    for (int j = 0; j < NCOL; ++j)
-#pragma unroll
-      for (int ss = 0; ss < HC; ++ss) {
-        pv[j][ss].x += vc[j][ss].x; pv[j][ss].y += vc[j][ss].y;
-        pv[j][ss].z += vc[j][ss].z; pv[j][ss].w += vc[j][ss].w;
+        for (int ss = 0; ss < HC; ++ss)
+          vc[u][j][ss] = *reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4);
       }
+    }
+#pragma unroll
+    for (int u = 0; u < CB; ++u) {
+      if (c0 + u < S) {
+#pragma unroll
+        for (int ss = 0; ss < HC; ++ss) {
+          q[ss].x += qc[u][ss].x; q[ss].y += qc[u][ss].y; q[ss].z += qc[u][ss].z; q[ss].w += qc[u][ss].w;
+        }
+#pragma unroll
+        for (int j = 0; j < NCOL; ++j)
+#pragma unroll
+          for (int ss = 0; ss < HC; ++ss) {
+            pv[j][ss].x += vc[u][j][ss].x; pv[j][ss].y += vc[u][j][ss].y;
+            pv[j][ss].z += vc[u][j][ss].z; pv[j][ss].w += vc[u][j][ss].w;
+          }
+      }
+    }
   }
   }
   float4 rs[HC];
@@ -1014,9 +1026,11 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   // ---------------- reduce
   {
     const dim3 grid((np + RED_COLS - 1) / RED_COLS, n_mt);
+    const bool batch2 = S > 1 && static_cast<int64_t>(grid.x) * grid.y <= 2 * dev.sms;
 #define HCGR_RED(HCV)                                                                        \
   case HCV:                                                                                  \
-    k1_reduce_kernel<HCV><<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,     \
+    (batch2 ? k1_reduce_kernel<HCV, (HCV <= 4 ? 2 : 1)> : k1_reduce_kernel<HCV, 1>)          \
+        <<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,                      \
                                                           c.inj_next, h, c.Wnorm,            \
                                                           static_cast<int>(c.ld_wnorm), w1, M, S,  \
                                                           c.r, np, c.HS, 1.0f / c.HS, c.eps);\
