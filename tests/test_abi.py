@@ -96,3 +96,50 @@ def test_args_struct_offsets_match_c(root, tmp_path):
                                            check=True).stdout.split()]
     assert vals[0] == ctypes.sizeof(_native.Args)
     assert vals[1:] == [getattr(_native.Args, n).offset for n in names]
+
+
+C_CONSUMER = r"""
+#include <stdio.h>
+#include <string.h>
+#include "hc_gr.h"
+
+/* A plain C caller: every rejection below happens in the argument checks,
+   before any CUDA call, so this runs without a GPU. */
+int main(void) {
+  int fails = 0;
+  hc_gr_handle h = NULL;
+  hc_gr_args a;
+  memset(&a, 0, sizeof(a));
+#define EXPECT(call, want) do { int st_ = (call); if (st_ != (want)) { \
+    printf("%s -> %d (want %d)\n", #call, st_, (want)); ++fails; } } while (0)
+  EXPECT(hc_gr_create(NULL, 0, 8, 4, 2560, 320), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_create(&h, 0, 0, 4, 2560, 320), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_forward_ex(NULL, &a, NULL), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_forward(NULL, 4, 4, 2560, 320, 1e-6f, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                       NULL, NULL, NULL, NULL, NULL, NULL), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_combine(NULL, 4, 4, 2560, NULL, NULL, NULL, 0, NULL, NULL), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_mix(NULL, 4, 4, 2560, 320, 1e-6f, NULL, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                   NULL, NULL), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_check(NULL, NULL), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_destroy(NULL), HC_GR_OK);
+  if (strcmp(hc_gr_strerror(HC_GR_OK), "ok") != 0) { printf("strerror\n"); ++fails; }
+  printf("%s\n", fails ? "FAIL" : "PASS");
+  return fails != 0;
+}
+"""
+
+
+def test_plain_c_caller_links_and_gets_rejections(root, lib, tmp_path):
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CONSUMER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(_native.LIB_PATH)
+    subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(root, "include"), str(src),
+                    "-L", libdir, "-lhc_gr", "-Wl,-rpath," + libdir, "-o", str(exe)], check=True)
+    res = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert res.returncode == 0 and res.stdout.strip().endswith("PASS"), res.stdout + res.stderr
