@@ -157,6 +157,73 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------- CPU baseline
+_ORACLE_CASE = None
+
+
+def _oracle_worker_init():
+    """Pool worker set-up: the weights and the sweep's 32 token rows, once."""
+    global _ORACLE_CASE
+    from hyper_connection_gated_gb300 import inputs
+
+    w = {k: inputs.bf16_bits_to_f64(v) for k, v in inputs.weights().items()}
+    a = inputs.activations(32)
+    _ORACLE_CASE = (w, inputs.bf16_bits_to_f64(a["R"]), inputs.bf16_bits_to_f64(a["y"]),
+                    a["inj"].astype("f8"))
+
+
+def _oracle_sweep(_: int) -> int:
+    """One task of the all-cores baseline: one whole sweep (the five calls)
+    through the oracle, as the single-core baseline runs it; returns tokens."""
+    import oracle
+
+    w, R, y, inj = _ORACLE_CASE
+    for M in SWEEP:
+        oracle.forward(R=R[:M], y=y[:M], inj=inj[:M], Wnorm=w["Wnorm"], Wd=w["Wd"], Wi=w["Wi"],
+                       Wu=w["Wu"], eps=1e-6)
+    return sum(SWEEP)
+
+
+def _oracle_pool_run(seconds: float, cores: int) -> dict:
+    """Sweeps over a spawn-started pool of `cores` single-threaded workers
+    (one sweep per worker per round) until `seconds` have passed."""
+    import multiprocessing
+
+    ctx = multiprocessing.get_context("spawn")
+    with ctx.Pool(cores, initializer=_oracle_worker_init) as pool:
+        pool.map(_oracle_sweep, range(cores), chunksize=1)          # warm-up round
+        t0, n, tok = time.perf_counter(), 0, 0
+        while True:
+            tok += sum(pool.map(_oracle_sweep, range(cores), chunksize=1))
+            n += cores
+            el = time.perf_counter() - t0
+            if el >= seconds:
+                break
+    return {"tokens": tok, "seconds": el, "sweeps": n}
+
+
+def cpu_baseline_all_cores(seconds: float = 10.0) -> dict:
+    """The same oracle over every host core: independent sweeps, one per
+    pool worker (one BLAS thread each) at a time, in a child process with no
+    CUDA.  (One token per task reads the whole weight set for a single row
+    and measured slower than one core running the batched calls.)"""
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    code = (f"import sys, json; sys.path.insert(0, {ROOT!r}); import bench; "
+            f"print(json.dumps(bench._oracle_pool_run({seconds!r}, {cores!r})))")
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    res = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env,
+                         timeout=600, cwd=ROOT)
+    if res.returncode != 0:
+        return {"value": None, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                "error": res.stderr[-500:]}
+    d = json.loads(res.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens"] / d["seconds"], "unit": "tokens/s", "cores": cores,
+            "kind": "oracle",
+            "sample": f"{d['sweeps']} sweeps of M={list(SWEEP)} ({d['tokens']} tokens), one sweep "
+                      f"per task over {cores} spawn-started workers, fp64 numpy, 1 BLAS thread "
+                      f"each, {d['seconds']:.1f} s"}
+
+
 def cpu_baseline(seconds: float = 12.0, max_steps: int | None = None, warmup: int = 0) -> dict:
     """The fp64 oracle, single-threaded BLAS, on the sweep's token mix.
 
@@ -769,6 +836,7 @@ def main():
         line["entry_points_us"] = entry_sweep()
     if rank == 0:
         line["cpu_baseline"] = None if args.no_cpu_baseline else cpu_baseline()
+        line["cpu_baseline_all_cores"] = None if args.no_cpu_baseline else cpu_baseline_all_cores()
         print(json.dumps(line))
     if world > 1:
         import torch

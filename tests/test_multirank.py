@@ -81,3 +81,14 @@ def test_reference_arm_runs_on_rank_zero_only(rank):
     assert line["impl"] == "reference" and line["value"] > 0
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+
+
+def test_all_cores_oracle_baseline_runs():
+    # the spawn-started pool runs whole sweeps on every core, without CUDA
+    sys.path.insert(0, ROOT)
+    import bench
+
+    res = bench.cpu_baseline_all_cores(seconds=1.0)
+    assert res.get("error") is None, res
+    assert res["kind"] == "oracle" and res["value"] > 0 and res["cores"] >= 1
+    assert "one sweep per task" in res["sample"]
