@@ -39,6 +39,10 @@
 // alternates between two copies by call parity (a ticket counter), and each
 // call empties the copy the next call will use.
 //
+// Without y (the mix alone) steps 1 and 4 take R as R2 and nothing is stored
+// for it; the Wnorm slice of stream s starts at s * ld_wnorm (0 when one [HS]
+// norm weight is shared by the streams).
+//
 // Weights move as TMA boxes issued at kernel start; when they do not all fit
 // in shared memory they stream through rings whose slots the MMA thread hands
 // back with tcgen05.commit.  With a programmatic dependent launch the weight

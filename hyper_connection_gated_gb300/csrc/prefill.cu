@@ -11,31 +11,38 @@
 //   rrms_s is constant over stream s, lora = sum_s rrms_s * (R2_s . W_s^T):
 //   the products are accumulated per stream without rrms and scaled later.
 //   Warp roles:
-//     warp 8      TMA producer: R and y tiles (128 x 64, 128-byte swizzle),
-//                 the matching 64 columns of the r Wd rows and of the inject
-//                 rows, and the K block's Wnorm values;
+//     warp 8      TMA: R and y tiles (128 x 64, 128-byte swizzle) and the K
+//                 block's Wnorm values into the R/y ring;
+//     warp 10     TMA: the matching 64 columns of the Wd rows and of the
+//                 inject rows, in one or two column blocks, into the weight
+//                 ring;
 //     warps 0-7   converters: R2 = bf16(R + y * iw) (written to HBM), the sum
 //                 of R2^2 per row, and the MMA operand in place: R2 for a
 //                 folded weight, else the hi/lo bf16 split of R2 * (1 + Wnorm)
 //                 (two MMAs, so the product keeps ~16 mantissa bits);
-//     warp 9      one thread issues tcgen05.mma (M=128, N = r + 16: the Wd
-//                 rows and the inject rows, in <= 256-column blocks).
+//     warps 9, 11 tcgen05.mma, one column block each (M=128, N = r + 16: the
+//                 Wd rows and the inject rows, in <= 256-column blocks), one
+//                 elected lane issuing; warp 9 also owns the TMEM allocation.
 //   When r + 16 exceeds the 512 tensor-memory columns the inject dot
 //   products run on the converters' CUDA cores instead.  The epilogue writes
-//   the partial sums of squares and the un-scaled partial products.
+//   the partial sums of squares and the un-scaled partial products.  Without
+//   y (the mix alone) the converters take R as R2 and store nothing for it;
+//   the Wnorm slice of stream s starts at s * ld_wnorm (0 for one [HS] norm
+//   weight shared by the streams).
 // R  (reduce): rrms_s from the partial sums of squares, lora / inj_next =
 //   sum_s rrms_s * (sum of the stream's partial products), and the up-GEMM
 //   operand hh = bf16(SiLU(lora / HC) / 2).  With few token tiles K1 splits
 //   each stream's K range into chunks so that the CTAs cover the SMs.  The
-//   partials are laid out [token][stream, chunk][column], so a row's reduce
-//   reads one contiguous run.
+//   partials are laid out [tile][stream, chunk][column][128 rows]: column-major
+//   inside a token tile, so K1's epilogue (a thread per row) stores whole
+//   128-byte lines and the reduce reads them as float4 runs.
 // K2, persistent over (128-token tile, NCU-channel block) units with
 //   N = HC * NCU = 256 for HC = 4 and 8: A = hh tile, B = the HC * NCU rows
 //   {s * HS + c} of Wu, D = 128 x N fp32 (G / 2) in double-buffered tensor
 //   memory.  The unit's R2 tile and 1 + Wnorm stream through a ring of
 //   per-stream slots; epilogue warps read a row's gates stream by stream,
 //   apply sigmoid, rebuild xn from R2, rrms and 1 + Wnorm and store
-//   x = (1/HC) * sum_s G * xn.
+//   x = (1/HC) * sum_s G * xn.  For the mix alone, R itself is the R2 tile.
 #include <cstring>
 #include <algorithm>
 #include <type_traits>
