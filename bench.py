@@ -51,18 +51,22 @@ DECODE_TRAFFIC = {
 }
 
 
+def code_only(text: str) -> str:
+    """C/C++/CUDA source without comments, trailing blanks and blank lines."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip())
+
+
 def decode_sources_sha256() -> str:
     """Hash of the decode kernel's code: its sources with comments and blank
     lines removed, so that an edit of the prose alone keeps the capture."""
     import hashlib
-    import re
     h = hashlib.sha256()
     for name in DECODE_SOURCES:
         with open(os.path.join(ROOT, "hyper_connection_gated_gb300", "csrc", name)) as f:
-            text = f.read()
-        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-        text = re.sub(r"//[^\n]*", "", text)
-        h.update("\n".join(ln.rstrip() for ln in text.splitlines() if ln.strip()).encode())
+            h.update(code_only(f.read()).encode())
     return h.hexdigest()
 
 
