@@ -825,13 +825,10 @@ cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
       !make_tmap_bf16(&prm.tm_wi, c.Wi, 3, dwi, wstr, bwi, SW) ||
       !make_tmap_bf16(&prm.tm_wu, c.Wu, 3, dwu, swu, bwu, SW))
     return cudaErrorNotSupported;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         SMEM_ALLOC);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  static std::atomic<unsigned long long> attr_done{0};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(decode_kernel), SMEM_ALLOC, dev.id,
+                                  attr_done);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(g.G);
   cfg.blockDim = dim3(NT);

@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/hc_gr.h"
 
 namespace hcgr {
@@ -61,6 +63,19 @@ struct Device {
   int smem_optin = 0;
   int l2_bytes = 0;
 };
+
+// Raises a kernel's dynamic shared-memory limit on `device` (the current
+// device).  The attribute belongs to the device, so it is set once per device:
+// `done` holds one bit per device id below 64 (higher ids set it on every
+// call).  Concurrent first calls may both set it, which is harmless.
+inline cudaError_t smem_limit_once(const void* func, int bytes, int device,
+                                   std::atomic<unsigned long long>& done) {
+  const unsigned long long bit = device >= 0 && device < 64 ? 1ull << device : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
 
 // Decode path (M <= DECODE_MAX_M): one persistent kernel.
 constexpr int DECODE_MAX_M = 32;

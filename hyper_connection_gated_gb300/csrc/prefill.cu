@@ -855,13 +855,10 @@ uint32_t pow2_cols(int n) {
 template <int HCT, bool INJ_MMA>
 cudaError_t launch_k1(const K1Params& p, int grid, size_t smem, const Device& dev,
                       cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k1_kernel<HCT, INJ_MMA>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k1_kernel<HCT, INJ_MMA>),
+                                  dev.smem_optin, dev.id, attr);
+  if (e != cudaSuccess) return e;
   k1_kernel<HCT, INJ_MMA><<<grid, K1_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
 }
@@ -869,13 +866,10 @@ cudaError_t launch_k1(const K1Params& p, int grid, size_t smem, const Device& de
 template <int HCT>
 cudaError_t launch_k2(const K2Params& p, int grid, size_t smem, const Device& dev,
                       cudaStream_t stream) {
-  static bool attr = false;
-  if (!attr) {
-    cudaError_t e = cudaFuncSetAttribute(k2_kernel<HCT>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, dev.smem_optin);
-    if (e != cudaSuccess) return e;
-    attr = true;
-  }
+  static std::atomic<unsigned long long> attr{0};
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k2_kernel<HCT>), dev.smem_optin,
+                                  dev.id, attr);
+  if (e != cudaSuccess) return e;
   k2_kernel<HCT><<<grid, K2_THREADS, smem, stream>>>(p);
   return cudaGetLastError();
 }

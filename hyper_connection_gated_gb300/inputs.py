@@ -131,28 +131,41 @@ def weights(shape: Shape = DEFAULT, seed: int = SEED) -> dict:
     return {k: to_bf16_bits(v) for k, v in out.items()}
 
 
-def activations(M: int, shape: Shape = DEFAULT, seed: int = SEED,
-                distinct_rows: int | None = None) -> dict:
-    """R [M, HC, HS] bf16, y [M, HS] bf16, inj [M, HC] float32.
+def activation_rows(start: int, stop: int, shape: Shape = DEFAULT, seed: int = SEED) -> dict:
+    """Rows start .. stop-1 of R [., HC, HS] bf16, y [., HS] bf16 and inj [., HC]
+    float32 -- exactly the rows ``activations`` gives for any M >= stop.
 
     R, y ~ N(0, 1) (wide workload: R ~ Student-t(3), y ~ 10 N(0, 1)) and
-    inj ~ N(0, 2) (std 2).  With ``distinct_rows`` set, row m holds the
-    generator's row ``m % distinct_rows`` so very large M stays cheap to
-    build; every row is still a row of the same seeded distribution.
+    inj ~ N(0, 2) (std 2).  Row m of a tensor reads counter positions
+    m * row_length onwards of that tensor's stream, so any row range can be
+    drawn on its own (for instance by several processes in parallel).
     """
     HC, HS, K = shape.HC, shape.HS, shape.K
-    G = M if distinct_rows is None else min(M, distinct_rows)
+    n = stop - start
     if shape.heavy_tailed:
-        R = student_t3(seed, _ID["R"], 0, G * K)
-        y = 10.0 * normals(seed, _ID["y"], 0, G * HS)
+        R = student_t3(seed, _ID["R"], start * K, n * K)
+        y = 10.0 * normals(seed, _ID["y"], start * HS, n * HS)
     else:
-        R = normals(seed, _ID["R"], 0, G * K)
-        y = normals(seed, _ID["y"], 0, G * HS)
-    inj = 2.0 * normals(seed, _ID["inj"], 0, G * HC)
-    R = to_bf16_bits(R).reshape(G, HC, HS)
-    y = to_bf16_bits(y).reshape(G, HS)
-    inj = inj.astype(np.float32).reshape(G, HC)
+        R = normals(seed, _ID["R"], start * K, n * K)
+        y = normals(seed, _ID["y"], start * HS, n * HS)
+    inj = 2.0 * normals(seed, _ID["inj"], start * HC, n * HC)
+    return {"R": to_bf16_bits(R).reshape(n, HC, HS), "y": to_bf16_bits(y).reshape(n, HS),
+            "inj": inj.astype(np.float32).reshape(n, HC)}
+
+
+def activations(M: int, shape: Shape = DEFAULT, seed: int = SEED,
+                distinct_rows: int | None = None) -> dict:
+    """R [M, HC, HS] bf16, y [M, HS] bf16, inj [M, HC] float32 (rows 0 .. M-1
+    of ``activation_rows``).
+
+    With ``distinct_rows`` set, row m holds the generator's row
+    ``m % distinct_rows``: the benchmark uses it to build very large inputs
+    quickly (timing does not depend on the values); parity tests draw every
+    row.
+    """
+    G = M if distinct_rows is None else min(M, distinct_rows)
+    a = activation_rows(0, G, shape, seed)
     if G < M:
         idx = np.arange(M) % G
-        R, y, inj = R[idx], y[idx], inj[idx]
-    return {"R": R, "y": y, "inj": inj}
+        a = {k: v[idx] for k, v in a.items()}
+    return a

@@ -88,12 +88,19 @@ def test_combine_special_values(torch_cuda):
     np.testing.assert_array_equal(tl.to_f64(b), r)
 
 
-def test_combine_full_size_sampled(torch_cuda):
+@pytest.fixture(scope="module")
+def pool():
+    with tl.oracle_pool() as p:
+        yield p
+
+
+def test_combine_full_size_every_row(torch_cuda, pool):
     # the 65536-token workload: bit-identical to the fused prefill R2 on every
-    # element, and within tolerance of the oracle on sampled rows
+    # element, and within tolerance of the oracle on every row
     torch = torch_cuda
-    M = 65536
-    case = tl.make_case(M, inputs.DEFAULT, seed=24, distinct_rows=512)
+    M, seed = 65536, 24
+    case = {"shape": inputs.DEFAULT, "M": M, **inputs.weights(inputs.DEFAULT, seed),
+            **tl.pooled_activations(pool, M, inputs.DEFAULT, seed)}
     d = tl.device_case(case)
     with HcGatedResidual(max_M=M) as op:
         R2 = op.combine(d["R"], d["y"], d["inj"])
@@ -101,12 +108,9 @@ def test_combine_full_size_sampled(torch_cuda):
                            check=True, want_lora=False)
         torch.cuda.synchronize()
         assert torch.equal(R2.view(torch.int16), fused["R2"].view(torch.int16))
-    rows = np.array([0, 1, 511, 512, 4097, 33333, M - 1])
-    ref, _ = tl.oracle.combine(inputs.bf16_bits_to_f64(case["R"][rows]),
-                               inputs.bf16_bits_to_f64(case["y"][rows]),
-                               case["inj"][rows].astype(np.float64))
-    g = tl.to_f64(R2)[rows]
-    assert np.max(np.abs(g - ref) / (tl.TOL_BF16 * (1.0 + np.abs(ref)))) <= 1.0
+    del fused
+    tl.assert_pooled_parity(pool, tl.host_outputs({"R2": R2}), M, shape=inputs.DEFAULT, seed=seed,
+                            kind="combine", label="combine M=65536")
 
 
 def test_combine_rejects(torch_cuda):
@@ -186,18 +190,17 @@ def test_mix_wide_shape(torch_cuda):
     tl.assert_parity(out, tl.oracle_mix_ref(case), label="mix wide decode")
 
 
-def test_mix_full_size_sampled(torch_cuda):
+def test_mix_full_size_every_row(torch_cuda, pool):
     torch = torch_cuda
-    M = 65536
-    case = tl.make_case(M, inputs.DEFAULT, seed=31, distinct_rows=512)
+    M, seed = 65536, 31
+    case = {"shape": inputs.DEFAULT, "M": M, **inputs.weights(inputs.DEFAULT, seed),
+            **tl.pooled_activations(pool, M, inputs.DEFAULT, seed)}
     d = tl.device_case(case)
     with HcGatedResidual(max_M=M) as op:
         out = op.mix(d["R"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"], check=True)
         torch.cuda.synchronize()
-    rows = np.array([0, 3, 127, 128, 9999, 40000, M - 1])
-    idx = torch.as_tensor(rows, device="cuda")
-    got = {k: v.index_select(0, idx) for k, v in out.items()}
-    tl.assert_parity(got, tl.oracle_mix_ref(case, rows=rows), label="mix M=65536 sampled")
+    tl.assert_pooled_parity(pool, tl.host_outputs(out), M, shape=inputs.DEFAULT, seed=seed,
+                            kind="mix", label="mix M=65536")
 
 
 def test_mix_rejects_partial_null(torch_cuda):

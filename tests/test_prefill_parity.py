@@ -2,9 +2,10 @@
 
 Covers ragged token counts around the 128-row tile, the mid-batch workload
 (M in {512, 1024, 2048} with the merged 336-row weight, folded and unfolded),
-the large-M workload (M up to 65536, checked on sampled rows), the wide
-variant (HC=8, HS=4096, r=512), agreement with the decode path, and
-determinism.
+the large-M workload (M up to 65536) and the wide variant (HC=8, HS=4096,
+r=512) -- both with every token row drawn from the seed and every row checked
+against the oracle in a pool of worker processes --, agreement with the
+decode path, and determinism.
 """
 import numpy as np
 import pytest
@@ -69,27 +70,29 @@ def test_prefill_separate_weights(torch_cuda, case2k, M):
     tl.assert_parity(_run(case, M), tl.oracle_ref(case), label=f"prefill M={M}")
 
 
-def _sample_rows(M, n=48, seed=0):
-    rng = np.random.default_rng(seed)
-    rows = set(rng.choice(M, size=min(n, M), replace=False).tolist())
-    rows |= {0, 1, 127, 128, M - 129, M - 1}
-    return sorted(r for r in rows if 0 <= r < M)
+@pytest.fixture(scope="module")
+def pool():
+    with tl.oracle_pool() as p:
+        yield p
+
+
+def _full_case(pool, M, shape, seed=inputs.SEED):
+    acts = tl.pooled_activations(pool, M, shape, seed)
+    return {"shape": shape, "M": M, **inputs.weights(shape, seed), **acts}
 
 
 @pytest.mark.parametrize("M", [4096, 8192, 16384, 32768, 65536])
-def test_prefill_large_M_sampled_rows(torch_cuda, M):
-    case = tl.make_case(M, distinct_rows=4096)
-    rows = _sample_rows(M)
-    out = _run(case, M, rows=rows)
-    tl.assert_parity(out, tl.oracle_ref(case, rows=rows), label=f"prefill M={M}")
+def test_prefill_large_M_every_row(torch_cuda, pool, M):
+    case = _full_case(pool, M, inputs.DEFAULT)
+    out = tl.host_outputs(_run(case, M))
+    tl.assert_pooled_parity(pool, out, M, shape=inputs.DEFAULT, label=f"prefill M={M}")
 
 
 @pytest.mark.parametrize("M", [64, 1024, 8192])
-def test_prefill_wide_variant(torch_cuda, M):
-    case = tl.make_case(M, inputs.WIDE, distinct_rows=2048)
-    rows = _sample_rows(M, n=24)
-    out = _run(case, M, shape=inputs.WIDE, rows=rows)
-    tl.assert_parity(out, tl.oracle_ref(case, rows=rows), label=f"wide prefill M={M}")
+def test_prefill_wide_variant_every_row(torch_cuda, pool, M):
+    case = _full_case(pool, M, inputs.WIDE)
+    out = tl.host_outputs(_run(case, M, shape=inputs.WIDE))
+    tl.assert_pooled_parity(pool, out, M, shape=inputs.WIDE, label=f"wide prefill M={M}")
 
 
 def test_prefill_agrees_with_decode(torch_cuda, case2k):
