@@ -802,6 +802,95 @@ def entry_sweep(reps: int = 5):
     return res
 
 
+TRACE_PHASES = {0: "start", 1: "prologue done", 2: "previous kernel done", 3: "COMBINE done",
+                4: "issuer 0: boxes landed, MMAs issued", 5: "down MMAs complete",
+                6: "pieces written", 7: "first block gathered", 8: "blocks reduced, h published",
+                9: "h gathered", 10: "gate MMAs complete", 11: "x stored", 12: "end"}
+DOWN_PHASES = (0, 1, 2, 3, 4, 5, 6, 12)
+UP_PHASES = (0, 1, 2, 7, 8, 9, 10, 11, 12)
+
+
+def decode_trace(args):
+    """Phase timeline of the decode kernel, from the library's HCGR_TRACE twin
+    (libhc_gr_trace.so, built here if missing).  Per M: `--calls` traced calls
+    after 5 warm-up calls, each on one of several weight+input sets whose
+    total exceeds twice the L2 (so the weights come from HBM); plain launches,
+    or with --trace-pdl each traced call chained after a previous decode call
+    by programmatic dependent launch.  Prints, per phase and role, the
+    min / median / max over CTAs of the time since the grid's first CTA
+    started (µs), each the median over the traced calls."""
+    import ctypes
+
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import _native, build
+
+    if not os.path.exists(build.LIB_TRACE):
+        build.build(trace=True)
+    lib = _native.load(build.LIB_TRACE)
+    lib.hc_gr_trace_read.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    lib.hc_gr_trace_read.restype = ctypes.c_int
+    _native._LIB = lib
+    from hyper_connection_gated_gb300 import PATH_DECODE, HcGatedResidual, inputs
+
+    shape = inputs.WIDE if args.wide else inputs.DEFAULT
+    dev = torch.cuda.current_device()
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+    wbytes = 2 * (shape.r + shape.HC) * shape.K + 2 * shape.K * shape.r
+    nsets = max(3, int(np.ceil(2.0 * l2 / wbytes)) + 1)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = {k: bf(v) for k, v in inputs.weights(shape).items()}
+    a = inputs.activations(32, shape)
+    base = dict(w, R=bf(a["R"]), y=bf(a["y"]), inj=torch.from_numpy(a["inj"]).cuda())
+    sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
+    n = 256 * 16
+    buf = np.zeros(n, dtype=np.uint64)
+    report = {}
+    with HcGatedResidual(max_M=32, HC=shape.HC, HS=shape.HS, r=shape.r) as op:
+        for M in [int(v) for v in args.trace_M.split(",")]:
+            runs = []
+            for rep in range(5 + args.calls):
+                if args.trace_pdl:
+                    s0 = sets[(rep + 1) % nsets]
+                    op.forward(s0["R"][:M], s0["y"][:M], s0["inj"][:M], s0["Wnorm"], s0["Wu"],
+                               Wd=s0["Wd"], Wi=s0["Wi"], force_path=PATH_DECODE)
+                s1 = sets[rep % nsets]
+                op.forward(s1["R"][:M], s1["y"][:M], s1["inj"][:M], s1["Wnorm"], s1["Wu"],
+                           Wd=s1["Wd"], Wi=s1["Wi"], force_path=PATH_DECODE, pdl=args.trace_pdl)
+                op.check()
+                assert lib.hc_gr_trace_read(buf.ctypes.data, n) == 0
+                if rep >= 5:
+                    runs.append(buf.reshape(256, 16).astype(np.int64).copy())
+            table = {}
+            for role, phases, sel in (("down", DOWN_PHASES, 6), ("up", UP_PHASES, 11)):
+                per_run = []
+                for st in runs:
+                    live = st[st[:, 0] > 0]
+                    t0 = live[:, 0].min()
+                    rows = live[live[:, sel] > 0]
+                    per_run.append({ph: ((rows[:, ph] - t0) / 1e3) for ph in phases})
+                table[role] = {
+                    TRACE_PHASES[ph]: [round(float(np.median([np.min(r[ph]) for r in per_run])), 2),
+                                       round(float(np.median([np.median(r[ph]) for r in per_run])), 2),
+                                       round(float(np.median([np.max(r[ph]) for r in per_run])), 2)]
+                    for ph in phases}
+                table[role + "_ctas"] = int(len(runs[-1][(runs[-1][:, 0] > 0) & (runs[-1][:, sel] > 0)]))
+            report[str(M)] = table
+            print(f"M={M} ({'chained by programmatic dependent launch' if args.trace_pdl else 'plain launch'}, "
+                  f"weights from HBM): µs since the first CTA started, min / median / max over CTAs, "
+                  f"median of {args.calls} calls")
+            for role in ("down", "up"):
+                print(f"  {role} CTAs ({table[role + '_ctas']}):")
+                for name, v in table[role].items():
+                    print(f"    {name:40s} {v[0]:7.2f} {v[1]:7.2f} {v[2]:7.2f}")
+    print(json.dumps({"decode_trace": report, "shape": [shape.HC, shape.HS, shape.r],
+                      "pdl": bool(args.trace_pdl)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--case", choices=["auto", "decode", "prefill", "combine", "mix"], default=None,
@@ -816,11 +905,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-prefill-sweep", action="store_true",
                     help="skip the per-M table of the prefill path")
+    ap.add_argument("--trace", action="store_true",
+                    help="phase timeline of the decode kernel (diagnostic build)")
+    ap.add_argument("--trace-M", default="1,8,32")
+    ap.add_argument("--trace-pdl", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if args.case is not None:
         run_case(args)
+        return
+    if args.trace:
+        decode_trace(args)
         return
 
     if args.impl == "reference":

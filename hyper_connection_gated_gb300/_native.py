@@ -17,7 +17,10 @@ PATH_AUTO, PATH_DECODE, PATH_PREFILL = range(3)
 
 EXPORTS = ("hc_gr_create", "hc_gr_forward", "hc_gr_forward_ex", "hc_gr_check",
            "hc_gr_destroy", "hc_gr_strerror", "hc_gr_last_cuda_error", "hc_gr_forward_noalloc",
-           "hc_gr_combine", "hc_gr_mix")
+           "hc_gr_combine", "hc_gr_mix", "hc_gr_noalloc_check")
+
+MAX_TOKENS = 1 << 30   # HC_GR_MAX_TOKENS: largest M and max_M
+MAX_WIDTH = 1 << 30    # HC_GR_MAX_WIDTH: largest K = HC * HS
 
 _vp = ctypes.c_void_p
 _fp = ctypes.c_void_p   # float* passed as an address
@@ -71,6 +74,8 @@ def load(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.hc_gr_forward_noalloc.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           ctypes.c_float] + [_vp] * 12 + [_vp]
     lib.hc_gr_forward_noalloc.restype = ctypes.c_int
+    lib.hc_gr_noalloc_check.argtypes = [_vp]
+    lib.hc_gr_noalloc_check.restype = ctypes.c_int
     lib.hc_gr_combine.argtypes = [_vp, ctypes.c_int64, ctypes.c_int, ctypes.c_int, _vp, _vp, _vp,
                                   ctypes.c_int64, _vp, _vp]
     lib.hc_gr_combine.restype = ctypes.c_int

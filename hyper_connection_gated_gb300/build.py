@@ -3,6 +3,10 @@
 Each .cu file under csrc/ is compiled to an object in parallel, then the
 objects are linked into one shared library next to this file.  Nothing is
 installed; the library is loaded from the package directory.
+
+build(trace=True) builds the diagnostic twin libhc_gr_trace.so from the same
+sources with HCGR_TRACE defined: the decode kernel then records a phase
+timeline (include/hc_gr_trace.h).  The product library never has it.
 """
 from __future__ import annotations
 
@@ -17,6 +21,8 @@ CSRC = os.path.join(PKG, "csrc")
 ROOT = os.path.dirname(PKG)
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libhc_gr.so")
+BUILD_TRACE = os.path.join(PKG, "_build_trace")
+LIB_TRACE = os.path.join(PKG, "libhc_gr_trace.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -38,8 +44,8 @@ def sources() -> list[str]:
     return sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".cu"))
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], out_dir: str = BUILD) -> str:
+    obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
@@ -49,21 +55,25 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False) -> str:
-    """Compile every csrc/*.cu for sm_103a and link libhc_gr.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(verbose_ptxas: bool = False, trace: bool = False) -> str:
+    """Compile every csrc/*.cu for sm_103a and link libhc_gr.so (with trace:
+    the phase-timeline twin libhc_gr_trace.so); returns its path."""
+    out_dir, lib = (BUILD_TRACE, LIB_TRACE) if trace else (BUILD, LIB)
+    os.makedirs(out_dir, exist_ok=True)
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
+    if trace:
+        extra = extra + ["-DHCGR_TRACE"]
     srcs = sources()
     with concurrent.futures.ThreadPoolExecutor(max_workers=len(srcs)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, out_dir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(verbose_ptxas="-v" in sys.argv))
+    print(build(verbose_ptxas="-v" in sys.argv, trace="--trace" in sys.argv))

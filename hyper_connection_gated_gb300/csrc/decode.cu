@@ -3,8 +3,12 @@
 // (aiter PR #5913, "Technical Details"; the page's skinny decode with split-K
 // partials and a last-stage reduce is the prior art).
 //
-// Grid: G CTAs; CTA b owns the channel slice [c0, c0 + 64 nkc) of stream
-// s = b / P (P slices per stream; the stream end clips the last one).
+// The grid has two roles, so that the whole weight set streams from HBM on
+// every SM at once: Gd "down" CTAs hold the down/inject weight (Wd and Wi, or
+// the merged Wdi), Gu "up" CTAs hold the up weight Wu.
+//
+// Down CTA b owns the channel slice [c0, c0 + 64 nkc) of stream s = b / P
+// (P slices per stream; the stream end clips the last one):
 //   1. COMBINE on the slice: R2 = bf16(R + y * iw) (stored), the partial sum
 //      of R2^2 per token, and the MMA operand a = R2 * (1 + Wnorm) split into
 //      two bf16 terms (hi + lo, ~16 mantissa bits), or a = R2 for a folded
@@ -14,22 +18,22 @@
 //      every 128-row tile of the down/inject weight (TMA, 128-byte swizzle):
 //      D[n][m] = sum_{c in slice} W[n, s HS + c] a[m, c].  The hi and lo
 //      terms are stacked as the two halves of the MMA's N dimension (one MMA
-//      per weight tile and k-step), and one thread per row tile issues (the
-//      issues run side by side; each costs ~100 cycles).
+//      per weight tile and k-step), and one thread per row tile issues.
 //      rrms_s is constant over stream s, so lora = sum_s rrms_s sum_{b in s}
 //      D_b is exact: the per-stream factor commutes out of the K-sum.
-//   3. Reduce-scatter: the M (r + HC) outputs are cut into blocks of Qn
-//      outputs of one token.  Every CTA writes its piece of every block, plus
-//      its sum of squares, to a global exchange buffer straight from TMEM; the
-//      block's reducer (CTA j mod G) sums the pieces in a fixed order
-//      (deterministic) and forms rrms, lora, inj_next and
-//      h = bf16(SiLU(lora / HC)).
-//   4. All-gather: the reducers publish h and rrms to a second exchange
-//      buffer; every CTA reads all of it into the swizzled operand layout,
-//      forms the gates G[s, c] = sigmoid(Wu[s HS + c] . h) for its channel
-//      range and every stream on the tensor cores, rebuilds xn from R2
-//      (recomputed from R, y and inj bit-identically to step 1), rrms and
-//      Wnorm, and stores x = (1 / HC) sum_s G * xn.
+//   3. Its piece of every reduce-scatter block (below) goes to a global
+//      exchange buffer straight from TMEM; then the down CTA is done.
+// Up CTA u owns the channel range [cp0, cp0 + nc) of every stream:
+//   4. Reduce-scatter: the M (r + HC) outputs are cut into blocks of Qn
+//      outputs of one token; up CTA j mod Gu reduces block j over the Gd
+//      pieces in a fixed order (deterministic) and forms rrms, lora,
+//      inj_next and h = bf16(SiLU(lora / HC)).
+//   5. All-gather: the reducers publish h and rrms to a second exchange
+//      buffer; every up CTA reads all of it into the swizzled operand layout,
+//      forms the gates G[s, c] = sigmoid(Wu[s HS + c] . h) of its channel
+//      range on the tensor cores (its Wu rows landed meanwhile), rebuilds xn
+//      from R2 (recomputed from R, y and inj bit-identically to step 1), rrms
+//      and Wnorm, and stores x = (1 / HC) sum_s G * xn.
 // The exchanges need no grid barrier.  Every 32-bit word of an exchange
 // buffer is either the empty marker 0xffffffff or a value, and a reader spins
 // (bounded in time) on each word until it holds a value.  A value never equals
@@ -39,16 +43,23 @@
 // alternates between two copies by call parity (a ticket counter), and each
 // call empties the copy the next call will use.
 //
-// Without y (the mix alone) steps 1 and 4 take R as R2 and nothing is stored
+// Without y (the mix alone) steps 1 and 5 take R as R2 and nothing is stored
 // for it; the Wnorm slice of stream s starts at s * ld_wnorm (0 when one [HS]
 // norm weight is shared by the streams).
 //
-// Weights move as TMA boxes issued at kernel start; when they do not all fit
-// in shared memory they stream through rings whose slots the MMA thread hands
-// back with tcgen05.commit.  With a programmatic dependent launch the weight
-// copies start before the previous kernel in the stream has finished;
-// activations are read, and outputs written, only after it has.  The kernel is
-// short enough that instruction fetch matters: loops stay rolled.
+// Weights move as TMA boxes issued first thing in the kernel; when they do not
+// all fit in shared memory they stream through rings whose slots the MMA
+// threads hand back with tcgen05.commit.  Every CTA allows the next kernel in
+// the stream to launch right after its prologue: that kernel's CTAs take the
+// SMs the down CTAs leave and start their own weight copies while this call's
+// up CTAs finish.  With a programmatic dependent launch the weight copies
+// start before the previous kernel in the stream has finished; activations
+// and exchange buffers are touched, and outputs written, only after it has.
+// The kernel is short enough that instruction fetch matters: loops stay
+// rolled.
+//
+// Built with HCGR_TRACE defined, the kernel records %globaltimer stamps of its
+// phases per CTA in a device array (hc_gr_trace_read, include/hc_gr_trace.h).
 #include <algorithm>
 
 #include "hc_gr_internal.cuh"
@@ -67,18 +78,21 @@ constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int HDR = 512;             // mbarriers, TMEM address, flags
 constexpr int SMEM_BUDGET = 220 * 1024;
 constexpr int SMEM_ALLOC = SMEM_BUDGET + 1024;
+// Dynamic shared memory of a launch is at least this much, so that two CTAs
+// (of this grid or of consecutive calls) never share an SM: every CTA holds
+// tensor memory, and an exchange must never wait on a CTA that is not running.
+constexpr int SMEM_MIN = 120 * 1024;
 
 struct Geom {
   int Nt, Nd, Nu;                 // tokens rounded to 8; down MMA N (hi + lo); up MMA N
-  int nkc, P, G;                  // 64-column chunks per slice, slices per stream, CTAs
+  int Gd, Gu, G;                  // down CTAs, up CTAs, grid
+  int nkc, P;                     // down: 64-column chunks per slice, slices per stream
   int merged, rows_w, tail, wi_shared, wi_tile, wi_row, ntd, nsl_w;   // down weight
-  int nc_max, rows_u, ntu, nchunk_u, slot_u, nsl_u;                    // up weight
+  int nc_max, rows_u, ntu, nchunk_u, slot_u, nsl_u, ncu;               // up weight
   int Qn, Jm, nred, row, nquad, R, ppr, L2w;                           // exchanges
-  int tmem_cols;
-  int ncu;                        // gate-MMA issuers (accumulator copies)
-  int off_rr, off_iw, off_x3r, off_x3y, off_x3w, off_ssum, off_ss1, off_rl, off_act, off_u,
-      off_a;                      // (off_act: [nkc][Nd rows][128 B], hi rows then lo rows)
-  int off_red, off_hb, off_g;            // region A once the down weights are consumed
+  int tmem_d, tmem_u;             // tensor-memory columns of the two roles
+  int d_ss1, d_ssum, d_act, d_w, d_total;                              // down shared memory
+  int u_rr, u_iw, u_x3r, u_x3y, u_x3w, u_rl, u_red, u_g, u_hb, u_u, u_total;   // up
   int total;
 };
 
@@ -91,7 +105,7 @@ struct Params {
   CUtensorMap tm_wu;    // Wu as [HC][HS][r], box {64, nc_max, HC}
   Call c;
   Geom g;
-  uint32_t* xred;       // reduce-scatter words [nred][G][row]
+  uint32_t* xred;       // reduce-scatter words [nred][Gd][row]
   uint32_t* xgat;       // all-gather words, two copies of gat_words
   int gat_words;
   unsigned long long* ticket;
@@ -99,32 +113,41 @@ struct Params {
   uint64_t limit_ns;
 };
 
-bool layout(const Call& c, Geom& g) {
+int tmem_pow2(int cols) {
+  return cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+}
+
+bool layout_down(Geom& g) {
+  int off = HDR;
+  g.d_ss1 = off;  off += round_up(g.Nt * g.nkc * 8 * 4, 128);
+  g.d_ssum = off; off += round_up(g.Nt * 4, 128);
+  off = round_up(off, 1024);
+  g.d_act = off;  off += g.nkc * g.Nd * 128;          // [nkc][Nd rows][128 B], hi rows then lo rows
+  g.d_w = off;    off += g.nsl_w * TILE;
+  g.d_total = off;
+  return off <= SMEM_BUDGET;
+}
+
+bool layout_up(const Call& c, Geom& g) {
   const int M = static_cast<int>(c.M), Nt = g.Nt;
   int off = HDR;
-  g.off_rr = off;   off += round_up(Nt * c.HC * 4, 128);
-  g.off_iw = off;   off += round_up(Nt * c.HC * 4, 128);
-  g.off_x3r = off;  off += round_up(M * c.HC * g.nc_max * 2, 128);
-  g.off_x3y = off;  off += round_up(M * g.nc_max * 2, 128);
-  g.off_x3w = off;  off += round_up(c.HC * g.nc_max * 2, 128);
-  g.off_ssum = off; off += round_up(Nt * 4, 128);
-  g.off_ss1 = off;  off += round_up(Nt * g.nkc * 8 * 4, 128);
-  g.off_rl = off;   off += round_up(c.HC * 4, 128);
+  g.u_rr = off;  off += round_up(Nt * c.HC * 4, 128);
+  g.u_iw = off;  off += round_up(Nt * c.HC * 4, 128);
+  g.u_x3r = off; off += round_up(M * c.HC * g.nc_max * 2, 128);
+  g.u_x3y = off; off += round_up(M * g.nc_max * 2, 128);
+  g.u_x3w = off; off += round_up(c.HC * g.nc_max * 2, 128);
+  g.u_rl = off;  off += round_up(c.HC * 4, 128);
+  g.u_red = off; off += round_up(c.HC * g.row * 4, 128);
+  g.u_g = off;   off += round_up(M * g.rows_u * 4, 128);
   off = round_up(off, 1024);
-  g.off_act = off;  off += g.nkc * g.Nd * 128;
-  g.off_u = off;    off += g.nsl_u * g.slot_u;
-  g.off_a = off;
-  const int pw = g.nsl_w * TILE;
-  g.off_red = off;
-  const int pr = round_up(c.HC * g.row * 4, 128);
-  g.off_hb = off;
-  g.off_g = off + g.nchunk_u * g.Nu * 128;
-  const int pg = g.nchunk_u * g.Nu * 128 + round_up(M * g.rows_u * 4, 128);
+  g.u_hb = off;  off += g.nchunk_u * g.Nu * 128;       // [nchunk_u][Nu rows][128 B]
+  off = round_up(off, 1024);
+  g.u_u = off;   off += g.nsl_u * g.slot_u;
   // the up-weight A tiles read ntu * TILE bytes from a slot's start: the
-  // region after the last slot covers the overhang
-  const int over = g.ntu * TILE - g.slot_u;
-  g.total = off + std::max(std::max(pw, pr), std::max(pg, over));
-  return g.total <= SMEM_BUDGET;
+  // last slot's overhang stays inside the allocation
+  off += std::max(0, g.ntu * TILE - g.slot_u);
+  g.u_total = off;
+  return off <= SMEM_BUDGET;
 }
 
 bool make_geom(const Call& c, const Device& dev, Geom& g) {
@@ -142,19 +165,25 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
   g.wi_row = g.wi_shared ? g.tail : 0;
   g.ntd = g.merged || g.wi_shared ? nwd : nwd + 1;
   g.nchunk_u = (c.r + 63) / 64;
+  if (g.ntd > DOWN_ISSUERS || g.nchunk_u > UP_ISSUERS) return false;
   const int hsc = c.HS / 64;                            // 64-column chunks per stream
+  const int sms = std::min(dev.sms, MAX_GRID);
   for (g.nkc = 1; g.nkc <= hsc; ++g.nkc) {
     g.P = (hsc + g.nkc - 1) / g.nkc;
-    g.G = c.HC * g.P;
-    if (g.G > MAX_GRID) continue;
-    g.nc_max = round_up((c.HS + g.G - 1) / g.G, 2);
+    g.Gd = c.HC * g.P;
+    if (g.Gd >= sms) continue;
+    // up CTAs: the remaining SMs, each a channel range (an even count) of
+    // every stream; no up CTA without channels
+    g.nc_max = round_up((c.HS + (sms - g.Gd) - 1) / (sms - g.Gd), 2);
+    g.Gu = (c.HS + g.nc_max - 1) / g.nc_max;
+    g.G = g.Gd + g.Gu;
     g.rows_u = c.HC * g.nc_max;
-    if (g.nc_max > 256 || g.rows_u > 256) continue;
+    if (g.nc_max > 256 || g.rows_u > 512) continue;
     g.ntu = (g.rows_u + 127) / 128;
     g.slot_u = round_up(g.rows_u * 128, 1024);
     for (g.Qn = 4;; g.Qn += 4) {
       g.Jm = (c.n_out + g.Qn - 1) / g.Qn;
-      if (M * g.Jm <= g.G || g.Jm == 1) break;
+      if (M * g.Jm <= g.Gu || g.Jm == 1) break;
     }
     g.nred = M * g.Jm;
     g.row = g.Qn + 4;                       // Qn partials, the sum of squares, 3 pad words
@@ -166,38 +195,39 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     while (2 * g.R <= 32 && 2 * g.R * c.HC * g.nquad <= NT) g.R *= 2;
     g.ppr = (g.P + g.R - 1) / g.R;
     g.L2w = round_up(c.r / 2 + c.HC, 4);     // h pairs, then rrms, then pad words
-    if (g.ntd > DOWN_ISSUERS || g.nchunk_u > UP_ISSUERS) return false;
-    // all weight tiles resident when they fit, else rings
+    // down: every box resident when they fit, else the deepest ring that
+    // fits, with a multiple of ntd slots, so that each slot only ever holds
+    // boxes of one row tile: its issuer then waits on the slot's phases in
+    // order (a waiter more than one phase ahead would see the older phase)
     const int nbox = g.ntd * g.nkc;
     bool fits = false;
-    // With rings the weight streams are bound by the bytes in flight per SM,
-    // so the rings take what the budget allows: the up ring first (its
-    // refills sit on the critical path after the exchanges; a ring of fewer
-    // slots than chunks alternates its slots between two issuers, so it has
-    // an even count), then the down ring (at least four slots if possible).
-    g.nsl_w = nbox;
-    g.nsl_u = g.nchunk_u;
-    fits = g.nsl_w <= MAX_SLOTS && g.nsl_u <= MAX_SLOTS && layout(c, g);
-    for (int wmin = std::min(nbox, 4); wmin >= 2 && !fits; wmin -= 2) {
-      for (int u = std::min(g.nchunk_u, MAX_SLOTS); u >= 2 && !fits; --u) {
-        if (u < g.nchunk_u && (u & 1)) continue;
-        g.nsl_u = u;
-        for (int w = std::min(nbox, MAX_SLOTS); w >= wmin && !fits; --w) {
-          g.nsl_w = w;
-          fits = layout(c, g);
-        }
-      }
+    for (int w = std::min(nbox, MAX_SLOTS); w >= 1 && !fits; --w) {
+      if (w < nbox && w % g.ntd != 0) continue;
+      g.nsl_w = w;
+      fits = layout_down(g);
     }
+    if (!fits) continue;
+    // up: every chunk resident when it fits, else an even ring (its two
+    // issuers take alternate slots)
+    bool fits_u = false;
+    for (int u = std::min(g.nchunk_u, MAX_SLOTS); u >= 1 && !fits_u; --u) {
+      if (u < g.nchunk_u && (u & 1)) continue;
+      g.nsl_u = u;
+      fits_u = layout_up(c, g);
+    }
+    if (!fits_u) continue;
     // down: one accumulator per row tile (one issuing thread each); up: one
     // accumulator copy per issuing thread -- a thread per Wu chunk when every
-    // chunk has its own slot and the copies fit, else two (the ring's two
-    // slots alternate between them)
-    g.ncu = g.nsl_u >= g.nchunk_u && g.nchunk_u * g.ntu * g.Nu <= 512 ? g.nchunk_u : 2;
-    const int cols = std::max(g.ntd * g.Nd, g.ncu * g.ntu * g.Nu);
-    if (cols > 512) fits = false;
-    g.tmem_cols = cols <= 32 ? 32 : cols <= 64 ? 64 : cols <= 128 ? 128 : cols <= 256 ? 256 : 512;
+    // chunk has its own slot and the copies fit, else two
+    g.ncu = g.nsl_u >= g.nchunk_u && g.nchunk_u * g.ntu * g.Nu <= 512 ? g.nchunk_u
+                                                                       : std::min(2, g.nchunk_u);
+    const int cd = g.ntd * g.Nd, cu = g.ncu * g.ntu * g.Nu;
+    if (cd > 512 || cu > 512) continue;
+    g.tmem_d = tmem_pow2(cd);
+    g.tmem_u = tmem_pow2(cu);
+    g.total = std::max(std::max(g.d_total, g.u_total), SMEM_MIN - 1024);
     // a kernel that allocates TMEM runs one CTA per SM
-    if (fits && g.G <= dev.sms) return true;
+    if (g.G <= dev.sms) return true;
   }
   return false;
 }
@@ -221,6 +251,20 @@ __device__ __noinline__ uint4 wait_words(const uint32_t* p, int* err, long long 
   return v;
 }
 
+#ifdef HCGR_TRACE
+constexpr int TRACE_SLOTS = 16;
+__device__ unsigned long long g_trace[MAX_GRID * TRACE_SLOTS];
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Phase stamp i of this CTA (the calling thread records it).
+#define HCGR_STAMP(i) (g_trace[blockIdx.x * TRACE_SLOTS + (i)] = globaltimer_ns())
+#else
+#define HCGR_STAMP(i) ((void)0)
+#endif
+
 // --------------------------------------------------------------- the kernel
 __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ Params p) {
   extern __shared__ unsigned char smem_raw[];
@@ -233,6 +277,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   const int M = static_cast<int>(c.M), Nt = g.Nt, Nd = g.Nd, Nu = g.Nu;
   const int HC = c.HC, HS = c.HS, K = c.K, r = c.r, n_out = c.n_out;
   const long long limit = wait_limit_cycles(p.limit_ns);
+  const bool down = b < g.Gd;
+  const bool has_y = c.y != nullptr;   // false: mix only, R2 = R
+  const float inv_hc = 1.0f / static_cast<float>(HC);
+  if (tid == 0) HCGR_STAMP(0);
 
   const uint32_t bar0 = smem_u32(smem);
   auto full_w = [&](int i) { return bar0 + 8u * i; };
@@ -243,30 +291,19 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 272);
   uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + 276);
   int* s_mma_ok = reinterpret_cast<int*>(smem + 280);
-  float* s_rr = reinterpret_cast<float*>(smem + g.off_rr);     // [Nt][HC] rrms (all-gather)
-  float* s_iw = reinterpret_cast<float*>(smem + g.off_iw);     // [Nt][HC]
-  bf16_t* s_x3r = reinterpret_cast<bf16_t*>(smem + g.off_x3r); // [M][HC][nc_max]
-  bf16_t* s_x3y = reinterpret_cast<bf16_t*>(smem + g.off_x3y); // [M][nc_max]
-  bf16_t* s_x3w = reinterpret_cast<bf16_t*>(smem + g.off_x3w); // [HC][nc_max]
-  float* s_ssum = reinterpret_cast<float*>(smem + g.off_ssum); // [Nt] sum of R2^2 on the slice
-  float* s_ss1 = reinterpret_cast<float*>(smem + g.off_ss1);   // [Nt][8 nkc]
-  float* s_rl = reinterpret_cast<float*>(smem + g.off_rl);     // [HC] the reducer's rrms
-  float* s_red = reinterpret_cast<float*>(smem + g.off_red);   // [HC][row]
-  float* s_g = reinterpret_cast<float*>(smem + g.off_g);       // [M][rows_u]
-  const uint32_t act = smem_u32(smem + g.off_act);             // [nkc][Nd rows][128 B]
-  const uint32_t wbase = smem_u32(smem + g.off_a);             // down weight slots
-  const uint32_t ubase = smem_u32(smem + g.off_u);             // up weight slots
-  const uint32_t hbase = smem_u32(smem + g.off_hb);            // [nchunk_u][Nu rows][128 B]
 
-  // this CTA's slice (step 1) and channel range (step 4)
-  const int s = b / g.P;
-  const int c0 = (b % g.P) * 64 * g.nkc;
-  const int nkv = min(g.nkc, (HS - c0) / 64);                  // chunks of the slice
+  // this CTA's work: the down slice, or the up channel range
+  const int s = down ? b / g.P : 0;
+  const int c0 = down ? (b % g.P) * 64 * g.nkc : 0;
+  const int nkv = down ? min(g.nkc, (HS - c0) / 64) : 0;       // chunks of the slice
   const int k0 = s * HS + c0;
-  const int cp0 = min(HS, b * g.nc_max);
-  const int nc = min(HS, cp0 + g.nc_max) - cp0;
   const int nbox = g.ntd * nkv;                                // down weight boxes
+  const int u_idx = down ? 0 : b - g.Gd;
+  const int cp0 = down ? 0 : min(HS, u_idx * g.nc_max);
+  const int nc = down ? 0 : min(HS, cp0 + g.nc_max) - cp0;
   const int nub = nc > 0 ? g.nchunk_u : 0;                     // up weight boxes
+  const uint32_t wbase = smem_u32(smem + g.d_w);               // down weight slots
+  const uint32_t ubase = smem_u32(smem + g.u_u);               // up weight slots
 
   auto issue_w = [&](int i) {   // box i: chunk i / ntd, row tile i % ntd
     const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
@@ -286,12 +323,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     tma_load_3d(ubase + slot * g.slot_u, &p.tm_wu, q * 64, cp0, 0, full_u(slot));
   };
 
-  // Down-weight copies first (they do not depend on the previous kernel):
-  // thread 0 initialises the barriers, then lane 0 of warp w issues down box
-  // w, so the issue latencies overlap; warp 15 takes the call ticket and warp
-  // 3 allocates TMEM meanwhile.
+  // Prologue: thread 0 initialises the barriers, then lane 0 of warp w
+  // issues the role's weight box w, so the issue latencies overlap; warp 15
+  // takes the call ticket and warp 3 allocates TMEM meanwhile.  None of this
+  // depends on the previous kernel.
   const int pre_w = min(g.nsl_w, nbox), pre_u = min(g.nsl_u, nub);
-  int issued_w = pre_w, issued_u = pre_u;   // kept by thread 0, which drains them
+  int issued_w = down ? pre_w : 0, issued_u = down ? 0 : pre_u;   // kept by thread 0
   if (tid == 0) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
@@ -302,14 +339,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   }
   __syncthreads();
   if (lane == 0) {
+    const int npre = down ? pre_w : pre_u;
+    if (warp < npre) prefetch_tmap(down ? &p.tm_w : &p.tm_wu);
 #pragma unroll 1
-    for (int k = warp; k < pre_w + pre_u; k += NW) {
-      if (k < pre_w) {
-        prefetch_tmap(&p.tm_w);
-        issue_w(k);
-      } else {
-        prefetch_tmap(&p.tm_wu);   // the up boxes are issued after COMBINE (step 2)
-      }
+    for (int k = warp; k < npre; k += NW) {
+      if (down) issue_w(k);
+      else issue_u(k);
     }
   } else if (warp == NW - 1 && lane == 1) {
     // arrivals in the low half, the call's epoch in the high half; the last
@@ -319,433 +354,453 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       atomicAdd(p.ticket, (1ull << 32) - static_cast<unsigned long long>(g.G));
     *s_epoch = static_cast<uint32_t>(old >> 32);
   }
+  const int tmem_cols = down ? g.tmem_d : g.tmem_u;
   if (warp == 3) {
     __syncwarp();
-    tmem_alloc(smem_u32(s_tmem), g.tmem_cols);
+    tmem_alloc(smem_u32(s_tmem), tmem_cols);
     tmem_relinquish();
   }
-  // inputs and outputs may belong to the previous kernel in the stream
+  if (tid == 0) HCGR_STAMP(1);
+  // Every CTA of this grid is running: the next kernel in the stream may
+  // launch (its CTAs wait for SMs this grid frees, then for this grid's end
+  // before they touch activations or exchange buffers).
+  grid_dep_launch();
+  // inputs, outputs and exchange buffers may belong to the previous kernel
   grid_dep_wait();
+  if (tid == 0) HCGR_STAMP(2);
 
-  // Inputs of this CTA's channel range for the final mix -- R, y, Wnorm in
-  // channel pairs, and inj (iw is formed from it later) -- copied
-  // asynchronously now, so that their latency hides behind COMBINE and the
-  // down MMAs.
-  const bool has_y = c.y != nullptr;   // false: mix only, R2 = R
-  {
-    const int np = nc / 2;
-    const int n_iw = has_y ? M * HC : 0, n_r = M * HC * np, n_y = has_y ? M * np : 0, n_w = HC * np;
-#pragma unroll 1
-    for (int i = tid; i < n_iw + n_r + n_y + n_w; i += NT) {
-      if (i < n_iw) {
-        cp_async4(s_iw + i, c.inj + (i / HC) * c.ld_inj + (i % HC));
-      } else if (i < n_iw + n_r) {
-        const int j = i - n_iw, row = j / np, cc = 2 * (j - row * np);   // row = m * HC + stream
-        const int m = row / HC, ss = row - m * HC;
-        cp_async4(s_x3r + row * g.nc_max + cc, c.R + static_cast<int64_t>(m) * K + ss * HS + cp0 + cc);
-      } else if (i < n_iw + n_r + n_y) {
-        const int j = i - n_iw - n_r, m = j / np, cc = 2 * (j - m * np);
-        cp_async4(s_x3y + m * g.nc_max + cc, c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
-      } else {
-        const int j = i - n_iw - n_r - n_y, ss = j / np, cc = 2 * (j - ss * np);
-        cp_async4(s_x3w + ss * g.nc_max + cc, c.Wnorm + ss * c.ld_wnorm + cp0 + cc);
-      }
-    }
-  }
+  bool ok = true;
+  bool down_issued = false, up_issued = false;   // MMAs to drain at the end
+  if (down) {
+    // ====================================================== down role
+    float* s_ss1 = reinterpret_cast<float*>(smem + g.d_ss1);   // [Nt][8 nkc]
+    float* s_ssum = reinterpret_cast<float*>(smem + g.d_ssum); // [Nt] sum of R2^2 on the slice
+    const uint32_t act = smem_u32(smem + g.d_act);             // [nkc][Nd rows][128 B]
 
-  // --- step 1: COMBINE on this CTA's slice, R2 stored, MMA operands in the
-  // swizzled layout (16-byte unit u of row m of a chunk at (u ^ (m & 7)) * 16;
-  // hi in rows m, lo in rows Nt + m)
-  const int nu = g.nkc * 8;                                    // 16-byte units per row
-  const float inv_hc0 = 1.0f / static_cast<float>(HC);
+    // --- step 1: COMBINE on this CTA's slice, R2 stored, MMA operands in the
+    // swizzled layout (16-byte unit u of row m of a chunk at (u ^ (m & 7)) *
+    // 16; hi in rows m, lo in rows Nt + m)
+    const int nu = g.nkc * 8;                                  // 16-byte units per row
 #pragma unroll 1
-  for (int it = tid; it < Nt * nu; it += NT) {
-    const int m = it / nu, un = it - m * nu;
-    const int ch = un >> 3, u = un & 7;
-    uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
-    float ss = 0.f;
-    if (m < M && ch < nkv) {
-      const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
-      float rv[8], yv[8] = {}, wv[8], a[8];
-      float iw = 0.f;
-      unpack8(__ldg(reinterpret_cast<const uint4*>(c.R + kk)), rv);
-      if (has_y) {
-        iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc0);
-        unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
-      }
-      unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + s * c.ld_wnorm + c0 + un * 8)), wv);
-      uint32_t pr[4], ph[4], pl[4];
+    for (int it = tid; it < Nt * nu; it += NT) {
+      const int m = it / nu, un = it - m * nu;
+      const int ch = un >> 3, uu = un & 7;
+      uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
+      float ss = 0.f;
+      if (m < M && ch < nkv) {
+        const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
+        float rv[8], yv[8] = {}, wv[8], a[8];
+        float iw = 0.f;
+        unpack8(__ldg(reinterpret_cast<const uint4*>(c.R + kk)), rv);
+        if (has_y) {
+          iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc);
+          unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
+        }
+        unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + s * c.ld_wnorm + c0 + un * 8)), wv);
+        uint32_t pr[4], ph[4], pl[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(yv[i], iw, rv[i]))) : rv[i];
-        ss = fmaf(r2, r2, ss);
-        rv[i] = r2;
-        a[i] = c.fold ? r2 : r2 * (1.0f + wv[i]);
-      }
+        for (int i = 0; i < 8; ++i) {
+          const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(yv[i], iw, rv[i]))) : rv[i];
+          ss = fmaf(r2, r2, ss);
+          rv[i] = r2;
+          a[i] = c.fold ? r2 : r2 * (1.0f + wv[i]);
+        }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        pr[i] = pack2(rv[2 * i], rv[2 * i + 1]);
-        const float h0 = bf16_to_f32(f32_to_bf16(a[2 * i]));
-        const float h1 = bf16_to_f32(f32_to_bf16(a[2 * i + 1]));
-        ph[i] = pack2(h0, h1);
-        pl[i] = pack2(a[2 * i] - h0, a[2 * i + 1] - h1);
+        for (int i = 0; i < 4; ++i) {
+          pr[i] = pack2(rv[2 * i], rv[2 * i + 1]);
+          const float h0 = bf16_to_f32(f32_to_bf16(a[2 * i]));
+          const float h1 = bf16_to_f32(f32_to_bf16(a[2 * i + 1]));
+          ph[i] = pack2(h0, h1);
+          pl[i] = pack2(a[2 * i] - h0, a[2 * i + 1] - h1);
+        }
+        if (c.R2) *reinterpret_cast<uint4*>(c.R2 + kk) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+        hv = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+        lv = make_uint4(pl[0], pl[1], pl[2], pl[3]);
       }
-      if (c.R2) *reinterpret_cast<uint4*>(c.R2 + kk) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-      hv = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-      lv = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+      const int sw = ch * Nd * 128 + m * 128 + ((uu ^ (m & 7)) << 4);
+      *reinterpret_cast<uint4*>(smem + g.d_act + sw) = hv;
+      *reinterpret_cast<uint4*>(smem + g.d_act + sw + Nt * 128) = lv;
+      s_ss1[m * nu + un] = ss;
     }
-    const int sw = ch * Nd * 128 + m * 128 + ((u ^ (m & 7)) << 4);
-    *reinterpret_cast<uint4*>(smem + g.off_act + sw) = hv;
-    *reinterpret_cast<uint4*>(smem + g.off_act + sw + Nt * 128) = lv;
-    s_ss1[m * nu + un] = ss;
-  }
-  fence_proxy_async_smem();   // the operand rows are read by the tensor cores
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *s_tmem;
+    fence_proxy_async_smem();   // the operand rows are read by the tensor cores
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) HCGR_STAMP(3);
+    const uint32_t tmem = *s_tmem;
 
-  // --- step 2: the down/inject products on the tensor cores.  When every
-  // box has its own slot, lane 0 of warp 2t + 1 issues the MMAs of row tile t
-  // (all chunks, one accumulator per tile): up to DOWN_ISSUERS threads issue
-  // side by side, each tcgen05.mma issue costing ~100 cycles.  With a ring
-  // (whose slots the issuer hands back) thread 32 alone consumes the boxes,
-  // in order, and thread 0 refills.  Every issuer thread commits barD.
-  const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
-  const bool ring = g.nsl_w < nbox;
-  if ((tid & 63) == 32 && (tid >> 6) < DOWN_ISSUERS) {
-    const int me = tid >> 6;
-    const uint32_t idesc = idesc_bf16(128, Nd);
-    bool okm = true;
+    // --- step 2: the down/inject products on the tensor cores: lane 0 of
+    // warp 2t + 1 issues the MMAs of row tile t (all chunks, one accumulator
+    // per tile), so up to DOWN_ISSUERS threads issue side by side.  With a
+    // ring, thread 0 refills each slot once the MMAs that read it have
+    // completed; every issuer thread commits barD.
+    const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
+    if ((tid & 63) == 32 && (tid >> 6) < DOWN_ISSUERS) {
+      const int me = tid >> 6;
+      const uint32_t idesc = idesc_bf16(128, Nd);
+      bool okm = true;
 #pragma unroll 1
-    for (int i = 0; i < nbox && okm; ++i) {
-      const int ch = i / g.ntd, t = i - ch * g.ntd, slot = i % g.nsl_w;
-      if (ring ? me != 0 : t != me) continue;
-      const uint32_t ph = (i / g.nsl_w) & 1;
-      okm = mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns);
-      if (!okm) break;
-      tc_fence_after();
-      const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
-      const uint32_t d = tmem + t * Nd;
+      for (int i = me; i < nbox && okm && me < g.ntd; i += g.ntd) {
+        const int ch = i / g.ntd, slot = i % g.nsl_w;
+        const uint32_t ph = (i / g.nsl_w) & 1;
+        okm = mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns);
+        if (!okm) break;
+        tc_fence_after();
+        const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
+        const uint32_t d = tmem + me * Nd;
 #pragma unroll 1
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc, (ch || ks) ? 1u : 0u);
-      umma_commit(free_w(slot));
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc, (ch || ks) ? 1u : 0u);
+        umma_commit(free_w(slot));
+      }
+      if (me == 0) HCGR_STAMP(4);
+      if (!okm) *s_mma_ok = 0;
+      umma_commit(barD);
+    } else if (tid == 0) {
+      // ring refills: a slot is free once the MMAs that read it have completed
+#pragma unroll 1
+      for (int i = pre_w; i < nbox; ++i) {
+        const int slot = i % g.nsl_w;
+        if (!wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)) break;
+        issue_w(i);
+        ++issued_w;
+      }
     }
-    if (!okm) *s_mma_ok = 0;
-    umma_commit(barD);
-  } else if (tid == 0) {
-    // the up-weight boxes: requested only now, so that the down boxes, which
-    // the next MMAs need, do not share this SM's copy bandwidth with them
+    down_issued = true;
+    // the sum of squares, and the non-product words of this CTA's piece of
+    // every reduce-scatter block ([Qn partials][sum of squares][3 pad
+    // words], partials past n_out zero)
+    if (tid < Nt) {
+      float ss = 0.f;
 #pragma unroll 1
-    for (int q = 0; q < pre_u; ++q) issue_u(q);
-    // ring refills: a slot is free once the MMAs that read it have completed
-#pragma unroll 1
-    for (int i = pre_w; i < nbox; ++i) {
-      const int slot = i % g.nsl_w;
-      if (!wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)) break;
-      issue_w(i);
-      ++issued_w;
+      for (int j = 0; j < nkv * 8; ++j) ss += s_ss1[tid * nu + j];
+      s_ssum[tid] = ss;
     }
-  }
-  // the final mix's inputs (copied since the prologue) have landed; iw from inj
-  cp_async_wait_all();
+    __syncthreads();
+    if (!dead) {
 #pragma unroll 1
-  for (int i = tid; i < M * HC; i += NT) s_iw[i] = has_y ? combine_weight(s_iw[i], inv_hc0) : 0.f;
-  // and the sum of squares, and the non-product words of this CTA's
-  // piece of every reduce-scatter block ([Qn partials][sum of squares][3 pad
-  // words], partials past n_out zero)
-  if (tid < Nt) {
-    float ss = 0.f;
+      for (int j = tid; j < g.nred; j += NT) {
+        const int m = j / g.Jm, jn = j - m * g.Jm;
+        uint32_t* dst = p.xred + (static_cast<size_t>(j) * g.Gd + b) * g.row;
+        st_relaxed_v4(dst + g.Qn, make_uint4(xword(s_ssum[m]), 0u, 0u, 0u));
 #pragma unroll 1
-    for (int j = 0; j < nkv * 8; ++j) ss += s_ss1[tid * nu + j];
-    s_ssum[tid] = ss;
-  }
-  __syncthreads();
-  if (!dead) {
-#pragma unroll 1
-    for (int j = tid; j < g.nred; j += NT) {
-      const int m = j / g.Jm, jn = j - m * g.Jm;
-      uint32_t* dst = p.xred + (static_cast<size_t>(j) * g.G + b) * g.row;
-      st_relaxed_v4(dst + g.Qn, make_uint4(xword(s_ssum[m]), 0u, 0u, 0u));
-#pragma unroll 1
-      for (int q = n_out - jn * g.Qn; q < g.Qn; ++q) st_relaxed_u32(dst + q, 0u);
+        for (int q = n_out - jn * g.Qn; q < g.Qn; ++q) st_relaxed_u32(dst + q, 0u);
+      }
     }
-  }
-  // the products, straight from TMEM (hi + lo halves, both accumulator
-  // copies): warp w reads lanes 32 (w % 4) ..; the two warp groups take
-  // alternate row tiles
-  bool ok = wait_bar(barD, 0, p.err, p.limit_ns);
-  tc_fence_after();
-  ok = __syncthreads_and(ok && *s_mma_ok != 0);
-  if (ok && !dead) {
-    const int q4 = warp & 3, grp = warp >> 2;                  // 4 groups of 4 warps
-    const int tr = 32 * q4 + lane;                             // row within a tile
-    const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-    const int nmc = Nt / 8;                                    // 8-token chunks
+    // the products, straight from TMEM (hi + lo halves): warp w reads lanes
+    // 32 (w % 4) ..; the four warp groups take alternate (tile, 8-token) items
+    ok = wait_bar(barD, 0, p.err, p.limit_ns);
+    tc_fence_after();
+    ok = __syncthreads_and(ok && *s_mma_ok != 0);
+    if (tid == 0) HCGR_STAMP(5);
+    if (ok && !dead) {
+      const int q4 = warp & 3, grp = warp >> 2;
+      const int tr = 32 * q4 + lane;                           // row within a tile
+      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+      const int nmc = Nt / 8;                                  // 8-token chunks
 #pragma unroll 1
-    for (int item = grp; item < g.ntd * nmc; item += NW / 4) {
-      const int t = item / nmc, m0 = (item - t * nmc) * 8;
-      const int rt = t * 128 + tr;
-      const bool inj_row = t == g.wi_tile && tr >= g.wi_row;
-      const int n = inj_row ? r + (tr - g.wi_row) : rt;
-      const bool valid = inj_row ? n < n_out : rt < g.rows_w;
-      const int jn = n / g.Qn, qn = n - jn * g.Qn;
-      uint32_t h0[8], l0[8];
-      tmem_ld8x2_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, h0, l0);
-      if (valid) {
+      for (int item = grp; item < g.ntd * nmc; item += NW / 4) {
+        const int t = item / nmc, m0 = (item - t * nmc) * 8;
+        const int rt = t * 128 + tr;
+        const bool inj_row = t == g.wi_tile && tr >= g.wi_row;
+        const int n = inj_row ? r + (tr - g.wi_row) : rt;
+        const bool valid = inj_row ? n < n_out : rt < g.rows_w;
+        const int jn = n / g.Qn, qn = n - jn * g.Qn;
+        uint32_t h0[8], l0[8];
+        tmem_ld8x2_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, h0, l0);
+        if (valid) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float v = __uint_as_float(h0[e]) + __uint_as_float(l0[e]);
-          if (m0 + e < M)
-            st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.G + b) * g.row + qn,
-                           xword(v));
+          for (int e = 0; e < 8; ++e) {
+            const float v = __uint_as_float(h0[e]) + __uint_as_float(l0[e]);
+            if (m0 + e < M)
+              st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.Gd + b) * g.row + qn,
+                             xword(v));
+          }
         }
       }
     }
-  }
-  // The weights of the down step are consumed: the next kernel in the stream
-  // may start launching.
-  grid_dep_launch();
-  tc_fence_before();
-  __syncthreads();
-  const uint32_t par = *s_epoch & 1u;
-  uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
+    if (tid == 0) HCGR_STAMP(6);
+  } else {
+    // ======================================================== up role
+    float* s_rr = reinterpret_cast<float*>(smem + g.u_rr);     // [Nt][HC] rrms (all-gather)
+    float* s_iw = reinterpret_cast<float*>(smem + g.u_iw);     // [Nt][HC]
+    bf16_t* s_x3r = reinterpret_cast<bf16_t*>(smem + g.u_x3r); // [M][HC][nc_max]
+    bf16_t* s_x3y = reinterpret_cast<bf16_t*>(smem + g.u_x3y); // [M][nc_max]
+    bf16_t* s_x3w = reinterpret_cast<bf16_t*>(smem + g.u_x3w); // [HC][nc_max]
+    float* s_rl = reinterpret_cast<float*>(smem + g.u_rl);     // [HC] the reducer's rrms
+    float* s_red = reinterpret_cast<float*>(smem + g.u_red);   // [HC][row]
+    float* s_g = reinterpret_cast<float*>(smem + g.u_g);       // [M][rows_u]
+    const uint32_t hbase = smem_u32(smem + g.u_hb);            // [nchunk_u][Nu rows][128 B]
 
-  // --- step 3: the reducer of blocks b, b + G, ...  Work item (stream, quad,
-  // sub-range) sums quad u of the stream's pieces in its sub-range, XU loads
-  // in flight; the R sub-ranges of one (stream, quad) sit in consecutive
-  // lanes and fold with a fixed shuffle tree (deterministic).
+    // Inputs of this CTA's channel range for the final mix -- R, y, Wnorm in
+    // channel pairs, and inj (iw is formed from it later) -- copied
+    // asynchronously now, so that their latency hides behind the reduce.
+    {
+      const int np = nc / 2;
+      const int n_iw = has_y ? M * HC : 0, n_r = M * HC * np, n_y = has_y ? M * np : 0, n_w = HC * np;
 #pragma unroll 1
-  for (int j = b; j < g.nred && ok; j += g.G) {
-    const int m = j / g.Jm, jn = j - m * g.Jm;
-    const uint32_t* blk = p.xred + static_cast<size_t>(j) * g.G * g.row;
-    bool got = true;
-    const int nitem = HC * g.nquad * g.R;
+      for (int i = tid; i < n_iw + n_r + n_y + n_w; i += NT) {
+        if (i < n_iw) {
+          cp_async4(s_iw + i, c.inj + (i / HC) * c.ld_inj + (i % HC));
+        } else if (i < n_iw + n_r) {
+          const int j = i - n_iw, rw = j / np, cc = 2 * (j - rw * np);   // rw = m * HC + stream
+          const int m = rw / HC, ss = rw - m * HC;
+          cp_async4(s_x3r + rw * g.nc_max + cc, c.R + static_cast<int64_t>(m) * K + ss * HS + cp0 + cc);
+        } else if (i < n_iw + n_r + n_y) {
+          const int j = i - n_iw - n_r, m = j / np, cc = 2 * (j - m * np);
+          cp_async4(s_x3y + m * g.nc_max + cc, c.y + static_cast<int64_t>(m) * HS + cp0 + cc);
+        } else {
+          const int j = i - n_iw - n_r - n_y, ss = j / np, cc = 2 * (j - ss * np);
+          cp_async4(s_x3w + ss * g.nc_max + cc, c.Wnorm + ss * c.ld_wnorm + cp0 + cc);
+        }
+      }
+    }
+    const uint32_t par = *s_epoch & 1u;
+    uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
+
+    // --- step 4: the reducer of blocks u, u + Gu, ...  Work item (stream,
+    // quad, sub-range) sums quad uq of the stream's pieces in its sub-range,
+    // XU loads in flight; the R sub-ranges of one (stream, quad) sit in
+    // consecutive lanes and fold with a fixed shuffle tree (deterministic).
 #pragma unroll 1
-    for (int wi0 = 0; wi0 < nitem; wi0 += NT) {            // uniform: whole warps shuffle
-      const int wi = wi0 + tid;
-      const int su = wi / g.R, jr = wi - su * g.R;         // su = stream * nquad + quad
-      const int ss = su / g.nquad, u = su - ss * g.nquad;
-      const int p0 = jr * g.ppr, p1 = wi < nitem ? min(g.P, p0 + g.ppr) : p0;
-      float run[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int j = u_idx; j < g.nred && ok; j += g.Gu) {
+      const int m = j / g.Jm, jn = j - m * g.Jm;
+      const uint32_t* blk = p.xred + static_cast<size_t>(j) * g.Gd * g.row;
+      bool got = true;
+      const int nitem = HC * g.nquad * g.R;
 #pragma unroll 1
-      for (int pp0 = p0; pp0 < p1 && got; pp0 += XU) {
+      for (int wi0 = 0; wi0 < nitem; wi0 += NT) {            // uniform: whole warps shuffle
+        const int wi = wi0 + tid;
+        const int su = wi / g.R, jr = wi - su * g.R;         // su = stream * nquad + quad
+        const int ss = su / g.nquad, uq = su - ss * g.nquad;
+        const int p0 = jr * g.ppr, p1 = wi < nitem ? min(g.P, p0 + g.ppr) : p0;
+        float run[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int pp0 = p0; pp0 < p1 && got; pp0 += XU) {
+          uint4 v[XU];
+#pragma unroll
+          for (int k = 0; k < XU; ++k)
+            v[k] = pp0 + k < p1 ? ld_relaxed_v4(blk + (ss * g.P + pp0 + k) * g.row + uq * 4)
+                                : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+          for (int k = 0; k < XU; ++k) {
+            if (pp0 + k >= p1 || !got) break;
+            uint32_t* src = const_cast<uint32_t*>(blk) + (ss * g.P + pp0 + k) * g.row + uq * 4;
+            if (!all_set(v[k])) {
+              v[k] = wait_words(src, p.err, limit);
+              if (!all_set(v[k])) { got = false; break; }
+            }
+            *reinterpret_cast<uint4*>(src) = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
+            run[0] += __uint_as_float(v[k].x);
+            run[1] += __uint_as_float(v[k].y);
+            run[2] += __uint_as_float(v[k].z);
+            run[3] += __uint_as_float(v[k].w);
+          }
+        }
+#pragma unroll 1
+        for (int o = g.R / 2; o > 0; o >>= 1)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) run[e] += __shfl_xor_sync(0xffffffffu, run[e], o);
+        if (wi < nitem && jr == 0)
+          *reinterpret_cast<float4*>(s_red + ss * g.row + uq * 4) = make_float4(run[0], run[1], run[2], run[3]);
+      }
+      ok = __syncthreads_and(got);
+      if (!ok) break;
+      if (tid == 0 && j == u_idx) HCGR_STAMP(7);
+      if (tid < HC) {
+        const float rr = rsqrt_nr(fmaf(s_red[tid * g.row + g.Qn], __fdividef(1.0f, static_cast<float>(HS)), c.eps));
+        s_rl[tid] = rr;
+        if (jn == 0) c.rrms[m * HC + tid] = rr;
+      }
+      __syncthreads();
+#pragma unroll 1
+      for (int qp = tid; qp < g.Qn / 2; qp += NT) {
+        float v[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int q = 2 * qp + e;
+          float a = 0.f;
+#pragma unroll 1
+          for (int ss = 0; ss < HC; ++ss) a += s_rl[ss] * s_red[ss * g.row + q];
+          v[e] = a;
+          const int n = jn * g.Qn + q;
+          if (n < r)
+            c.lora[static_cast<int64_t>(m) * r + n] = a;
+          else if (n < n_out)
+            c.inj_next[static_cast<int64_t>(m) * HC + (n - r)] = a;
+        }
+        const int n0 = jn * g.Qn + 2 * qp;
+        if (n0 < r) {   // r is even: n0 + 1 < r too
+          const float u0 = v[0] * inv_hc, u1 = v[1] * inv_hc;
+          st_relaxed_u32(gat + m * g.L2w + n0 / 2,
+                         pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1)));
+        }
+      }
+      if (jn == 0) {
+#pragma unroll 1
+        for (int i = r / 2 + tid; i < g.L2w; i += NT) {
+          const int ss = i - r / 2;
+          st_relaxed_u32(gat + m * g.L2w + i, ss < HC ? xword(s_rl[ss]) : 0u);
+        }
+      }
+      __syncthreads();   // s_red is reused by the next block
+    }
+    if (tid == 0) HCGR_STAMP(8);
+    // empty this CTA's share of the copy the next call uses
+    {
+      uint4* nxt = reinterpret_cast<uint4*>(p.xgat + static_cast<size_t>(par ^ 1u) * p.gat_words);
+      const int nq = p.gat_words / 4;
+      const int per = (nq + g.Gu - 1) / g.Gu;
+#pragma unroll 1
+      for (int i = u_idx * per + tid; i < min(nq, (u_idx + 1) * per); i += NT)
+        nxt[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
+    }
+    // the final mix's inputs (copied since the prologue) have landed; iw from
+    // inj (each thread converts the words it copied)
+    cp_async_wait_all();
+#pragma unroll 1
+    for (int i = tid; i < M * HC; i += NT) s_iw[i] = has_y ? combine_weight(s_iw[i], inv_hc) : 0.f;
+
+    // --- step 5: all-gather of h (into the swizzled operand layout) and rrms
+    if (ok && nc > 0) {
+      bool got = true;
+      const int hw = r / 2;
+      const int nq = M * g.L2w / 4;
+#pragma unroll 1
+      for (int i0 = tid; i0 < nq && got; i0 += XU * NT) {
         uint4 v[XU];
 #pragma unroll
         for (int k = 0; k < XU; ++k)
-          v[k] = pp0 + k < p1 ? ld_relaxed_v4(blk + (ss * g.P + pp0 + k) * g.row + u * 4)
-                              : make_uint4(0u, 0u, 0u, 0u);
+          v[k] = i0 + k * NT < nq ? ld_relaxed_v4(gat + (i0 + k * NT) * 4) : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
         for (int k = 0; k < XU; ++k) {
-          if (pp0 + k >= p1 || !got) break;
-          uint32_t* src = const_cast<uint32_t*>(blk) + (ss * g.P + pp0 + k) * g.row + u * 4;
+          const int i = i0 + k * NT;
+          if (i >= nq || !got) break;
           if (!all_set(v[k])) {
-            v[k] = wait_words(src, p.err, limit);
+            v[k] = wait_words(gat + i * 4, p.err, limit);
             if (!all_set(v[k])) { got = false; break; }
           }
-          *reinterpret_cast<uint4*>(src) = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
-          run[0] += __uint_as_float(v[k].x);
-          run[1] += __uint_as_float(v[k].y);
-          run[2] += __uint_as_float(v[k].z);
-          run[3] += __uint_as_float(v[k].w);
-        }
-      }
-#pragma unroll 1
-      for (int o = g.R / 2; o > 0; o >>= 1)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) run[e] += __shfl_xor_sync(0xffffffffu, run[e], o);
-      if (wi < nitem && jr == 0)
-        *reinterpret_cast<float4*>(s_red + ss * g.row + u * 4) = make_float4(run[0], run[1], run[2], run[3]);
-    }
-    ok = __syncthreads_and(got);
-    if (!ok) break;
-    if (tid < HC) {
-      const float rr = rsqrt_nr(fmaf(s_red[tid * g.row + g.Qn], __fdividef(1.0f, static_cast<float>(HS)), c.eps));
-      s_rl[tid] = rr;
-      if (jn == 0) c.rrms[m * HC + tid] = rr;
-    }
-    __syncthreads();
-    const float inv_hc = 1.0f / static_cast<float>(HC);
-#pragma unroll 1
-    for (int qp = tid; qp < g.Qn / 2; qp += NT) {
-      float v[2];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int q = 2 * qp + e;
-        float a = 0.f;
-#pragma unroll 1
-        for (int ss = 0; ss < HC; ++ss) a += s_rl[ss] * s_red[ss * g.row + q];
-        v[e] = a;
-        const int n = jn * g.Qn + q;
-        if (n < r)
-          c.lora[static_cast<int64_t>(m) * r + n] = a;
-        else if (n < n_out)
-          c.inj_next[static_cast<int64_t>(m) * HC + (n - r)] = a;
-      }
-      const int n0 = jn * g.Qn + 2 * qp;
-      if (n0 < r) {   // r is even: n0 + 1 < r too
-        const float u0 = v[0] * inv_hc, u1 = v[1] * inv_hc;
-        st_relaxed_u32(gat + m * g.L2w + n0 / 2,
-                       pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1)));
-      }
-    }
-    if (jn == 0) {
-#pragma unroll 1
-      for (int i = r / 2 + tid; i < g.L2w; i += NT) {
-        const int ss = i - r / 2;
-        st_relaxed_u32(gat + m * g.L2w + i, ss < HC ? xword(s_rl[ss]) : 0u);
-      }
-    }
-    __syncthreads();   // s_red is reused by the next block
-  }
-  // empty this CTA's share of the copy the next call uses
-  {
-    uint4* nxt = reinterpret_cast<uint4*>(p.xgat + static_cast<size_t>(par ^ 1u) * p.gat_words);
-    const int nq = p.gat_words / 4;
-    const int per = (nq + g.G - 1) / g.G;
-#pragma unroll 1
-    for (int i = b * per + tid; i < min(nq, (b + 1) * per); i += NT)
-      nxt[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
-  }
-
-  // --- step 4: all-gather of h (into the swizzled operand layout) and rrms
-  if (ok && nc > 0) {
-    bool got = true;
-    const int hw = r / 2;
-    const int nq = M * g.L2w / 4;
-#pragma unroll 1
-    for (int i0 = tid; i0 < nq && got; i0 += XU * NT) {
-      uint4 v[XU];
-#pragma unroll
-      for (int k = 0; k < XU; ++k)
-        v[k] = i0 + k * NT < nq ? ld_relaxed_v4(gat + (i0 + k * NT) * 4) : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-      for (int k = 0; k < XU; ++k) {
-        const int i = i0 + k * NT;
-        if (i >= nq || !got) break;
-        if (!all_set(v[k])) {
-          v[k] = wait_words(gat + i * 4, p.err, limit);
-          if (!all_set(v[k])) { got = false; break; }
-        }
-        // r / 2 and L2w are multiples of 4: a quad is 8 h values or rrms/pad
-        const int m = (i * 4) / g.L2w, w0 = i * 4 - m * g.L2w;
-        if (w0 < hw) {
-          const int n0 = 2 * w0;                                  // 8 values from n0
-          const int q = n0 >> 6, un = (n0 & 63) >> 3;
-          *reinterpret_cast<uint4*>(smem + g.off_hb + q * Nu * 128 + m * 128 +
-                                    ((un ^ (m & 7)) << 4)) = v[k];
-        } else {
-          const uint32_t vv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            if (w0 + e < hw + HC) s_rr[m * HC + w0 + e - hw] = __uint_as_float(vv[e]);
-        }
-      }
-    }
-    // token rows past M, and h columns past r in the last chunk, are zero
-#pragma unroll 1
-    for (int i = tid; i < g.nchunk_u * Nu * 8; i += NT) {
-      const int q = i / (Nu * 8), rem = i - q * Nu * 8, m = rem >> 3, un = rem & 7;
-      if (m >= M || q * 64 + un * 8 >= r)
-        *reinterpret_cast<uint4*>(smem + g.off_hb + q * Nu * 128 + m * 128 + ((un ^ (m & 7)) << 4)) =
-            make_uint4(0u, 0u, 0u, 0u);
-    }
-    fence_proxy_async_smem();
-    ok = __syncthreads_and(got);
-  }
-  // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
-  // channel) of this CTA's range; lane 0 of warp 2k + 1 (k < ncu) issues
-  // chunks k, k + ncu, .. into its own accumulator copy (with a ring, ncu = 2
-  // and each of its two slots serves one issuer).  Every candidate thread
-  // commits barG.
-  const bool up_issued = ok && nc > 0;
-  if (up_issued) {
-    if ((tid & 63) == 32 && (tid >> 6) < UP_ISSUERS) {
-      const int me = tid >> 6;
-      tc_fence_after();
-      const uint32_t idesc = idesc_bf16(128, Nu);
-      bool okm = true;
-#pragma unroll 1
-      for (int q = me; q < nub && okm && me < g.ncu; q += g.ncu) {
-        const int slot = q % g.nsl_u;
-        const uint32_t ph = (q / g.nsl_u) & 1;
-        okm = mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns);
-        if (!okm) break;
-        tc_fence_after();
-        const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
-#pragma unroll 1
-        for (int tu = 0; tu < g.ntu; ++tu)
-#pragma unroll 1
-          for (int ks = 0; ks < 4; ++ks)
-            umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
-                      desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
-        umma_commit(free_u(slot));
-      }
-      if (!okm) *s_mma_ok = 0;
-      umma_commit(barG);
-    } else if (tid == 0) {
-#pragma unroll 1
-      for (int q = pre_u; q < nub; ++q) {
-        const int slot = q % g.nsl_u;
-        if (!wait_bar(free_u(slot), ((q / g.nsl_u) - 1) & 1, p.err, p.limit_ns)) break;
-        issue_u(q);
-        ++issued_u;
-      }
-    }
-    bool got = wait_bar(barG, 0, p.err, p.limit_ns);
-    tc_fence_after();
-    ok = __syncthreads_and(got && *s_mma_ok != 0);
-    if (ok) {
-      const int q4 = warp & 3, grp = warp >> 2;
-      const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
-      const int nmc = Nu / 8;
-#pragma unroll 1
-      for (int item = grp; item < g.ntu * nmc; item += NW / 4) {
-        const int tu = item / nmc, m0 = (item - tu * nmc) * 8;
-        const int i = tu * 128 + 32 * q4 + lane;               // row (stream, channel)
-        // sum of the issuers' accumulator copies that hold a chunk
-        const int ncopy = min(g.ncu, nub);
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) v[e] = 0.f;
-#pragma unroll 1
-        for (int k = 0; k < ncopy; k += 2) {
-          uint32_t v0[8], v1[8];
-          if (k + 1 < ncopy) {
-            tmem_ld8x2_wait(tl + (k * g.ntu + tu) * Nu + m0, tl + ((k + 1) * g.ntu + tu) * Nu + m0, v0, v1);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(v0[e]) + __uint_as_float(v1[e]);
+          // r / 2 and L2w are multiples of 4: a quad is 8 h values or rrms/pad
+          const int m = (i * 4) / g.L2w, w0 = i * 4 - m * g.L2w;
+          if (w0 < hw) {
+            const int n0 = 2 * w0;                                  // 8 values from n0
+            const int q = n0 >> 6, un = (n0 & 63) >> 3;
+            *reinterpret_cast<uint4*>(smem + g.u_hb + q * Nu * 128 + m * 128 +
+                                      ((un ^ (m & 7)) << 4)) = v[k];
           } else {
-            tmem_ld8_wait(tl + (k * g.ntu + tu) * Nu + m0, v0);
+            const uint32_t vv[4] = {v[k].x, v[k].y, v[k].z, v[k].w};
 #pragma unroll
-            for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(v0[e]);
+            for (int e = 0; e < 4; ++e)
+              if (w0 + e < hw + HC) s_rr[m * HC + w0 + e - hw] = __uint_as_float(vv[e]);
           }
         }
-        if (i < g.rows_u) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e)
-            if (m0 + e < M) s_g[(m0 + e) * g.rows_u + i] = sigmoid_fast(v[e]);
+      }
+      // token rows past M, and h columns past r in the last chunk, are zero
+#pragma unroll 1
+      for (int i = tid; i < g.nchunk_u * Nu * 8; i += NT) {
+        const int q = i / (Nu * 8), rem = i - q * Nu * 8, m = rem >> 3, un = rem & 7;
+        if (m >= M || q * 64 + un * 8 >= r)
+          *reinterpret_cast<uint4*>(smem + g.u_hb + q * Nu * 128 + m * 128 + ((un ^ (m & 7)) << 4)) =
+              make_uint4(0u, 0u, 0u, 0u);
+      }
+      fence_proxy_async_smem();
+      ok = __syncthreads_and(got);
+    }
+    if (tid == 0) HCGR_STAMP(9);
+    // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
+    // channel) of this CTA's range; lane 0 of warp 2k + 1 (k < ncu) issues
+    // chunks k, k + ncu, .. into its own accumulator copy (with a ring, ncu =
+    // 2 and each of its two slots serves one issuer).  Every candidate thread
+    // commits barG.
+    const uint32_t tmem = *s_tmem;
+    up_issued = ok && nc > 0;
+    if (up_issued) {
+      if ((tid & 63) == 32 && (tid >> 6) < UP_ISSUERS) {
+        const int me = tid >> 6;
+        tc_fence_after();
+        const uint32_t idesc = idesc_bf16(128, Nu);
+        bool okm = true;
+#pragma unroll 1
+        for (int q = me; q < nub && okm && me < g.ncu; q += g.ncu) {
+          const int slot = q % g.nsl_u;
+          const uint32_t ph = (q / g.nsl_u) & 1;
+          okm = mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns);
+          if (!okm) break;
+          tc_fence_after();
+          const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
+#pragma unroll 1
+          for (int tu = 0; tu < g.ntu; ++tu)
+#pragma unroll 1
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
+                        desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
+          umma_commit(free_u(slot));
+        }
+        if (!okm) *s_mma_ok = 0;
+        umma_commit(barG);
+      } else if (tid == 0) {
+#pragma unroll 1
+        for (int q = pre_u; q < nub; ++q) {
+          const int slot = q % g.nsl_u;
+          if (!wait_bar(free_u(slot), ((q / g.nsl_u) - 1) & 1, p.err, p.limit_ns)) break;
+          issue_u(q);
+          ++issued_u;
         }
       }
-      __syncthreads();
-      const float inv_hc = 1.0f / static_cast<float>(HC);
+      bool got = wait_bar(barG, 0, p.err, p.limit_ns);
+      tc_fence_after();
+      ok = __syncthreads_and(got && *s_mma_ok != 0);
+      if (tid == 0) HCGR_STAMP(10);
+      if (ok) {
+        const int q4 = warp & 3, grp = warp >> 2;
+        const uint32_t tl = tmem + (static_cast<uint32_t>(32 * q4) << 16);
+        const int nmc = Nu / 8;
+        const int ncopy = min(g.ncu, nub);   // issuers' accumulator copies that hold a chunk
 #pragma unroll 1
-      for (int i = tid; i < M * nc; i += NT) {
-        const int m = i / nc, cc = i - m * nc, ch = cp0 + cc;
-        float sum = 0.f;
+        for (int item = grp; item < g.ntu * nmc; item += NW / 4) {
+          const int tu = item / nmc, m0 = (item - tu * nmc) * 8;
+          const int i = tu * 128 + 32 * q4 + lane;               // row (stream, channel)
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) v[e] = 0.f;
 #pragma unroll 1
-        for (int ss = 0; ss < HC; ++ss) {
-          const float rv = bf16_to_f32(s_x3r[(m * HC + ss) * g.nc_max + cc]);
-          const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(bf16_to_f32(s_x3y[m * g.nc_max + cc]),
-                                                                s_iw[m * HC + ss], rv)))
-                                 : rv;
-          const float xn = r2 * s_rr[m * HC + ss] * (1.0f + bf16_to_f32(s_x3w[ss * g.nc_max + cc]));
-          sum = fmaf(s_g[m * g.rows_u + ss * g.nc_max + cc], xn, sum);
+          for (int k = 0; k < ncopy; k += 2) {
+            uint32_t v0[8], v1[8];
+            if (k + 1 < ncopy) {
+              tmem_ld8x2_wait(tl + (k * g.ntu + tu) * Nu + m0, tl + ((k + 1) * g.ntu + tu) * Nu + m0, v0, v1);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(v0[e]) + __uint_as_float(v1[e]);
+            } else {
+              tmem_ld8_wait(tl + (k * g.ntu + tu) * Nu + m0, v0);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] += __uint_as_float(v0[e]);
+            }
+          }
+          if (i < g.rows_u) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (m0 + e < M) s_g[(m0 + e) * g.rows_u + i] = sigmoid_fast(v[e]);
+          }
         }
-        c.x[static_cast<int64_t>(m) * HS + ch] = f32_to_bf16(sum * inv_hc);
+        __syncthreads();
+#pragma unroll 1
+        for (int i = tid; i < M * nc; i += NT) {
+          const int m = i / nc, cc = i - m * nc, ch = cp0 + cc;
+          float sum = 0.f;
+#pragma unroll 1
+          for (int ss = 0; ss < HC; ++ss) {
+            const float rv = bf16_to_f32(s_x3r[(m * HC + ss) * g.nc_max + cc]);
+            const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(bf16_to_f32(s_x3y[m * g.nc_max + cc]),
+                                                                  s_iw[m * HC + ss], rv)))
+                                   : rv;
+            const float xn = r2 * s_rr[m * HC + ss] * (1.0f + bf16_to_f32(s_x3w[ss * g.nc_max + cc]));
+            sum = fmaf(s_g[m * g.rows_u + ss * g.nc_max + cc], xn, sum);
+          }
+          c.x[static_cast<int64_t>(m) * HS + ch] = f32_to_bf16(sum * inv_hc);
+        }
       }
     }
+    if (tid == 0) HCGR_STAMP(11);
   }
 
   // Teardown: every copy this CTA issued lands and every MMA it issued
@@ -757,15 +812,16 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll 1
     for (int q = max(0, issued_u - g.nsl_u); q < issued_u; ++q)
       drain_bar(full_u(q % g.nsl_u), (q / g.nsl_u) & 1, limit);
-    drain_bar(barD, 0, limit);
+    if (down_issued) drain_bar(barD, 0, limit);
     if (up_issued) drain_bar(barG, 0, limit);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 3) {
     tc_fence_after();
-    tmem_dealloc(tmem, g.tmem_cols);
+    tmem_dealloc(*s_tmem, tmem_cols);
   }
+  if (tid == 0) HCGR_STAMP(12);
 }
 
 Call shape_call(int64_t M, int HC, int HS, int r) {
@@ -784,7 +840,7 @@ Call shape_call(int64_t M, int HC, int HS, int r) {
 size_t decode_xred_words(const Device& dev, int64_t M, int HC, int HS, int r) {
   Geom g;
   if (!make_geom(shape_call(M, HC, HS, r), dev, g)) return 0;
-  return static_cast<size_t>(g.nred) * g.G * g.row;
+  return static_cast<size_t>(g.nred) * g.Gd * g.row;
 }
 
 size_t decode_xgat_words(int n_out_max) {
@@ -804,7 +860,7 @@ cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
   prm.limit_ns = c.debug_fault ? 50ull * 1000 * 1000 : 1000ull * 1000 * 1000;
   if (!make_geom(c, dev, prm.g)) return cudaErrorNotSupported;
   const Geom& g = prm.g;
-  if (static_cast<size_t>(g.nred) * g.G * g.row > ws.xred_words ||
+  if (static_cast<size_t>(g.nred) * g.Gd * g.row > ws.xred_words ||
       static_cast<size_t>(c.M) * g.L2w > ws.xgat_words || ws.xgat_words % 4 != 0)
     return cudaErrorNotSupported;
   const uint64_t wstr[2] = {static_cast<uint64_t>(c.HS) * 2, static_cast<uint64_t>(c.K) * 2};
@@ -848,3 +904,19 @@ cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
 }
 
 }  // namespace hcgr
+
+#ifdef HCGR_TRACE
+// Copies the phase stamps of the last traced decode launch (n <= MAX_GRID *
+// 16 values, [CTA][16] in ns of %globaltimer) to host memory, then clears the
+// array, so that a slot no CTA of the next launch passes reads 0.
+extern "C" int hc_gr_trace_read(unsigned long long* host, int n) {
+  const size_t cap = sizeof(hcgr::g_trace) / sizeof(unsigned long long);
+  if (n < 0 || static_cast<size_t>(n) > cap) return static_cast<int>(cudaErrorInvalidValue);
+  cudaError_t e = cudaMemcpyFromSymbol(host, hcgr::g_trace, n * sizeof(unsigned long long));
+  if (e != cudaSuccess) return static_cast<int>(e);
+  void* dev = nullptr;
+  e = cudaGetSymbolAddress(&dev, hcgr::g_trace);
+  if (e == cudaSuccess) e = cudaMemset(dev, 0, sizeof(hcgr::g_trace));
+  return static_cast<int>(e);
+}
+#endif

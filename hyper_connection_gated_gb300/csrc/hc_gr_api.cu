@@ -88,6 +88,8 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   *out = nullptr;
   if (max_M < 1 || HC < 1 || HS < 1 || r < 1 || device < 0) return HC_GR_ERR_INVALID_ARG;
   if (HS % 8 != 0 || r % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
+  if (max_M > HC_GR_MAX_TOKENS || static_cast<int64_t>(HC) * HS > HC_GR_MAX_WIDTH)
+    return HC_GR_ERR_UNSUPPORTED;
   hc_gr_ctx* h = new (std::nothrow) hc_gr_ctx();
   if (!h) return HC_GR_ERR_CUDA;
   DeviceGuard guard(device);
@@ -127,6 +129,7 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   void* base = nullptr;
   e = cudaMalloc(&base, off);
   if (e != cudaSuccess) {
+    cudaGetLastError();   // leave no stale error for the caller's next CUDA call
     delete h;
     return HC_GR_ERR_CUDA;
   }
@@ -191,6 +194,7 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
     if (!aligned(p, 4)) return HC_GR_ERR_INVALID_ARG;
   if (HS % 8 != 0 || r % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
   const int64_t K = static_cast<int64_t>(HC) * HS;
+  if (M > HC_GR_MAX_TOKENS || K > HC_GR_MAX_WIDTH) return HC_GR_ERR_UNSUPPORTED;
   if (M > h->max_M || K > h->K_max || r + HC > h->n_out_max) return HC_GR_ERR_UNSUPPORTED;
   if (merged && a->n_pad < r + HC) return HC_GR_ERR_UNSUPPORTED;
   if (a->force_path == HC_GR_PATH_DECODE && M > hcgr::DECODE_MAX_M) return HC_GR_ERR_UNSUPPORTED;
@@ -274,6 +278,7 @@ int hc_gr_combine(hc_gr_handle h, int64_t M, int HC, int HS, const void* R, cons
     return HC_GR_ERR_INVALID_ARG;
   if (HS % 8 != 0) return HC_GR_ERR_UNSUPPORTED;
   const int64_t K = static_cast<int64_t>(HC) * HS;
+  if (M > HC_GR_MAX_TOKENS || K > HC_GR_MAX_WIDTH) return HC_GR_ERR_UNSUPPORTED;
   const Range out = span(R2, M * K * 2);
   if (overlap(out, span(R, M * K * 2)) || overlap(out, span(y, M * HS * 2)) ||
       overlap(out, span(inj, ((M - 1) * ld_inj + HC) * 4)))

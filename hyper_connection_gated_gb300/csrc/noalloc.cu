@@ -159,14 +159,37 @@ extern "C" int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps
   c.pdl = 0;
 
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  // The ticket and the status word start at zero and every exchange word
-  // empty on every call (the array keeps whatever the previous call left
-  // there, and a call that timed out can leave values behind).
-  if (cudaMemsetAsync(ws.base, 0, CTL_BYTES, s) != cudaSuccess) return HC_GR_ERR_CUDA;
+  // The ticket starts at zero and every exchange word empty on every call
+  // (the array keeps whatever the previous call left there, and a call that
+  // timed out can leave values behind).  The status word is kept: a timeout
+  // stays recorded until hc_gr_noalloc_check clears it.
+  if (cudaMemsetAsync(ws.base, 0, MAX_GRID * 8, s) != cudaSuccess) return HC_GR_ERR_CUDA;
   const size_t xbytes = reinterpret_cast<unsigned char*>(ws.lora) -
                         reinterpret_cast<unsigned char*>(ws.xred);
   if (cudaMemsetAsync(ws.xred, 0xff, xbytes, s) != cudaSuccess) return HC_GR_ERR_CUDA;
   const cudaError_t e = launch_decode(c, ws, pd.dev, s);
   if (e == cudaErrorNotSupported) return HC_GR_ERR_UNSUPPORTED;
   return e == cudaSuccess ? HC_GR_OK : HC_GR_ERR_CUDA;
+}
+
+extern "C" int hc_gr_noalloc_check(struct CUstream_st* stream) {
+  using namespace hcgr;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess || device < 0 || device >= MAX_DEVICES)
+    return HC_GR_ERR_CUDA;
+  unsigned char* scratch = nullptr;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_dev[device].ready) scratch = g_dev[device].scratch;
+  }
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return HC_GR_ERR_CUDA;
+  if (!scratch) return HC_GR_OK;   // no call on this device yet
+  int* err = reinterpret_cast<int*>(scratch + MAX_GRID * 8);
+  int status = DEV_OK;
+  if (cudaMemcpy(&status, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return HC_GR_ERR_CUDA;
+  if (status == DEV_OK) return HC_GR_OK;
+  if (cudaMemset(err, 0, sizeof(int)) != cudaSuccess) return HC_GR_ERR_CUDA;
+  return HC_GR_ERR_TIMEOUT;
 }

@@ -53,6 +53,10 @@
  * recorded in the handle and reported by hc_gr_check; the outputs of that
  * call, and of every later call on the handle until hc_gr_check has cleared
  * the status, are undefined.
+ *
+ * Size limits: M and max_M at most HC_GR_MAX_TOKENS, HC * HS at most
+ * HC_GR_MAX_WIDTH (UNSUPPORTED beyond), so that every element offset the
+ * kernels form stays inside their index types.
  */
 #ifndef HC_GR_H_
 #define HC_GR_H_
@@ -67,24 +71,41 @@ struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
 typedef struct hc_gr_ctx* hc_gr_handle;
 
+#define HC_GR_MAX_TOKENS (1LL << 30) /* largest M (and max_M) accepted */
+#define HC_GR_MAX_WIDTH (1LL << 30)  /* largest K = HC * HS accepted */
+
+/* Status codes.  The contract follows the page's "PR Self-Review", section
+ * "Behavior and intent": the public entry points refuse what they cannot
+ * compute correctly (unsupported architecture, widths the kernels cannot
+ * tile, malformed or aliased buffers) instead of returning wrong results;
+ * the review findings on strided injection and up-weight validation are
+ * honoured by explicit strides and checks rather than rejected. */
 typedef enum hc_gr_status {
   HC_GR_OK = 0,
   HC_GR_ERR_INVALID_ARG = 1, /* NULL pointer, M < 1, eps <= 0 or not finite,
                                 misaligned pointer, ld_inj < HC, bad path */
   HC_GR_ERR_UNSUPPORTED = 2, /* shape outside what the handle was created for,
-                                HS or r not a multiple of 8, n_pad < r + HC */
+                                HS or r not a multiple of 8, n_pad < r + HC,
+                                M or HC * HS above the size limits, a device
+                                that is not sm_103 */
   HC_GR_ERR_ALIAS = 3,       /* an output overlaps another output or an input */
   HC_GR_ERR_CUDA = 4,        /* a CUDA call failed (launch, allocation, copy) */
   HC_GR_ERR_TIMEOUT = 5      /* a device-side bounded wait expired */
 } hc_gr_status;
 
+/* Dispatch between the two kernel families (the page's "Behavior and intent":
+ * a skinny decode path for few tokens beside the tiled two-kernel path). */
 typedef enum hc_gr_path {
   HC_GR_PATH_AUTO = 0,    /* M <= 32: decode kernel, otherwise prefill kernels */
   HC_GR_PATH_DECODE = 1,  /* weight-streaming persistent kernel, M <= 32 */
   HC_GR_PATH_PREFILL = 2  /* tensor-core (tcgen05) two-stage kernels */
 } hc_gr_path;
 
-/* Full argument set of hc_gr_forward_ex.  Zero-initialise, then fill. */
+/* Full argument set of hc_gr_forward_ex.  Zero-initialise, then fill.
+ * Wdi / n_pad / fold_w: the merged down/inject weight of the page's
+ * "Performance" setup (336 rows with (1 + w) folded in); ld_inj: the strided
+ * injection the review found a kernel ignoring ("Validation and unverified
+ * scope": the strided combine case). */
 typedef struct hc_gr_args {
   int64_t M;
   int32_t HC, HS, r;
@@ -125,24 +146,30 @@ typedef struct hc_gr_args {
 
 /* Creates a handle bound to `device` and allocates its workspace for calls
  * with M <= max_M, HC * HS <= the given HC * HS and r + HC <= the given
- * r + HC.  Queries the device (SM count, shared memory) once.
+ * r + HC.  Queries the device (SM count, shared memory) once.  (The page's
+ * op keeps per-device state -- its skinny decode's arrival counters, "PR
+ * Self-Review" -- in a process-wide cache; here that state is the handle's.)
  * Returns INVALID_ARG for out == NULL or non-positive sizes, UNSUPPORTED for
- * a device that is not sm_103, CUDA when allocation fails (*out is then
- * NULL). */
+ * max_M or HC * HS above the size limits or a device that is not sm_103,
+ * CUDA when the device query or the allocation fails (*out is then NULL in
+ * every failure). */
 int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, int r);
 
 /* The whole forward pass for one batch of M tokens with separate, unfolded
- * Wd and Wi (see the layouts above).  lora may be NULL.  Asynchronous on
- * `stream`. */
+ * Wd and Wi (see the layouts above): the (COMBINE), (N), (G1), (INJ), (G2)
+ * and (MIX) bullets of the page's "Technical Details" in one call -- its
+ * combine_and_mix entry point ("Behavior and intent").  lora may be NULL.
+ * Asynchronous on `stream`. */
 int hc_gr_forward(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps,
                   const void* R, const void* y, const float* inj, const void* Wnorm,
                   const void* Wd, const void* Wi, const void* Wu,
                   void* R2, float* rrms, float* inj_next, void* x, float* lora,
                   struct CUstream_st* stream);
 
-/* Same operation with every option: a merged (optionally folded) weight, a
- * strided inj and a forced path.  With y, inj and R2 all NULL the call is
- * the mix alone (see hc_gr_mix); NULL in only some of them is INVALID_ARG. */
+/* Same operation ("Technical Details", as hc_gr_forward) with every option:
+ * a merged (optionally folded) weight, a strided inj and a forced path.
+ * With y, inj and R2 all NULL the call is the mix alone (see hc_gr_mix);
+ * NULL in only some of them is INVALID_ARG. */
 int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* stream);
 
 /* COMBINE alone (the page's combine-only entry point, "Behavior and intent";
@@ -173,18 +200,23 @@ int hc_gr_mix(hc_gr_handle h, int64_t M, int HC, int HS, int r, float eps, const
 
 /* Waits for `stream`, then returns the device status recorded by the
  * handle's kernels since the last check (HC_GR_OK or HC_GR_ERR_TIMEOUT).
+ * The status comes from the bounded cross-CTA waits that replace the page's
+ * skinny-decode arrival counters ("Behavior and intent"); a wait that
+ * expires reports instead of hanging.
  * After a TIMEOUT it clears the status and resets the exchange buffers and
  * the call ticket, so the handle is usable again.  Returns HC_GR_ERR_CUDA if
  * the stream reports a CUDA error. */
 int hc_gr_check(hc_gr_handle h, struct CUstream_st* stream);
 
-/* Releases the workspace.  Waits for the device first.  NULL is a no-op. */
+/* Releases the workspace.  Waits for the device first.  NULL is a no-op.
+ * (No counterpart on the pages: their op owns no handle.) */
 int hc_gr_destroy(hc_gr_handle h);
 
-/* Static text for a status code. */
+/* Static text for a status code.  (No counterpart on the pages.) */
 const char* hc_gr_strerror(int status);
 
-/* Text of the last CUDA error seen by this handle (static storage). */
+/* Text of the last CUDA error seen by this handle (static storage).  (No
+ * counterpart on the pages.) */
 const char* hc_gr_last_cuda_error(hc_gr_handle h);
 
 /* hc_gr_forward without a handle and without any device allocation.  The
@@ -204,9 +236,11 @@ const char* hc_gr_last_cuda_error(hc_gr_handle h);
  *     capture.
  *   - Every call shares the one array: calls that overlap on the GPU (on
  *     different streams, or on several host threads) race and corrupt each
- *     other.  Each call first clears the ticket and the status word and
- *     empties the exchange buffers (two memsets on `stream`); a device-side
- *     timeout ends the kernel but is not reported here.
+ *     other.  Each call first empties the exchange buffers and clears the
+ *     call ticket (memsets on `stream`); the status word is left as it is,
+ *     so a device-side timeout of any call stays recorded until
+ *     hc_gr_noalloc_check reads and clears it (as with a handle, the outputs
+ *     of the failed call and of every later call until then are undefined).
  *   - Allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  *     routine.  Asynchronous on `stream`. */
 int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps,
@@ -214,6 +248,15 @@ int hc_gr_forward_noalloc(int64_t M, int HC, int HS, int r, float eps,
                           const void* Wd, const void* Wi, const void* Wu,
                           void* R2, float* rrms, float* inj_next, void* x, float* lora,
                           struct CUstream_st* stream);
+
+/* Status of the hc_gr_forward_noalloc calls on the current device.  The pages
+ * have no counterpart.  Waits for `stream`, then reads the status word in the
+ * fixed scratch array: HC_GR_OK, or HC_GR_ERR_TIMEOUT if a device-side bounded
+ * wait of any call since the last check expired (the outputs of those calls
+ * are undefined); a TIMEOUT is cleared by the check.  HC_GR_OK before the
+ * first call on the device.  HC_GR_ERR_CUDA if the stream reports an error.
+ * Allocates nothing. */
+int hc_gr_noalloc_check(struct CUstream_st* stream);
 
 #ifdef __cplusplus
 }

@@ -57,6 +57,11 @@ def test_strerror_and_null_handles(lib):
     assert lib.hc_gr_create(ctypes.byref(h), 0, 0, 4, 2560, 320) == _native.ERR_INVALID_ARG
     assert lib.hc_gr_create(ctypes.byref(h), 0, 8, 4, 2561, 320) == _native.ERR_UNSUPPORTED
     assert h.value is None
+    # the size limits are checked before any CUDA call
+    assert lib.hc_gr_create(ctypes.byref(h), 0, _native.MAX_TOKENS + 1, 4, 2560, 320) == \
+        _native.ERR_UNSUPPORTED
+    assert lib.hc_gr_create(ctypes.byref(h), 0, 8, 2, (1 << 29) + 8, 320) == _native.ERR_UNSUPPORTED
+    assert h.value is None
 
 
 def test_args_struct_matches_header_layout(root):
@@ -114,6 +119,9 @@ int main(void) {
     printf("%s -> %d (want %d)\n", #call, st_, (want)); ++fails; } } while (0)
   EXPECT(hc_gr_create(NULL, 0, 8, 4, 2560, 320), HC_GR_ERR_INVALID_ARG);
   EXPECT(hc_gr_create(&h, 0, 0, 4, 2560, 320), HC_GR_ERR_INVALID_ARG);
+  EXPECT(hc_gr_create(&h, 0, HC_GR_MAX_TOKENS + 1, 4, 2560, 320), HC_GR_ERR_UNSUPPORTED);
+  EXPECT(hc_gr_forward_noalloc(0, 4, 2560, 320, 1e-6f, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
+                               NULL, NULL, NULL, NULL, NULL, NULL), HC_GR_ERR_INVALID_ARG);
   EXPECT(hc_gr_forward_ex(NULL, &a, NULL), HC_GR_ERR_INVALID_ARG);
   EXPECT(hc_gr_forward(NULL, 4, 4, 2560, 320, 1e-6f, NULL, NULL, NULL, NULL, NULL, NULL, NULL,
                        NULL, NULL, NULL, NULL, NULL, NULL), HC_GR_ERR_INVALID_ARG);

@@ -4,7 +4,7 @@ import ctypes
 
 import pytest
 
-from hyper_connection_gated_gb300 import (ERR_ALIAS, ERR_INVALID_ARG, ERR_TIMEOUT,
+from hyper_connection_gated_gb300 import (ERR_ALIAS, ERR_CUDA, ERR_INVALID_ARG, ERR_TIMEOUT,
                                           ERR_UNSUPPORTED, OK, PATH_DECODE, HcGatedResidual,
                                           HcGrError, _native, inputs)
 
@@ -175,3 +175,27 @@ def test_prepared_call_rejects_like_forward(env):
     with pytest.raises(HcGrError) as ei:
         op.launch(args, torch.cuda.current_stream().cuda_stream)
     assert ei.value.status == ERR_INVALID_ARG
+
+
+def test_size_limits_and_allocation_failure(env):
+    # Sizes above the limits are refused on the host; a handle within them
+    # whose workspace cannot be allocated (max_M = 2^30 tokens needs several
+    # TB) reports a CUDA error and returns no handle; nothing is launched and
+    # the device stays usable.
+    torch, case, d, op = env
+    lib = _native.lib()
+    h = ctypes.c_void_p()
+    assert lib.hc_gr_create(ctypes.byref(h), 0, _native.MAX_TOKENS + 1, 4, 2560, 320) == ERR_UNSUPPORTED
+    assert h.value is None
+    assert lib.hc_gr_create(ctypes.byref(h), 0, 8, 2, (1 << 29) + 8, 320) == ERR_UNSUPPORTED
+    assert h.value is None
+    assert lib.hc_gr_create(ctypes.byref(h), 0, _native.MAX_TOKENS, 4, 2560, 320) == ERR_CUDA
+    assert h.value is None
+    a, out = _args(torch, d)
+    a.M = _native.MAX_TOKENS + 1
+    assert _run(op, torch, a) == ERR_UNSUPPORTED
+    a, out = _args(torch, d)
+    assert _run(op, torch, a) == OK
+    assert op.check_status(torch.cuda.current_stream().cuda_stream) == OK
+    tl.assert_parity(out, tl.oracle_ref(case))
+    torch.zeros(4, device="cuda").sum().item()     # torch sees no stale CUDA error
