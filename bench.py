@@ -805,9 +805,11 @@ def entry_sweep(reps: int = 5):
 TRACE_PHASES = {0: "start", 1: "prologue done", 2: "previous kernel done", 3: "COMBINE done",
                 4: "issuer 0: boxes landed, MMAs issued", 5: "down MMAs complete",
                 6: "pieces written", 7: "first block gathered", 8: "blocks reduced, h published",
-                9: "h gathered", 10: "gate MMAs complete", 11: "x stored", 12: "end"}
-DOWN_PHASES = (0, 1, 2, 3, 4, 5, 6, 12)
-UP_PHASES = (0, 1, 2, 7, 8, 9, 10, 11, 12)
+                9: "h gathered", 10: "gate MMAs complete", 11: "x stored", 12: "end",
+                13: "prologue barrier passed", 14: "thread 0: first box issued",
+                15: "issuer 0: gate MMAs issued"}
+DOWN_PHASES = (0, 13, 14, 1, 2, 3, 4, 5, 6, 12)
+UP_PHASES = (0, 13, 14, 1, 2, 7, 8, 9, 15, 10, 11, 12)
 
 
 def decode_trace(args):
@@ -816,9 +818,10 @@ def decode_trace(args):
     after 5 warm-up calls, each on one of several weight+input sets whose
     total exceeds twice the L2 (so the weights come from HBM); plain launches,
     or with --trace-pdl each traced call chained after a previous decode call
-    by programmatic dependent launch.  Prints, per phase and role, the
-    min / median / max over CTAs of the time since the grid's first CTA
-    started (µs), each the median over the traced calls."""
+    by programmatic dependent launch; --trace-hot uses one weight set, which
+    stays in L2.  Prints, per phase and role, the min / median / max over the
+    CTAs that passed it of the time since the grid's first CTA started (µs),
+    each the median over the traced calls."""
     import ctypes
 
     import numpy as np
@@ -838,7 +841,7 @@ def decode_trace(args):
     dev = torch.cuda.current_device()
     l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
     wbytes = 2 * (shape.r + shape.HC) * shape.K + 2 * shape.K * shape.r
-    nsets = max(3, int(np.ceil(2.0 * l2 / wbytes)) + 1)
+    nsets = 1 if args.trace_hot else max(3, int(np.ceil(2.0 * l2 / wbytes)) + 1)
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
@@ -872,7 +875,8 @@ def decode_trace(args):
                     live = st[st[:, 0] > 0]
                     t0 = live[:, 0].min()
                     rows = live[live[:, sel] > 0]
-                    per_run.append({ph: ((rows[:, ph] - t0) / 1e3) for ph in phases})
+                    # a phase some CTAs do not pass (no reducer block) keeps 0 there
+                    per_run.append({ph: ((rows[rows[:, ph] > 0][:, ph] - t0) / 1e3) for ph in phases})
                 table[role] = {
                     TRACE_PHASES[ph]: [round(float(np.median([np.min(r[ph]) for r in per_run])), 2),
                                        round(float(np.median([np.median(r[ph]) for r in per_run])), 2),
@@ -881,14 +885,14 @@ def decode_trace(args):
                 table[role + "_ctas"] = int(len(runs[-1][(runs[-1][:, 0] > 0) & (runs[-1][:, sel] > 0)]))
             report[str(M)] = table
             print(f"M={M} ({'chained by programmatic dependent launch' if args.trace_pdl else 'plain launch'}, "
-                  f"weights from HBM): µs since the first CTA started, min / median / max over CTAs, "
-                  f"median of {args.calls} calls")
+                  f"weights {'L2-resident' if args.trace_hot else 'from HBM'}): µs since the first CTA "
+                  f"started, min / median / max over CTAs, median of {args.calls} calls")
             for role in ("down", "up"):
                 print(f"  {role} CTAs ({table[role + '_ctas']}):")
                 for name, v in table[role].items():
                     print(f"    {name:40s} {v[0]:7.2f} {v[1]:7.2f} {v[2]:7.2f}")
     print(json.dumps({"decode_trace": report, "shape": [shape.HC, shape.HS, shape.r],
-                      "pdl": bool(args.trace_pdl)}))
+                      "pdl": bool(args.trace_pdl), "hot": bool(args.trace_hot)}))
 
 
 def main():
@@ -909,6 +913,7 @@ def main():
                     help="phase timeline of the decode kernel (diagnostic build)")
     ap.add_argument("--trace-M", default="1,8,32")
     ap.add_argument("--trace-pdl", action="store_true")
+    ap.add_argument("--trace-hot", action="store_true")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -50,9 +50,9 @@
 // Weights move as TMA boxes issued first thing in the kernel; when they do not
 // all fit in shared memory they stream through rings whose slots the MMA
 // threads hand back with tcgen05.commit.  Every CTA allows the next kernel in
-// the stream to launch right after its prologue: that kernel's CTAs take the
-// SMs the down CTAs leave and start their own weight copies while this call's
-// up CTAs finish.  With a programmatic dependent launch the weight copies
+// the stream to launch early (once its call-ticket arrival is performed):
+// that kernel's CTAs take the SMs the down CTAs leave and start their own
+// weight copies while this call's up CTAs finish.  With a programmatic dependent launch the weight copies
 // start before the previous kernel in the stream has finished; activations
 // and exchange buffers are touched, and outputs written, only after it has.
 // The kernel is short enough that instruction fetch matters: loops stay
@@ -338,6 +338,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     *s_mma_ok = 1;
   }
   __syncthreads();
+  if (tid == 0) HCGR_STAMP(13);
   if (lane == 0) {
     const int npre = down ? pre_w : pre_u;
     if (warp < npre) prefetch_tmap(down ? &p.tm_w : &p.tm_wu);
@@ -345,13 +346,19 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     for (int k = warp; k < npre; k += NW) {
       if (down) issue_w(k);
       else issue_u(k);
+      if (tid == 0 && k == 0) HCGR_STAMP(14);
     }
   } else if (warp == NW - 1 && lane == 1) {
     // arrivals in the low half, the call's epoch in the high half; the last
-    // arrival moves the epoch on and clears the count
+    // arrival moves the epoch on and clears the count.  Both atomics are
+    // performed before this thread reaches the CTA barrier that precedes the
+    // trigger of the next launch (below), so no arrival of the next call can
+    // come between this call's arrivals and its roll-over.
     const unsigned long long old = atomicAdd(p.ticket, 1ull);
-    if ((old & 0xffffffffull) == static_cast<unsigned long long>(g.G - 1))
+    if ((old & 0xffffffffull) == static_cast<unsigned long long>(g.G - 1)) {
       atomicAdd(p.ticket, (1ull << 32) - static_cast<unsigned long long>(g.G));
+      __threadfence();
+    }
     *s_epoch = static_cast<uint32_t>(old >> 32);
   }
   const int tmem_cols = down ? g.tmem_d : g.tmem_u;
@@ -361,10 +368,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     tmem_relinquish();
   }
   if (tid == 0) HCGR_STAMP(1);
-  // Every CTA of this grid is running: the next kernel in the stream may
-  // launch (its CTAs wait for SMs this grid frees, then for this grid's end
-  // before they touch activations or exchange buffers).
-  grid_dep_launch();
   // inputs, outputs and exchange buffers may belong to the previous kernel
   grid_dep_wait();
   if (tid == 0) HCGR_STAMP(2);
@@ -427,6 +430,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     __syncthreads();
     tc_fence_after();
     if (tid == 0) HCGR_STAMP(3);
+    // This CTA's call-ticket arrival is performed (the barrier above follows
+    // it): the next kernel in the stream may launch.  Its CTAs wait for SMs
+    // this grid frees, then for this grid's end before they touch
+    // activations or exchange buffers.
+    grid_dep_launch();
     const uint32_t tmem = *s_tmem;
 
     // --- step 2: the down/inject products on the tensor cores: lane 0 of
@@ -555,6 +563,10 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         }
       }
     }
+    // the call ticket's arrival (warp 15) is performed past this barrier:
+    // the next kernel in the stream may launch (see the down role)
+    __syncthreads();
+    grid_dep_launch();
     const uint32_t par = *s_epoch & 1u;
     uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
 
@@ -736,6 +748,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
                         desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
           umma_commit(free_u(slot));
         }
+        if (me == 0) HCGR_STAMP(15);
         if (!okm) *s_mma_ok = 0;
         umma_commit(barG);
       } else if (tid == 0) {
