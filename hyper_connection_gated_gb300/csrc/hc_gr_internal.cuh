@@ -396,6 +396,38 @@ __device__ __forceinline__ bool xwait4(const uint32_t* p, uint4& v, int* err, lo
   }
 }
 
+// Per-call counters of the decode kernel's exchanges (32-bit, in the
+// control block after the ticket, so every reset of the ticket clears them):
+// a producer CTA makes its data visible, then adds 1 with release semantics;
+// a consumer thread waits (acquire) until the count is complete, then its
+// CTA reads the data once.
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Waits (bounded) until *p >= target, polling with a short sleep between
+// reads so that a few pollers do not crowd the L2 slice the producers'
+// updates go to.  Gives up when the status word reports an error elsewhere or
+// after the time limit (then it reports the timeout itself).
+__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target, int* err,
+                                           long long limit) {
+  if (ld_acquire_u32(p) >= target) return true;
+  const long long t0 = clock64();
+  while (true) {
+    __nanosleep(32);
+    if (ld_acquire_u32(p) >= target) return true;
+    if (*((volatile int*)err) != DEV_OK) return false;
+    if (clock64() - t0 > limit) {
+      atomicCAS(err, DEV_OK, DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 // Programmatic dependent launch: wait for the grid this one depends on (a
 // no-op without that dependency), and let the next grid start launching.
 __device__ __forceinline__ void grid_dep_wait() {
