@@ -34,15 +34,14 @@
 //      range on the tensor cores (its Wu rows landed meanwhile), rebuilds xn
 //      from R2 (recomputed from R, y and inj bit-identically to step 1), rrms
 //      and Wnorm, and stores x = (1 / HC) sum_s G * xn.
-// The exchanges need no grid barrier.  Each has a per-call counter: a
-// producer CTA writes its data, fences, and adds 1 (release); one thread of a
-// consumer CTA waits (acquire, bounded in time, with a short sleep between
-// polls) until the count is complete, and then the CTA reads the data once.
-// Polling one word from one thread per CTA leaves the L2 free for the
-// producers' stores (many threads spinning on the data words themselves
-// delayed those stores by microseconds).  The counters alternate between two
-// copies by call parity (a ticket counter); each call clears the copies the
-// next call will use.
+// The exchanges need no grid barrier.  Every 32-bit word of an exchange
+// buffer is either the empty marker 0xffffffff or a value, and a reader spins
+// (bounded in time) on each word until it holds a value.  A value never equals
+// the marker: floats are stored with NaN canonicalised, and h as a pair of
+// bf16 from the rounding conversion, whose NaN is 0x7fff.  The reduce-scatter
+// buffer is emptied again by its single reader; the all-gather buffer
+// alternates between two copies by call parity (a ticket counter), and each
+// call empties the copy the next call will use.
 //
 // Without y (the mix alone) steps 1 and 5 take R as R2 and nothing is stored
 // for it; the Wnorm slice of stream s starts at s * ld_wnorm (0 when one [HS]
@@ -246,10 +245,11 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long 
   while (!mbar_try_wait(bar, parity) && clock64() - t0 < limit) {
   }
 }
-// An exchange counter, waited for (see wait_count).
-__device__ __noinline__ bool wait_counter(const unsigned* p, unsigned target, int* err,
-                                          long long limit) {
-  return wait_count(p, target, err, limit);
+// Four exchange words, waited for; on failure some word is still empty.
+__device__ __noinline__ uint4 wait_words(const uint32_t* p, int* err, long long limit) {
+  uint4 v;
+  xwait4(p, v, err, limit);
+  return v;
 }
 
 #ifdef HCGR_TRACE
@@ -297,10 +297,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 272);
   uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + 276);
   int* s_mma_ok = reinterpret_cast<int*>(smem + 280);
-  // exchange counters, two copies each (by call parity): down CTAs whose
-  // pieces are written, reducer CTAs whose h is published
-  unsigned* cnt_piece = reinterpret_cast<unsigned*>(p.ticket) + 32;   // byte 128 of the block
-  unsigned* cnt_h = reinterpret_cast<unsigned*>(p.ticket) + 64;       // byte 256
 
   // this CTA's work: the down slice, or the up channel range
   const int s = down ? b / g.P : 0;
@@ -500,9 +496,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       for (int j = tid; j < g.nred; j += NT) {
         const int m = j / g.Jm, jn = j - m * g.Jm;
         uint32_t* dst = p.xred + (static_cast<size_t>(j) * g.Gd + b) * g.row;
-        *reinterpret_cast<uint4*>(dst + g.Qn) = make_uint4(__float_as_uint(s_ssum[m]), 0u, 0u, 0u);
+        st_relaxed_v4(dst + g.Qn, make_uint4(xword(s_ssum[m]), 0u, 0u, 0u));
 #pragma unroll 1
-        for (int q = n_out - jn * g.Qn; q < g.Qn; ++q) dst[q] = 0u;
+        for (int q = n_out - jn * g.Qn; q < g.Qn; ++q) st_relaxed_u32(dst + q, 0u);
       }
     }
     // the products, straight from TMEM (hi + lo halves): warp w reads lanes
@@ -531,16 +527,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
           for (int e = 0; e < 8; ++e) {
             const float v = __uint_as_float(h0[e]) + __uint_as_float(l0[e]);
             if (m0 + e < M)
-              p.xred[(static_cast<size_t>((m0 + e) * g.Jm + jn) * g.Gd + b) * g.row + qn] =
-                  __float_as_uint(v);
+              st_relaxed_u32(p.xred + (static_cast<size_t>((m0 + e) * g.Jm + jn) * g.Gd + b) * g.row + qn,
+                             xword(v));
           }
         }
       }
     }
-    // every piece of this CTA is visible at GPU scope before it is counted
-    __threadfence();
-    __syncthreads();
-    if (tid == 0 && ok && !dead) red_release_add(cnt_piece + (*s_epoch & 1u), 1u);
     if (tid == 0) HCGR_STAMP(6);
   } else {
     // ======================================================== up role
@@ -582,29 +574,17 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     __syncthreads();
     grid_dep_launch();
     const uint32_t par = *s_epoch & 1u;
-    uint32_t* gat = p.xgat;
-    // the counters the next call uses start at zero (the next call touches
-    // them only after this one has finished)
-    if (u_idx == 0 && tid == 0) {
-      cnt_piece[par ^ 1u] = 0u;
-      cnt_h[par ^ 1u] = 0u;
-    }
-    const int nred_ctas = min(g.Gu, g.nred);   // up CTAs that reduce a block
+    uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
 
-    // --- step 4: the reducer of blocks u, u + Gu, ...: once every down CTA
-    // has counted its pieces, work item (stream, quad, sub-range) sums quad uq
-    // of the stream's pieces in its sub-range, XU loads in flight; the R
-    // sub-ranges of one (stream, quad) sit in consecutive lanes and fold with
-    // a fixed shuffle tree (deterministic).
-    if (u_idx < g.nred) {
-      bool got = true;
-      if (tid == 0) got = wait_counter(cnt_piece + par, static_cast<unsigned>(g.Gd), p.err, limit);
-      ok = __syncthreads_and(got);
-    }
+    // --- step 4: the reducer of blocks u, u + Gu, ...  Work item (stream,
+    // quad, sub-range) sums quad uq of the stream's pieces in its sub-range,
+    // XU loads in flight; the R sub-ranges of one (stream, quad) sit in
+    // consecutive lanes and fold with a fixed shuffle tree (deterministic).
 #pragma unroll 1
     for (int j = u_idx; j < g.nred && ok; j += g.Gu) {
       const int m = j / g.Jm, jn = j - m * g.Jm;
       const uint32_t* blk = p.xred + static_cast<size_t>(j) * g.Gd * g.row;
+      bool got = true;
       const int nitem = HC * g.nquad * g.R;
 #pragma unroll 1
       for (int wi0 = 0; wi0 < nitem; wi0 += NT) {            // uniform: whole warps shuffle
@@ -614,7 +594,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         const int p0 = jr * g.ppr, p1 = wi < nitem ? min(g.P, p0 + g.ppr) : p0;
         float run[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
-        for (int pp0 = p0; pp0 < p1; pp0 += XU) {
+        for (int pp0 = p0; pp0 < p1 && got; pp0 += XU) {
           uint4 v[XU];
 #pragma unroll
           for (int k = 0; k < XU; ++k)
@@ -622,7 +602,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
                                 : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
           for (int k = 0; k < XU; ++k) {
-            if (pp0 + k >= p1) break;
+            if (pp0 + k >= p1 || !got) break;
+            const uint32_t* src = blk + (ss * g.P + pp0 + k) * g.row + uq * 4;
+            if (!all_set(v[k])) {
+              v[k] = wait_words(src, p.err, limit);
+              if (!all_set(v[k])) { got = false; break; }
+            }
             run[0] += __uint_as_float(v[k].x);
             run[1] += __uint_as_float(v[k].y);
             run[2] += __uint_as_float(v[k].z);
@@ -636,7 +621,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         if (wi < nitem && jr == 0)
           *reinterpret_cast<float4*>(s_red + ss * g.row + uq * 4) = make_float4(run[0], run[1], run[2], run[3]);
       }
-      __syncthreads();
+      ok = __syncthreads_and(got);
+      if (!ok) break;
       if (tid == 0 && j == u_idx) HCGR_STAMP(7);
       if (tid < HC) {
         const float rr = rsqrt_nr(fmaf(s_red[tid * g.row + g.Qn], __fdividef(1.0f, static_cast<float>(HS)), c.eps));
@@ -663,24 +649,20 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         const int n0 = jn * g.Qn + 2 * qp;
         if (n0 < r) {   // r is even: n0 + 1 < r too
           const float u0 = v[0] * inv_hc, u1 = v[1] * inv_hc;
-          gat[m * g.L2w + n0 / 2] = pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1));
+          st_relaxed_u32(gat + m * g.L2w + n0 / 2,
+                         pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1)));
         }
       }
       if (jn == 0) {
 #pragma unroll 1
         for (int i = r / 2 + tid; i < g.L2w; i += NT) {
           const int ss = i - r / 2;
-          gat[m * g.L2w + i] = ss < HC ? __float_as_uint(s_rl[ss]) : 0u;
+          st_relaxed_u32(gat + m * g.L2w + i, ss < HC ? xword(s_rl[ss]) : 0u);
         }
       }
       __syncthreads();   // s_red is reused by the next block
     }
-    // this CTA's h and rrms are visible at GPU scope before they are counted
-    if (u_idx < g.nred) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0 && ok) red_release_add(cnt_h + par, 1u);
-    }
+    const bool red_done = ok;   // every block of this CTA read (and reduced)
     if (tid == 0) HCGR_STAMP(8);
     // the final mix's inputs (copied since the prologue) have landed; iw from
     // inj (each thread converts the words it copied)
@@ -688,18 +670,13 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll 1
     for (int i = tid; i < M * HC; i += NT) s_iw[i] = has_y ? combine_weight(s_iw[i], inv_hc) : 0.f;
 
-    // --- step 5: all-gather of h (into the swizzled operand layout) and
-    // rrms, once every reducer CTA has counted its blocks
+    // --- step 5: all-gather of h (into the swizzled operand layout) and rrms
     if (ok && nc > 0) {
       bool got = true;
-      if (tid == 0) got = wait_counter(cnt_h + par, static_cast<unsigned>(nred_ctas), p.err, limit);
-      ok = __syncthreads_and(got);
-    }
-    if (ok && nc > 0) {
       const int hw = r / 2;
       const int nq = M * g.L2w / 4;
 #pragma unroll 1
-      for (int i0 = tid; i0 < nq; i0 += XU * NT) {
+      for (int i0 = tid; i0 < nq && got; i0 += XU * NT) {
         uint4 v[XU];
 #pragma unroll
         for (int k = 0; k < XU; ++k)
@@ -707,7 +684,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 #pragma unroll
         for (int k = 0; k < XU; ++k) {
           const int i = i0 + k * NT;
-          if (i >= nq) break;
+          if (i >= nq || !got) break;
+          if (!all_set(v[k])) {
+            v[k] = wait_words(gat + i * 4, p.err, limit);
+            if (!all_set(v[k])) { got = false; break; }
+          }
           // r / 2 and L2w are multiples of 4: a quad is 8 h values or rrms/pad
           const int m = (i * 4) / g.L2w, w0 = i * 4 - m * g.L2w;
           if (w0 < hw) {
@@ -732,7 +713,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
               make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
-      __syncthreads();
+      ok = __syncthreads_and(got);
     }
     if (tid == 0) HCGR_STAMP(9);
     // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
@@ -830,6 +811,25 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       }
     }
     if (tid == 0) HCGR_STAMP(11);
+    // Off the critical path: empty the reduce-scatter blocks this CTA read
+    // (when a wait failed instead, hc_gr_check resets them) and this CTA's
+    // share of the all-gather copy the next call uses.
+    if (red_done) {
+#pragma unroll 1
+      for (int j = u_idx; j < g.nred; j += g.Gu) {
+        uint4* blk = reinterpret_cast<uint4*>(p.xred + static_cast<size_t>(j) * g.Gd * g.row);
+#pragma unroll 1
+        for (int i = tid; i < g.Gd * g.row / 4; i += NT) blk[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
+      }
+    }
+    {
+      uint4* nxt = reinterpret_cast<uint4*>(p.xgat + static_cast<size_t>(par ^ 1u) * p.gat_words);
+      const int nq = p.gat_words / 4;
+      const int per = (nq + g.Gu - 1) / g.Gu;
+#pragma unroll 1
+      for (int i = u_idx * per + tid; i < min(nq, (u_idx + 1) * per); i += NT)
+        nxt[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
+    }
   }
 
   // Teardown: every copy this CTA issued lands and every MMA it issued

@@ -375,55 +375,26 @@ __device__ __forceinline__ bool all_set(const uint4& v) {
 __device__ __forceinline__ uint32_t xword(float v) {
   return v != v ? 0x7fc00000u : __float_as_uint(v);
 }
-// Spin (bounded) until four consecutive exchange words all hold values.
-// Gives up when the status word reports an error elsewhere or after the time
-// limit (then it reports the timeout itself).
+// Spin (bounded) until four consecutive exchange words all hold values,
+// sleeping briefly between reads: many waiters reading the words back to back
+// crowd the L2 slice the producers' stores go to and delay them by
+// microseconds.  Gives up when the status word reports an error elsewhere or
+// after the time limit (then it reports the timeout itself).
 __device__ __forceinline__ bool xwait4(const uint32_t* p, uint4& v, int* err, long long limit) {
   v = ld_relaxed_v4(p);
   if (all_set(v)) return true;
   const long long t0 = clock64();
   uint32_t it = 0;
   while (true) {
+    __nanosleep(96);
     v = ld_relaxed_v4(p);
     if (all_set(v)) return true;
-    if ((++it & 15u) == 0) {
+    if ((++it & 7u) == 0) {
       if (*((volatile int*)err) != DEV_OK) return false;
       if (clock64() - t0 > limit) {
         atomicCAS(err, DEV_OK, DEV_TIMEOUT);
         return false;
       }
-    }
-  }
-}
-
-// Per-call counters of the decode kernel's exchanges (32-bit, in the
-// control block after the ticket, so every reset of the ticket clears them):
-// a producer CTA makes its data visible, then adds 1 with release semantics;
-// a consumer thread waits (acquire) until the count is complete, then its
-// CTA reads the data once.
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-// Waits (bounded) until *p >= target, polling with a short sleep between
-// reads so that a few pollers do not crowd the L2 slice the producers'
-// updates go to.  Gives up when the status word reports an error elsewhere or
-// after the time limit (then it reports the timeout itself).
-__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target, int* err,
-                                           long long limit) {
-  if (ld_acquire_u32(p) >= target) return true;
-  const long long t0 = clock64();
-  while (true) {
-    __nanosleep(32);
-    if (ld_acquire_u32(p) >= target) return true;
-    if (*((volatile int*)err) != DEV_OK) return false;
-    if (clock64() - t0 > limit) {
-      atomicCAS(err, DEV_OK, DEV_TIMEOUT);
-      return false;
     }
   }
 }
