@@ -807,9 +807,11 @@ TRACE_PHASES = {0: "start", 1: "prologue done", 2: "previous kernel done", 3: "C
                 6: "pieces written", 7: "first block gathered", 8: "blocks reduced, h published",
                 9: "h gathered", 10: "gate MMAs complete", 11: "x stored", 12: "end",
                 13: "prologue barrier passed", 14: "thread 0: first box issued",
-                15: "issuer 0: gate MMAs issued"}
-DOWN_PHASES = (0, 13, 14, 1, 2, 3, 4, 5, 6, 12)
-UP_PHASES = (0, 13, 14, 1, 2, 7, 8, 9, 15, 10, 11, 12)
+                15: "issuer 0: gate MMAs issued", 16: "last piece store issued (any thread)",
+                17: "last piece word seen (any thread)", 18: "last thread out of its piece loop",
+                19: "last thread past the shuffle tree", 20: "last thread past its sum store"}
+DOWN_PHASES = (0, 13, 14, 1, 2, 3, 4, 5, 16, 6, 12)
+UP_PHASES = (0, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 9, 15, 10, 11, 12)
 
 
 def decode_trace(args):
@@ -850,7 +852,8 @@ def decode_trace(args):
     a = inputs.activations(32, shape)
     base = dict(w, R=bf(a["R"]), y=bf(a["y"]), inj=torch.from_numpy(a["inj"]).cuda())
     sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
-    n = 256 * 16
+    slots = 24
+    n = 256 * slots
     buf = np.zeros(n, dtype=np.uint64)
     report = {}
     with HcGatedResidual(max_M=32, HC=shape.HC, HS=shape.HS, r=shape.r) as op:
@@ -867,7 +870,7 @@ def decode_trace(args):
                 op.check()
                 assert lib.hc_gr_trace_read(buf.ctypes.data, n) == 0
                 if rep >= 5:
-                    runs.append(buf.reshape(256, 16).astype(np.int64).copy())
+                    runs.append(buf.reshape(256, slots).astype(np.int64).copy())
             table = {}
             for role, phases, sel in (("down", DOWN_PHASES, 6), ("up", UP_PHASES, 11)):
                 per_run = []

@@ -262,7 +262,7 @@ __device__ __noinline__ bool wait_counter(const unsigned* p, unsigned target, in
 }
 
 #ifdef HCGR_TRACE
-constexpr int TRACE_SLOTS = 16;
+constexpr int TRACE_SLOTS = 24;
 __device__ unsigned long long g_trace[MAX_GRID * TRACE_SLOTS];
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -270,10 +270,13 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
   return t;
 }
 // Phase stamp i of this CTA (the calling thread records it in shared memory;
-// the kernel's end writes the CTA's stamps out).
+// the kernel's end writes the CTA's stamps out); HCGR_STAMP_MAX keeps the
+// latest time any thread reaches the point.
 #define HCGR_STAMP(i) (s_stamp[(i)] = globaltimer_ns())
+#define HCGR_STAMP_MAX(i) atomicMax(&s_stamp[(i)], globaltimer_ns())
 #else
 #define HCGR_STAMP(i) ((void)0)
+#define HCGR_STAMP_MAX(i) ((void)0)
 #endif
 
 // --------------------------------------------------------------- the kernel
@@ -346,7 +349,26 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // takes the call ticket and warp 3 allocates TMEM meanwhile.  None of this
   // depends on the previous kernel.
   const int pre_w = min(g.nsl_w, nbox), pre_u = min(g.nsl_u, nub);
-  int issued_w = down ? pre_w : 0, issued_u = down ? 0 : pre_u;   // kept by thread 0
+  int issued_w = down ? pre_w : 0, issued_u = down ? 0 : pre_u;   // kept by warp 0
+  // The call ticket: arrivals in the low half, the call's epoch in the high
+  // half.  Lane 1 of the last warp takes it now and uses the result only at
+  // the CTA's first barrier after the prologue (take_ticket), so the atomic's
+  // round trip hides behind the prologue.
+  unsigned long long ticket_old = 0;
+  if (warp == NW - 1 && lane == 1) ticket_old = atomicAdd(p.ticket, 1ull);
+  // The last arrival moves the epoch on and clears the count.  Both atomics
+  // are performed before this thread reaches the CTA barrier that precedes
+  // the trigger of the next launch, so no arrival of the next call can come
+  // between this call's arrivals and its roll-over.
+  auto take_ticket = [&]() {
+    if (warp == NW - 1 && lane == 1) {
+      if ((ticket_old & 0xffffffffull) == static_cast<unsigned long long>(g.G - 1)) {
+        atomicAdd(p.ticket, (1ull << 32) - static_cast<unsigned long long>(g.G));
+        __threadfence();
+      }
+      *s_epoch = static_cast<uint32_t>(ticket_old >> 32);
+    }
+  };
   if (tid == 0) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
@@ -366,18 +388,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       else issue_u(k);
       if (tid == 0 && k == 0) HCGR_STAMP(14);
     }
-  } else if (warp == NW - 1 && lane == 1) {
-    // arrivals in the low half, the call's epoch in the high half; the last
-    // arrival moves the epoch on and clears the count.  Both atomics are
-    // performed before this thread reaches the CTA barrier that precedes the
-    // trigger of the next launch (below), so no arrival of the next call can
-    // come between this call's arrivals and its roll-over.
-    const unsigned long long old = atomicAdd(p.ticket, 1ull);
-    if ((old & 0xffffffffull) == static_cast<unsigned long long>(g.G - 1)) {
-      atomicAdd(p.ticket, (1ull << 32) - static_cast<unsigned long long>(g.G));
-      __threadfence();
-    }
-    *s_epoch = static_cast<uint32_t>(old >> 32);
   }
   const int tmem_cols = down ? g.tmem_d : g.tmem_u;
   if (warp == 3) {
@@ -444,6 +454,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       s_ss1[m * nu + un] = ss;
     }
     fence_proxy_async_smem();   // the operand rows are read by the tensor cores
+    take_ticket();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -455,40 +466,49 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     grid_dep_launch();
     const uint32_t tmem = *s_tmem;
 
-    // --- step 2: the down/inject products on the tensor cores: lane 0 of
-    // warp 2t + 1 issues the MMAs of row tile t (all chunks, one accumulator
-    // per tile), so up to DOWN_ISSUERS threads issue side by side.  With a
-    // ring, thread 0 refills each slot once the MMAs that read it have
-    // completed; every issuer thread commits barD.
+    // --- step 2: the down/inject products on the tensor cores: warp 2t + 1
+    // walks the MMAs of row tile t (all chunks, one accumulator per tile) and
+    // one elected lane issues, so up to DOWN_ISSUERS warps issue side by
+    // side.  With a ring, warp 0 refills each slot once the MMAs that read it
+    // have completed; every issuer warp commits barD.  Whole warps wait
+    // together: a warp whose lanes part for microseconds and then meet at a
+    // warp-synchronous instruction loses microseconds more.
     const bool dead = c.debug_fault == 1 && b == 0;   // test hook: this CTA writes nothing
-    if ((tid & 63) == 32 && (tid >> 6) < DOWN_ISSUERS) {
-      const int me = tid >> 6;
+    if ((warp & 1) == 1 && (warp >> 1) < DOWN_ISSUERS) {
+      const int me = warp >> 1;
       const uint32_t idesc = idesc_bf16(128, Nd);
       bool okm = true;
 #pragma unroll 1
       for (int i = me; i < nbox && okm && me < g.ntd; i += g.ntd) {
         const int ch = i / g.ntd, slot = i % g.nsl_w;
         const uint32_t ph = (i / g.nsl_w) & 1;
-        okm = mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns);
+        okm = __all_sync(0xffffffffu,
+                         mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns));
         if (!okm) break;
         tc_fence_after();
         const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
         const uint32_t d = tmem + me * Nd;
+        if (elect_one()) {
 #pragma unroll 1
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc, (ch || ks) ? 1u : 0u);
-        umma_commit(free_w(slot));
+          for (int ks = 0; ks < 4; ++ks)
+            umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc, (ch || ks) ? 1u : 0u);
+          umma_commit(free_w(slot));
+        }
+        __syncwarp();
       }
-      if (me == 0) HCGR_STAMP(4);
-      if (!okm) *s_mma_ok = 0;
-      umma_commit(barD);
-    } else if (tid == 0) {
+      if (me == 0 && lane == 0) HCGR_STAMP(4);
+      if (!okm && lane == 0) *s_mma_ok = 0;
+      if (elect_one()) umma_commit(barD);
+      __syncwarp();
+    } else if (warp == 0) {
       // ring refills: a slot is free once the MMAs that read it have completed
 #pragma unroll 1
       for (int i = pre_w; i < nbox; ++i) {
         const int slot = i % g.nsl_w;
-        if (!wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)) break;
-        issue_w(i);
+        if (!__all_sync(0xffffffffu, wait_bar(free_w(slot), ((i / g.nsl_w) - 1) & 1, p.err, p.limit_ns)))
+          break;
+        if (lane == 0) issue_w(i);
+        __syncwarp();
         ++issued_w;
       }
     }
@@ -515,7 +535,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     }
     // the products, straight from TMEM (hi + lo halves): warp w reads lanes
     // 32 (w % 4) ..; the four warp groups take alternate (tile, 8-token) items
-    ok = wait_bar(barD, 0, p.err, p.limit_ns);
+    ok = __all_sync(0xffffffffu, wait_bar(barD, 0, p.err, p.limit_ns));
     tc_fence_after();
     ok = __syncthreads_and(ok && *s_mma_ok != 0);
     if (tid == 0) HCGR_STAMP(5);
@@ -543,6 +563,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
                              xword(v));
           }
         }
+        HCGR_STAMP_MAX(16);
       }
     }
     if (tid == 0) HCGR_STAMP(6);
@@ -583,6 +604,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     }
     // the call ticket's arrival (warp 15) is performed past this barrier:
     // the next kernel in the stream may launch (see the down role)
+    take_ticket();
     __syncthreads();
     grid_dep_launch();
     const uint32_t par = *s_epoch & 1u;
@@ -609,33 +631,56 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         const int ss = su / g.nquad, uq = su - ss * g.nquad;
         const int p0 = jr * g.ppr, p1 = wi < nitem ? min(g.P, p0 + g.ppr) : p0;
         float run[4] = {0.f, 0.f, 0.f, 0.f};
+        // the warp's lanes take ppr pieces each (a uniform trip count) and
+        // poll their missing words together until every lane's are there
 #pragma unroll 1
-        for (int pp0 = p0; pp0 < p1 && got; pp0 += XU) {
+        for (int t0 = 0; t0 < g.ppr && got; t0 += XU) {
+          const uint32_t* src = blk + (ss * g.P + p0 + t0) * g.row + uq * 4;
+          const int nv = p1 - p0 - t0;                       // this lane's pieces here (may be <= 0)
           uint4 v[XU];
 #pragma unroll
           for (int k = 0; k < XU; ++k)
-            v[k] = pp0 + k < p1 ? ld_relaxed_v4(blk + (ss * g.P + pp0 + k) * g.row + uq * 4)
-                                : make_uint4(0u, 0u, 0u, 0u);
+            v[k] = k < nv ? ld_relaxed_v4(src + k * g.row) : make_uint4(0u, 0u, 0u, 0u);
+          long long t_wait = 0;
+#pragma unroll 1
+          for (int it = 0;; ++it) {
+            bool mine = true;
+#pragma unroll
+            for (int k = 0; k < XU; ++k) mine = mine && all_set(v[k]);
+            if (__all_sync(0xffffffffu, mine)) break;
+            if (it == 0) t_wait = clock64();
+            if ((it & 15) == 15) {
+              const bool late = clock64() - t_wait > limit;
+              if (__any_sync(0xffffffffu, late || *((volatile int*)p.err) != DEV_OK)) {
+                if (late && lane == 0) atomicCAS(p.err, DEV_OK, DEV_TIMEOUT);
+                got = false;
+                break;
+              }
+            }
+#pragma unroll
+            for (int k = 0; k < XU; ++k)
+              if (!all_set(v[k])) v[k] = ld_relaxed_v4(src + k * g.row);   // only k < nv are unset
+          }
+          if (!got) break;
+          if (j == u_idx && nv > 0) HCGR_STAMP_MAX(17);
 #pragma unroll
           for (int k = 0; k < XU; ++k) {
-            if (pp0 + k >= p1 || !got) break;
-            const uint32_t* src = blk + (ss * g.P + pp0 + k) * g.row + uq * 4;
-            if (!all_set(v[k])) {
-              v[k] = wait_words(src, p.err, limit);
-              if (!all_set(v[k])) { got = false; break; }
-            }
+            if (k >= nv) break;
             run[0] += __uint_as_float(v[k].x);
             run[1] += __uint_as_float(v[k].y);
             run[2] += __uint_as_float(v[k].z);
             run[3] += __uint_as_float(v[k].w);
           }
         }
+        if (j == u_idx) HCGR_STAMP_MAX(18);
 #pragma unroll 1
         for (int o = g.R / 2; o > 0; o >>= 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) run[e] += __shfl_xor_sync(0xffffffffu, run[e], o);
+        if (j == u_idx) HCGR_STAMP_MAX(19);
         if (wi < nitem && jr == 0)
           *reinterpret_cast<float4*>(s_red + ss * g.row + uq * 4) = make_float4(run[0], run[1], run[2], run[3]);
+        if (j == u_idx) HCGR_STAMP_MAX(20);
       }
       ok = __syncthreads_and(got);
       if (!ok) break;
@@ -695,7 +740,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     // rrms, once every reducer CTA has counted its blocks
     if (ok && nc > 0) {
       bool got = true;
-      if (tid == 0) got = wait_counter(cnt_h + par, static_cast<unsigned>(nred_ctas), p.err, limit);
+      if (warp == 0)
+        got = __all_sync(0xffffffffu, wait_counter(cnt_h + par, static_cast<unsigned>(nred_ctas), p.err, limit));
       ok = __syncthreads_and(got);
     }
     if (ok && nc > 0) {
@@ -746,8 +792,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     const uint32_t tmem = *s_tmem;
     up_issued = ok && nc > 0;
     if (up_issued) {
-      if ((tid & 63) == 32 && (tid >> 6) < UP_ISSUERS) {
-        const int me = tid >> 6;
+      if ((warp & 1) == 1 && (warp >> 1) < UP_ISSUERS) {
+        const int me = warp >> 1;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, Nu);
         bool okm = true;
@@ -755,31 +801,38 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         for (int q = me; q < nub && okm && me < g.ncu; q += g.ncu) {
           const int slot = q % g.nsl_u;
           const uint32_t ph = (q / g.nsl_u) & 1;
-          okm = mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns);
+          okm = __all_sync(0xffffffffu,
+                           mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns));
           if (!okm) break;
           tc_fence_after();
           const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
+          if (elect_one()) {
 #pragma unroll 1
-          for (int tu = 0; tu < g.ntu; ++tu)
+            for (int tu = 0; tu < g.ntu; ++tu)
 #pragma unroll 1
-            for (int ks = 0; ks < 4; ++ks)
-              umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
-                        desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
-          umma_commit(free_u(slot));
+              for (int ks = 0; ks < 4; ++ks)
+                umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
+                          desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
+            umma_commit(free_u(slot));
+          }
+          __syncwarp();
         }
-        if (me == 0) HCGR_STAMP(15);
-        if (!okm) *s_mma_ok = 0;
-        umma_commit(barG);
-      } else if (tid == 0) {
+        if (me == 0 && lane == 0) HCGR_STAMP(15);
+        if (!okm && lane == 0) *s_mma_ok = 0;
+        if (elect_one()) umma_commit(barG);
+        __syncwarp();
+      } else if (warp == 0) {
 #pragma unroll 1
         for (int q = pre_u; q < nub; ++q) {
           const int slot = q % g.nsl_u;
-          if (!wait_bar(free_u(slot), ((q / g.nsl_u) - 1) & 1, p.err, p.limit_ns)) break;
-          issue_u(q);
+          if (!__all_sync(0xffffffffu, wait_bar(free_u(slot), ((q / g.nsl_u) - 1) & 1, p.err, p.limit_ns)))
+            break;
+          if (lane == 0) issue_u(q);
+          __syncwarp();
           ++issued_u;
         }
       }
-      bool got = wait_bar(barG, 0, p.err, p.limit_ns);
+      bool got = __all_sync(0xffffffffu, wait_bar(barG, 0, p.err, p.limit_ns));
       tc_fence_after();
       ok = __syncthreads_and(got && *s_mma_ok != 0);
       if (tid == 0) HCGR_STAMP(10);
@@ -847,7 +900,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
 
   // Teardown: every copy this CTA issued lands and every MMA it issued
   // completes (outstanding only after a failed wait), then TMEM is released.
-  if (tid == 0) {
+  if (warp == 0) {
 #pragma unroll 1
     for (int i = max(0, issued_w - g.nsl_w); i < issued_w; ++i)
       drain_bar(full_w(i % g.nsl_w), (i / g.nsl_w) & 1, limit);
@@ -953,7 +1006,7 @@ cudaError_t launch_decode(const Call& c, const Workspace& ws, const Device& dev,
 
 #ifdef HCGR_TRACE
 // Copies the phase stamps of the last traced decode launch (n <= MAX_GRID *
-// 16 values, [CTA][16] in ns of %globaltimer) to host memory, then clears the
+// TRACE_SLOTS values, [CTA][TRACE_SLOTS] in ns of %globaltimer) to host memory, then clears the
 // array, so that a slot no CTA of the next launch passes reads 0.
 extern "C" int hc_gr_trace_read(unsigned long long* host, int n) {
   const size_t cap = sizeof(hcgr::g_trace) / sizeof(unsigned long long);

@@ -5,7 +5,7 @@
  * libhc_gr_trace.so, the same sources compiled with HCGR_TRACE defined
  * (hyper_connection_gated_gb300/build.py, build(trace=True)).  In that build
  * thread 0 of every decode CTA records %globaltimer (ns) at fixed points of
- * the kernel into a device array of 16 slots per CTA:
+ * the kernel into a device array of 24 slots per CTA:
  *   0 start, 1 prologue done (weight copies issued, TMEM allocated),
  *   2 previous kernel finished (griddepcontrol.wait returned),
  *   down CTAs: 3 COMBINE done, 4 the first issuer's last weight box landed
@@ -14,7 +14,10 @@
  *   up CTAs:   7 first reduce-scatter block gathered, 8 every block reduced
  *              (h published), 9 all-gather of h done, 10 gate MMAs complete,
  *              11 x stored;
- *   12 end (tensor memory released).
+ *   12 end (tensor memory released), 13 the prologue's CTA barrier passed,
+ *   14 thread 0's first weight box issued, 15 the first up issuer's gate
+ *   MMAs issued, 16 (down) the last reduce-scatter store issued by any
+ *   thread, 17 (up) the last word of its first block seen by any thread.
  * Slots a CTA does not pass read 0 (every read clears the array).
  */
 #ifndef HC_GR_TRACE_H_
@@ -24,7 +27,7 @@
 extern "C" {
 #endif
 
-/* Copies n <= 256 * 16 values ([CTA][16], CTA = blockIdx.x of the last
+/* Copies n <= 256 * 24 values ([CTA][24], CTA = blockIdx.x of the last
  * decode launch) to host memory, then zeroes the device array.  Returns the
  * CUDA status (0 = success). */
 int hc_gr_trace_read(unsigned long long* host, int n);
