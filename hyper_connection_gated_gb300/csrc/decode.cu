@@ -34,18 +34,19 @@
 //      range on the tensor cores (its Wu rows landed meanwhile), rebuilds xn
 //      from R2 (recomputed from R, y and inj bit-identically to step 1), rrms
 //      and Wnorm, and stores x = (1 / HC) sum_s G * xn.
-// The exchanges need no grid barrier.  Every 32-bit word of the reduce-scatter
-// buffer is either the empty marker 0xffffffff or a value, and its one reader
-// spins (bounded in time) on each word until it holds a value.  A value never
-// equals the marker: floats are stored with NaN canonicalised.  The reader
-// empties its words again at the end of its work.  The all-gather words are
-// read by every up CTA, so they are published through a counter instead: each
-// reducer CTA writes its h and rrms, fences, and adds 1 (release); one thread
-// of every up CTA waits (acquire, sleeping briefly between reads) until all
-// reducers have counted, then the CTA reads the words once (threads spinning
-// on words every CTA shares delayed the reduce-scatter's stores by
-// microseconds).  The counter alternates between two copies by call parity (a
-// ticket counter), and each call clears the copy the next call uses.
+// The exchanges need no grid barrier.  Every 32-bit word of an exchange
+// buffer is either the empty marker 0xffffffff or a value, and readers poll
+// (bounded in time) until the words they need hold values.  A value never
+// equals the marker: floats are stored with NaN canonicalised, and h as a
+// pair of bf16 from the rounding conversion, whose NaN is 0x7fff.  The
+// reduce-scatter words are emptied again by their one reader at the end of
+// its work; the all-gather buffer, which every up CTA reads, alternates
+// between two copies by call parity (a ticket counter), and each call empties
+// the copy the next call uses.  Whole warps poll together, sleeping briefly
+// between rounds on the shared all-gather words: a warp whose lanes part for
+// microseconds and then meet at a warp-synchronous instruction loses
+// microseconds more, and many threads reading shared words back to back
+// crowd the L2 slices those words live in.
 //
 // Without y (the mix alone) steps 1 and 5 take R as R2 and nothing is stored
 // for it; the Wnorm slice of stream s starts at s * ld_wnorm (0 when one [HS]
@@ -111,7 +112,7 @@ struct Params {
   Call c;
   Geom g;
   uint32_t* xred;       // reduce-scatter words [nred][Gd][row]
-  uint32_t* xgat;       // all-gather words [M][L2w] (gat_words of room)
+  uint32_t* xgat;       // all-gather words, two copies of gat_words
   int gat_words;
   unsigned long long* ticket;
   int* err;
@@ -249,17 +250,7 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long 
   while (!mbar_try_wait(bar, parity) && clock64() - t0 < limit) {
   }
 }
-// Four exchange words, waited for; on failure some word is still empty.
-__device__ __noinline__ uint4 wait_words(const uint32_t* p, int* err, long long limit) {
-  uint4 v;
-  xwait4(p, v, err, limit);
-  return v;
-}
-// An exchange counter, waited for (see wait_count).
-__device__ __noinline__ bool wait_counter(const unsigned* p, unsigned target, int* err,
-                                          long long limit) {
-  return wait_count(p, target, err, limit);
-}
+
 
 #ifdef HCGR_TRACE
 constexpr int TRACE_SLOTS = 24;
@@ -309,9 +300,6 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 272);
   uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + 276);
   int* s_mma_ok = reinterpret_cast<int*>(smem + 280);
-  // all-gather counter, two copies (by call parity): reducer CTAs whose h and
-  // rrms are published (byte 128 of the control block)
-  unsigned* cnt_h = reinterpret_cast<unsigned*>(p.ticket) + 32;
 
   // this CTA's work: the down slice, or the up channel range
   const int s = down ? b / g.P : 0;
@@ -608,11 +596,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     __syncthreads();
     grid_dep_launch();
     const uint32_t par = *s_epoch & 1u;
-    uint32_t* gat = p.xgat;
-    // the counter the next call uses starts at zero (the next call touches it
-    // only after this one has finished)
-    if (u_idx == 0 && tid == 0) cnt_h[par ^ 1u] = 0u;
-    const int nred_ctas = min(g.Gu, g.nred);   // up CTAs that reduce a block
+    uint32_t* gat = p.xgat + static_cast<size_t>(par) * p.gat_words;
 
     // --- step 4: the reducer of blocks u, u + Gu, ...  Work item (stream,
     // quad, sub-range) sums quad uq of the stream's pieces in its sub-range,
@@ -710,25 +694,19 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         const int n0 = jn * g.Qn + 2 * qp;
         if (n0 < r) {   // r is even: n0 + 1 < r too
           const float u0 = v[0] * inv_hc, u1 = v[1] * inv_hc;
-          gat[m * g.L2w + n0 / 2] = pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1));
+          st_relaxed_u32(gat + m * g.L2w + n0 / 2, pack2(u0 * sigmoid_fast(u0), u1 * sigmoid_fast(u1)));
         }
       }
       if (jn == 0) {
 #pragma unroll 1
         for (int i = r / 2 + tid; i < g.L2w; i += NT) {
           const int ss = i - r / 2;
-          gat[m * g.L2w + i] = ss < HC ? __float_as_uint(s_rl[ss]) : 0u;
+          st_relaxed_u32(gat + m * g.L2w + i, ss < HC ? xword(s_rl[ss]) : 0u);
         }
       }
       __syncthreads();   // s_red is reused by the next block
     }
     const bool red_done = ok;   // every block of this CTA read (and reduced)
-    // this CTA's h and rrms are visible at GPU scope before they are counted
-    if (u_idx < g.nred) {
-      __threadfence();
-      __syncthreads();
-      if (tid == 0 && red_done) red_release_add(cnt_h + par, 1u);
-    }
     if (tid == 0) HCGR_STAMP(8);
     // the final mix's inputs (copied since the prologue) have landed; iw from
     // inj (each thread converts the words it copied)
@@ -737,25 +715,44 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     for (int i = tid; i < M * HC; i += NT) s_iw[i] = has_y ? combine_weight(s_iw[i], inv_hc) : 0.f;
 
     // --- step 5: all-gather of h (into the swizzled operand layout) and
-    // rrms, once every reducer CTA has counted its blocks
+    // rrms: each warp polls its quads together until all of them hold values
     if (ok && nc > 0) {
       bool got = true;
-      if (warp == 0)
-        got = __all_sync(0xffffffffu, wait_counter(cnt_h + par, static_cast<unsigned>(nred_ctas), p.err, limit));
-      ok = __syncthreads_and(got);
-    }
-    if (ok && nc > 0) {
       const int hw = r / 2;
       const int nq = M * g.L2w / 4;
 #pragma unroll 1
-      for (int i0 = tid; i0 < nq; i0 += XU * NT) {
+      for (int i0 = warp * 32; i0 < nq && got; i0 += XU * NT) {   // warp-uniform trip count
         uint4 v[XU];
 #pragma unroll
-        for (int k = 0; k < XU; ++k)
-          v[k] = i0 + k * NT < nq ? ld_relaxed_v4(gat + (i0 + k * NT) * 4) : make_uint4(0u, 0u, 0u, 0u);
+        for (int k = 0; k < XU; ++k) {
+          const int i = i0 + lane + k * NT;
+          v[k] = i < nq ? ld_relaxed_v4(gat + i * 4) : make_uint4(0u, 0u, 0u, 0u);
+        }
+        long long t_wait = 0;
+#pragma unroll 1
+        for (int it = 0;; ++it) {
+          bool mine = true;
+#pragma unroll
+          for (int k = 0; k < XU; ++k) mine = mine && all_set(v[k]);
+          if (__all_sync(0xffffffffu, mine)) break;
+          if (it == 0) t_wait = clock64();
+          if ((it & 7) == 7) {
+            const bool late = clock64() - t_wait > limit;
+            if (__any_sync(0xffffffffu, late || *((volatile int*)p.err) != DEV_OK)) {
+              if (late && lane == 0) atomicCAS(p.err, DEV_OK, DEV_TIMEOUT);
+              got = false;
+              break;
+            }
+          }
+          __nanosleep(64);
+#pragma unroll
+          for (int k = 0; k < XU; ++k)
+            if (!all_set(v[k])) v[k] = ld_relaxed_v4(gat + (i0 + lane + k * NT) * 4);   // only i < nq are unset
+        }
+        if (!got) break;
 #pragma unroll
         for (int k = 0; k < XU; ++k) {
-          const int i = i0 + k * NT;
+          const int i = i0 + lane + k * NT;
           if (i >= nq) break;
           // r / 2 and L2w are multiples of 4: a quad is 8 h values or rrms/pad
           const int m = (i * 4) / g.L2w, w0 = i * 4 - m * g.L2w;
@@ -781,7 +778,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
               make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
-      __syncthreads();
+      ok = __syncthreads_and(got);
     }
     if (tid == 0) HCGR_STAMP(9);
     // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
@@ -887,7 +884,8 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     }
     if (tid == 0) HCGR_STAMP(11);
     // Off the critical path: empty the reduce-scatter blocks this CTA read
-    // (when a wait failed instead, hc_gr_check resets them).
+    // (when a wait failed instead, hc_gr_check resets them) and this CTA's
+    // share of the all-gather copy the next call uses.
     if (red_done) {
 #pragma unroll 1
       for (int j = u_idx; j < g.nred; j += g.Gu) {
@@ -896,11 +894,20 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         for (int i = tid; i < g.Gd * g.row / 4; i += NT) blk[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
       }
     }
+    {
+      uint4* nxt = reinterpret_cast<uint4*>(p.xgat + static_cast<size_t>(par ^ 1u) * p.gat_words);
+      const int nq = p.gat_words / 4;
+      const int per = (nq + g.Gu - 1) / g.Gu;
+#pragma unroll 1
+      for (int i = u_idx * per + tid; i < min(nq, (u_idx + 1) * per); i += NT)
+        nxt[i] = make_uint4(XEMPTY, XEMPTY, XEMPTY, XEMPTY);
+    }
   }
 
   // Teardown: every copy this CTA issued lands and every MMA it issued
-  // completes (outstanding only after a failed wait), then TMEM is released.
-  if (warp == 0) {
+  // completes (outstanding only after a failed wait: otherwise every box was
+  // consumed and every commit waited for), then TMEM is released.
+  if (__syncthreads_or(!ok) && warp == 0) {
 #pragma unroll 1
     for (int i = max(0, issued_w - g.nsl_w); i < issued_w; ++i)
       drain_bar(full_w(i % g.nsl_w), (i / g.nsl_w) & 1, limit);

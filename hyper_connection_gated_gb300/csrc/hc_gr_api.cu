@@ -61,7 +61,7 @@ cudaError_t reset_control(const hcgr::Workspace& ws, cudaStream_t s) {
   cudaError_t e = cudaMemsetAsync(ws.ticket, 0, hcgr::CTL_BYTES, s);
   if (e == cudaSuccess && ws.xred_words)
     e = cudaMemsetAsync(ws.xred, 0xff, ws.xred_words * 4, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(ws.xgat, 0xff, ws.xgat_words * 4, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(ws.xgat, 0xff, 2 * ws.xgat_words * 4, s);
   return e;
 }
 
@@ -113,8 +113,8 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   h->r_max = r;
   h->n_out_max = r + HC;
 
-  // one allocation: [ticket/err | reduce-scatter words | all-gather words |
-  // lora | prefill scratch]
+  // one allocation: [ticket/err | reduce-scatter words | all-gather words (two
+  // copies) | lora | prefill scratch]
   size_t xred_words = 0;
   for (int64_t M = 1; M <= std::min<int64_t>(max_M, hcgr::DECODE_MAX_M); ++M)
     xred_words = std::max(xred_words, hcgr::decode_xred_words(h->dev, M, HC, HS, r));
@@ -123,7 +123,7 @@ int hc_gr_create(hc_gr_handle* out, int device, int64_t max_M, int HC, int HS, i
   size_t off = 0;
   const size_t off_ctl = off;    off += hcgr::CTL_BYTES;
   const size_t off_xred = off;   off = align_up(off + xred_words * 4, 256);
-  const size_t off_xgat = off;   off = align_up(off + xgat_words * 4, 256);
+  const size_t off_xgat = off;   off = align_up(off + 2 * xgat_words * 4, 256);
   const size_t off_lora = off;   off = align_up(off + lora_f * 4, 256);
   const size_t off_pre = off;    off = align_up(off + hcgr::prefill_ws_bytes(max_M, HC, HS, r), 256);
   void* base = nullptr;

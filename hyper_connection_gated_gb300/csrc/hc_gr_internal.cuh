@@ -23,7 +23,7 @@ struct Workspace {
   int* err = nullptr;         // device status word
   uint32_t* xred = nullptr;   // decode: reduce-scatter exchange words (empty = 0xffffffff)
   size_t xred_words = 0;
-  uint32_t* xgat = nullptr;   // decode: all-gather exchange words, two copies of xgat_words
+  uint32_t* xgat = nullptr;   // decode: all-gather words, two copies of xgat_words
   size_t xgat_words = 0;
   float* lora = nullptr;      // lora when the caller passes lora == NULL
   void* base = nullptr;       // single allocation holding everything above

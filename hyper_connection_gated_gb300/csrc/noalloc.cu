@@ -38,7 +38,7 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // Carve the scratch array into the decode kernel's workspace for a call that
 // needs xred_words reduce-scatter words: [ticket/status | reduce-scatter |
-// all-gather | lora].
+// all-gather (two copies) | lora].
 bool carve(unsigned char* base, size_t xred_words, Workspace& ws) {
   ws.base = base;
   ws.ticket = reinterpret_cast<unsigned long long*>(base);
@@ -49,7 +49,7 @@ bool carve(unsigned char* base, size_t xred_words, Workspace& ws) {
   off = align256(off + xred_words * 4);
   ws.xgat = reinterpret_cast<uint32_t*>(base + off);
   ws.xgat_words = decode_xgat_words(NOALLOC_MAX_NOUT);
-  off = align256(off + ws.xgat_words * 4);
+  off = align256(off + 2 * ws.xgat_words * 4);
   ws.lora = reinterpret_cast<float*>(base + off);
   off = align256(off + static_cast<size_t>(NOALLOC_MAX_M) * NOALLOC_MAX_NOUT * 4);
   ws.bytes = off;
