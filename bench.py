@@ -809,9 +809,11 @@ TRACE_PHASES = {0: "start", 1: "prologue done", 2: "previous kernel done", 3: "C
                 13: "prologue barrier passed", 14: "thread 0: first box issued",
                 15: "issuer 0: gate MMAs issued", 16: "last piece store issued (any thread)",
                 17: "last piece word seen (any thread)", 18: "last thread out of its piece loop",
-                19: "last thread past the shuffle tree", 20: "last thread past its sum store"}
-DOWN_PHASES = (0, 13, 14, 1, 2, 3, 4, 5, 16, 6, 12)
-UP_PHASES = (0, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 9, 15, 10, 11, 12)
+                19: "last thread past the shuffle tree", 20: "last thread past its sum store",
+                21: "last thread done with the gate readback", 22: "last thread done with x",
+                23: "last thread's first product readback"}
+DOWN_PHASES = (0, 13, 14, 1, 2, 3, 4, 5, 23, 16, 6, 12)
+UP_PHASES = (0, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 9, 15, 10, 21, 22, 11, 12)
 
 
 def decode_trace(args):

@@ -257,7 +257,7 @@ constexpr int TRACE_SLOTS = 24;
 __device__ unsigned long long g_trace[MAX_GRID * TRACE_SLOTS];
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t) : : "memory");   // no memory access moves across it
   return t;
 }
 // Phase stamp i of this CTA (the calling thread records it in shared memory;
@@ -542,6 +542,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         const int jn = n / g.Qn, qn = n - jn * g.Qn;
         uint32_t h0[8], l0[8];
         tmem_ld8x2_wait(tl + t * Nd + m0, tl + t * Nd + Nt + m0, h0, l0);
+        if (item == grp) HCGR_STAMP_MAX(23);
         if (valid) {
 #pragma unroll
           for (int e = 0; e < 8; ++e) {
@@ -641,6 +642,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
                 break;
               }
             }
+            __nanosleep(96);   // fewer reads of lines the down CTAs are writing
 #pragma unroll
             for (int k = 0; k < XU; ++k)
               if (!all_set(v[k])) v[k] = ld_relaxed_v4(src + k * g.row);   // only k < nv are unset
@@ -864,6 +866,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
               if (m0 + e < M) s_g[(m0 + e) * g.rows_u + i] = sigmoid_fast(v[e]);
           }
         }
+        HCGR_STAMP_MAX(21);
         __syncthreads();
 #pragma unroll 1
         for (int i = tid; i < M * nc; i += NT) {
@@ -880,6 +883,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
           }
           c.x[static_cast<int64_t>(m) * HS + ch] = f32_to_bf16(sum * inv_hc);
         }
+        HCGR_STAMP_MAX(22);
       }
     }
     if (tid == 0) HCGR_STAMP(11);
