@@ -579,11 +579,12 @@ def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
         R = R0.repeat(reps_rows, 1, 1)[:M].contiguous()
         y = y0.repeat(reps_rows, 1)[:M].contiguous()
         inj = inj0.repeat(reps_rows, 1)[:M].contiguous()
-        variants = [("unfolded", None, False)]
+        # (name, merged weight, folded, chained by programmatic dependent launch)
+        variants = [("unfolded", None, False, False), ("unfolded_pdl", None, False, True)]
         if M <= 2048:
-            variants += [("merged336", Wdi, False), ("merged336_folded", Wdi_f, True)]
+            variants += [("merged336", Wdi, False, False), ("merged336_folded", Wdi_f, True, False)]
         op = HcGatedResidual(max_M=M)
-        for name, Wm, fold in variants:
+        for name, Wm, fold, pdl in variants:
             sets = [(R, y, inj, w) if j == 0 else
                     (R.clone(), y.clone(), inj.clone(), {k: v.clone() for k, v in w.items()})
                     for j in range(nsets)]
@@ -596,7 +597,7 @@ def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
             def call(j):
                 Rj, yj, ij, wj = sets[j]
                 kw = dict(Wdi=mats[j], fold_w=fold) if mats[j] is not None else dict(Wd=wj["Wd"], Wi=wj["Wi"])
-                op.forward(Rj, yj, ij, wj["Wnorm"], wj["Wu"], out=outs[j], **kw)
+                op.forward(Rj, yj, ij, wj["Wnorm"], wj["Wu"], out=outs[j], pdl=pdl, **kw)
 
             for j in range(nsets):
                 call(j)

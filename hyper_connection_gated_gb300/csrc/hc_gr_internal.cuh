@@ -440,6 +440,12 @@ __device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target, i
   }
 }
 
+// Writes that an earlier grid made with ordinary stores, ordered before this
+// thread's later async-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // Programmatic dependent launch: wait for the grid this one depends on (a
 // no-op without that dependency), and let the next grid start launching.
 __device__ __forceinline__ void grid_dep_wait() {

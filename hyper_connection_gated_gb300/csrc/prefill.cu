@@ -46,6 +46,7 @@
 #include <cstring>
 #include <algorithm>
 #include <type_traits>
+#include <utility>
 
 #include "hc_gr_internal.cuh"
 #include "tmap.h"
@@ -155,6 +156,10 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // Launched as a programmatic dependent (hc_gr_args.pdl) this prologue may
+  // overlap the previous kernel in the stream; its inputs and outputs are
+  // touched only after that kernel has finished.  A no-op otherwise.
+  grid_dep_wait();
 
   if (warp == K1_RY_WARP) {
     if (lane == 0) {
@@ -433,6 +438,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
   }
   tc_fence_before();
   __syncthreads();
+  // every store of this CTA is issued: the reduce may launch (it waits for
+  // this grid's completion before it reads anything)
+  grid_dep_launch();
   if (warp == K1_MMA_WARP) {
     tc_fence_after();
     tmem_dealloc(tmem, p.tmem_cols);
@@ -463,6 +471,9 @@ __global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
                      int M, int S, int r, int np, int HS, float inv_hs, float eps) {
   __shared__ float s_acc[RED_COLS][BM + 1];
   const int tid = threadIdx.x;
+  // As K1's programmatic dependent this grid may start before K1 has
+  // finished: K1's partials are read only after the wait, and through L2.
+  grid_dep_wait();
   const int bid = blockIdx.y * gridDim.x + blockIdx.x;
   const int K = HC * HS;
   for (int k = bid * RED_THREADS + tid; k < K; k += gridDim.x * gridDim.y * RED_THREADS)
@@ -485,13 +496,13 @@ __global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
   if (S == 1) {
 #pragma unroll
     for (int ss = 0; ss < HC; ++ss)
-      q[ss] = *reinterpret_cast<const float4*>(sumsq + (tb + ss) * BM + r4);
+      q[ss] = __ldcg(reinterpret_cast<const float4*>(sumsq + (tb + ss) * BM + r4));
 #pragma unroll
     for (int j = 0; j < NCOL; ++j) {
       const int n = min(n0 + cw + 8 * j, np - 1);
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss)
-        pv[j][ss] = *reinterpret_cast<const float4*>(part + ((tb + ss) * np + n) * BM + r4);
+        pv[j][ss] = __ldcg(reinterpret_cast<const float4*>(part + ((tb + ss) * np + n) * BM + r4));
     }
   } else {
 #pragma unroll
@@ -508,13 +519,13 @@ __global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
       const int c = min(c0 + u, S - 1);
 #pragma unroll
       for (int ss = 0; ss < HC; ++ss)
-        qc[u][ss] = *reinterpret_cast<const float4*>(sumsq + (tb + ss * S + c) * BM + r4);
+        qc[u][ss] = __ldcg(reinterpret_cast<const float4*>(sumsq + (tb + ss * S + c) * BM + r4));
 #pragma unroll
       for (int j = 0; j < NCOL; ++j) {
         const int n = min(n0 + cw + 8 * j, np - 1);
 #pragma unroll
         for (int ss = 0; ss < HC; ++ss)
-          vc[u][j][ss] = *reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4);
+          vc[u][j][ss] = __ldcg(reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4));
       }
     }
 #pragma unroll
@@ -580,6 +591,9 @@ __global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
       inj_next[static_cast<int64_t>(m) * HC + (n - r)] = v;
     }
   }
+  // every store of this block is issued: K2 may launch (it waits for this
+  // grid's completion before it reads anything)
+  grid_dep_launch();
 }
 
 // ===================================================================== K2
@@ -691,6 +705,12 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // hh, rrms, 1 + Wnorm (the reduce) and R2 (K1): as the reduce's
+  // programmatic dependent this prologue may overlap the reduce's tail, so
+  // they are read only after the wait -- by TMA, after the proxy fence, or
+  // through L2 (rrms).
+  grid_dep_wait();
+  fence_proxy_async_global();
 
   if (warp == K2_TMA_WARP) {
     if (lane == 0) {
@@ -780,7 +800,7 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
       const bool v = m < p.M;
       float rr[HC];
 #pragma unroll
-      for (int ss = 0; ss < HC; ++ss) rr[ss] = v ? __ldg(p.rrms + m * HC + ss) : 0.f;
+      for (int ss = 0; ss < HC; ++ss) rr[ss] = v ? __ldcg(p.rrms + m * HC + ss) : 0.f;
       if (!__all_sync(0xffffffffu, mbar_wait_bounded(accfull(ab), (i >> 1) & 1, p.err, p.limit_ns)))
         break;
       tc_fence_after();
@@ -852,26 +872,44 @@ uint32_t pow2_cols(int n) {
   return c;
 }
 
+// A launch of `kernel` on `stream`, as a programmatic dependent of the
+// previous kernel in the stream when pdl is set (its prologue may then overlap
+// that kernel; it waits for it with griddepcontrol.wait before touching
+// memory the previous kernel may have written).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_maybe_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int HCT, bool INJ_MMA>
 cudaError_t launch_k1(const K1Params& p, int grid, size_t smem, const Device& dev,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool pdl) {
   static std::atomic<unsigned long long> attr{0};
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k1_kernel<HCT, INJ_MMA>),
                                   dev.smem_optin, dev.id, attr);
   if (e != cudaSuccess) return e;
-  k1_kernel<HCT, INJ_MMA><<<grid, K1_THREADS, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_maybe_pdl(k1_kernel<HCT, INJ_MMA>, dim3(grid), dim3(K1_THREADS), smem, stream, pdl, p);
 }
 
 template <int HCT>
 cudaError_t launch_k2(const K2Params& p, int grid, size_t smem, const Device& dev,
-                      cudaStream_t stream) {
+                      cudaStream_t stream, bool pdl) {
   static std::atomic<unsigned long long> attr{0};
   cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k2_kernel<HCT>), dev.smem_optin,
                                   dev.id, attr);
   if (e != cudaSuccess) return e;
-  k2_kernel<HCT><<<grid, K2_THREADS, smem, stream>>>(p);
-  return cudaGetLastError();
+  return launch_maybe_pdl(k2_kernel<HCT>, dim3(grid), dim3(K2_THREADS), smem, stream, pdl, p);
 }
 
 bool prefill_supported(const Call& c) {
@@ -911,6 +949,9 @@ size_t prefill_ws_bytes(int64_t max_M, int HC, int HS, int r) {
 cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev,
                            cudaStream_t stream) {
   if (!prefill_supported(c)) return cudaErrorNotSupported;
+  // hc_gr_args.pdl: K1 as a programmatic dependent of the previous kernel in
+  // the stream, the reduce of K1 and K2 of the reduce
+  const bool pdl = c.pdl != 0;
   if (prefill_ws_bytes(c.M, c.HC, c.HS, c.r) > ws.prefill_bytes) return cudaErrorNotSupported;
   const int M = static_cast<int>(c.M);
   const int n_mt = (M + BM - 1) / BM;
@@ -990,9 +1031,18 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     // inject) | barriers | row sums of squares | row inject sums]; the deepest
     // rings that fit
     p.w_slot = static_cast<uint32_t>((std::max(p.n1, p.n2) * 128 + 1023) / 1024 * 1024);
+    // The weight ring's slots take the column blocks in turn (box g in slot
+    // g % nw, block g % nh), so nw is a multiple of nh: every slot then only
+    // ever serves one MMA warp, which waits on its phases in order.  (With an
+    // odd nw and two MMA warps a warp could wait on a slot's next phase
+    // while the previous one was still incomplete; the parity wait then
+    // reports the older phase as complete and the MMAs read a box that has
+    // not landed.)
     const int depths[5][2] = {{4, 4}, {4, 3}, {3, 3}, {3, 2}, {2, 2}};
+    const int nh = p.n2 > 0 ? 2 : 1;
     size_t smem = 0;
     for (const auto& dpt : depths) {
+      if (dpt[1] % nh != 0) continue;
       p.nry = dpt[0];
       p.nw = dpt[1];
       p.off_w = static_cast<uint32_t>(p.nry) * RY_BYTES;
@@ -1013,13 +1063,13 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const int grid = n_mt * c.HC * S;
 #define HCGR_K1(HCV)                                                                        \
   case HCV:                                                                                 \
-    e = inj_mma ? launch_k1<HCV, true>(p, grid, smem, dev, stream)                          \
-                : launch_k1<HCV, false>(p, grid, smem, dev, stream);                         \
+    e = inj_mma ? launch_k1<HCV, true>(p, grid, smem, dev, stream, pdl)                     \
+                : launch_k1<HCV, false>(p, grid, smem, dev, stream, pdl);                    \
     break;
     switch (c.HC) {
       HCGR_K1(1) HCGR_K1(2) HCGR_K1(3) HCGR_K1(4) HCGR_K1(5) HCGR_K1(6) HCGR_K1(7)
-      default: e = inj_mma ? launch_k1<8, true>(p, grid, smem, dev, stream)
-                           : launch_k1<8, false>(p, grid, smem, dev, stream);
+      default: e = inj_mma ? launch_k1<8, true>(p, grid, smem, dev, stream, pdl)
+                           : launch_k1<8, false>(p, grid, smem, dev, stream, pdl);
     }
 #undef HCGR_K1
     if (e != cudaSuccess) return e;
@@ -1028,20 +1078,21 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   {
     const dim3 grid((np + RED_COLS - 1) / RED_COLS, n_mt);
     const bool batch2 = S > 1 && static_cast<int64_t>(grid.x) * grid.y <= 2 * dev.sms;
+    cudaError_t e = cudaSuccess;
 #define HCGR_RED(HCV)                                                                        \
   case HCV:                                                                                  \
-    (batch2 ? k1_reduce_kernel<HCV, (HCV <= 4 ? 2 : 1)> : k1_reduce_kernel<HCV, 1>)          \
-        <<<grid, RED_THREADS, 0, stream>>>(part, sumsq, c.rrms, c.lora,                      \
-                                                          c.inj_next, h, c.Wnorm,            \
-                                                          static_cast<int>(c.ld_wnorm), w1, M, S,  \
-                                                          c.r, np, c.HS, 1.0f / c.HS, c.eps);\
+    e = launch_maybe_pdl(batch2 ? k1_reduce_kernel<HCV, (HCV <= 4 ? 2 : 1)>                \
+                                : k1_reduce_kernel<HCV, 1>,                                  \
+                         grid, dim3(RED_THREADS), 0, stream, pdl, (const float*)part,         \
+                         (const float*)sumsq, c.rrms, c.lora, c.inj_next, h, c.Wnorm,         \
+                         static_cast<int>(c.ld_wnorm), w1, M, S, c.r, np, c.HS, 1.0f / c.HS,  \
+                         c.eps);                                                              \
     break;
     switch (c.HC) {
       HCGR_RED(1) HCGR_RED(2) HCGR_RED(3) HCGR_RED(4) HCGR_RED(5) HCGR_RED(6) HCGR_RED(7)
       default: HCGR_RED(8)
     }
 #undef HCGR_RED
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
   // ---------------- K2
@@ -1097,14 +1148,14 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const int grid = std::min(p.n_units, dev.sms);
     cudaError_t e = cudaSuccess;
     switch (c.HC) {
-      case 1: e = launch_k2<1>(p, grid, smem, dev, stream); break;
-      case 2: e = launch_k2<2>(p, grid, smem, dev, stream); break;
-      case 3: e = launch_k2<3>(p, grid, smem, dev, stream); break;
-      case 4: e = launch_k2<4>(p, grid, smem, dev, stream); break;
-      case 5: e = launch_k2<5>(p, grid, smem, dev, stream); break;
-      case 6: e = launch_k2<6>(p, grid, smem, dev, stream); break;
-      case 7: e = launch_k2<7>(p, grid, smem, dev, stream); break;
-      default: e = launch_k2<8>(p, grid, smem, dev, stream); break;
+      case 1: e = launch_k2<1>(p, grid, smem, dev, stream, pdl); break;
+      case 2: e = launch_k2<2>(p, grid, smem, dev, stream, pdl); break;
+      case 3: e = launch_k2<3>(p, grid, smem, dev, stream, pdl); break;
+      case 4: e = launch_k2<4>(p, grid, smem, dev, stream, pdl); break;
+      case 5: e = launch_k2<5>(p, grid, smem, dev, stream, pdl); break;
+      case 6: e = launch_k2<6>(p, grid, smem, dev, stream, pdl); break;
+      case 7: e = launch_k2<7>(p, grid, smem, dev, stream, pdl); break;
+      default: e = launch_k2<8>(p, grid, smem, dev, stream, pdl); break;
     }
     if (e != cudaSuccess) return e;
   }

@@ -131,13 +131,16 @@ typedef struct hc_gr_args {
                           none of its partial sums, as if it had died, so the
                           others' bounded waits expire and hc_gr_check reports
                           TIMEOUT */
-  int32_t pdl;         /* 1: launch the decode kernel as a programmatic
-                          dependent of the previous kernel on `stream`: its
-                          weight copies (Wd and Wi or Wdi, and Wu) may start
-                          before that kernel has finished, so that kernel must
-                          not write them; activations are read and outputs
-                          written only after it has finished.  0: plain stream
-                          order.  The prefill kernels ignore it. */
+  int32_t pdl;         /* 1: launch as a programmatic dependent of the
+                          previous kernel on `stream`.  Decode: its weight
+                          copies (Wd and Wi or Wdi, and Wu) may start before
+                          that kernel has finished, so that kernel must not
+                          write them; activations are read and outputs written
+                          only after it has finished.  Prefill: K1's prologue
+                          overlaps the previous kernel, the stream reduce is a
+                          dependent of K1 and K2 of the reduce; each waits for
+                          its predecessor before touching memory.  0: plain
+                          stream order. */
   int32_t wnorm_hs;    /* 1: Wnorm has HS entries, one per channel, shared by
                           every stream (xn[s, c] = R2[s, c] rrms[s]
                           (1 + Wnorm[c])); 0: the full-width [K] layout.  A
