@@ -838,6 +838,12 @@ __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant
             acc[4 * j + e] = __ffma2_rn(sg, xn, acc[4 * j + e]);
           }
         }
+        // The slot is read with ordinary loads (the generic proxy) and the
+        // next TMA write into it goes through the async proxy: this
+        // write-after-read across proxies needs the proxy fence before the
+        // slot is released, or the TMA refill can overtake the reads (seen
+        // as occasional wrong x for one warp of one unit).
+        fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(r2free(q));
       }

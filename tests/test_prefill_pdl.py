@@ -9,7 +9,11 @@ first call's K2 -- is replayed 1000 times; every replay's outputs must equal,
 bit for bit, the same call made in plain stream order, which itself matches
 the fp64 oracle.  Shapes: the split-K path (M = 512, K chunks per stream),
 the one-chunk path (M = 4096) and the wide variant (HC = 8, HS = 4096,
-r = 512), whose K1 weight ring holds two column blocks per K block.
+r = 512), whose K1 weight ring holds two column blocks per K block.  The
+same replays in plain stream order (pdl = 0) guard K2's R2 ring: its slots
+are read with ordinary loads and refilled by TMA, a write-after-read across
+memory proxies that once corrupted one warp's x in a few percent of calls at
+the wide shape.
 """
 import pytest
 
@@ -30,9 +34,10 @@ def torch_cuda():
     return torch
 
 
+@pytest.mark.parametrize("pdl", [True, False], ids=["pdl", "plain"])
 @pytest.mark.parametrize("M,shape", [(512, inputs.DEFAULT), (4096, inputs.DEFAULT), (1024, inputs.WIDE)],
                          ids=["M512", "M4096", "wide_M1024"])
-def test_prefill_pdl_graph_replays_bit_identical(torch_cuda, M, shape):
+def test_prefill_graph_replays_bit_identical(torch_cuda, M, shape, pdl):
     torch = torch_cuda
     case = tl.make_case(M, shape, seed=61)
     d = tl.device_case(case)
@@ -48,7 +53,7 @@ def test_prefill_pdl_graph_replays_bit_identical(torch_cuda, M, shape):
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph, stream=stream):
             for o in outs:
-                call(out=o, pdl=True)
+                call(out=o, pdl=pdl)
         torch.cuda.synchronize()
         mismatches = torch.zeros((), dtype=torch.int64, device="cuda")
         with torch.cuda.stream(stream):
