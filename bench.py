@@ -632,6 +632,73 @@ def prefill_sweep(Ms=PREFILL_MS, reps: int = 5):
     return res
 
 
+CROSS_MS = (24, 32, 40, 48, 56, 64, 96, 128, 256, 511)
+
+
+def crossover_sweep(Ms=CROSS_MS, reps: int = 5):
+    """Decode kernel against prefill kernels for the same call, M around and
+    past the decode kernel's limit (64 tokens): graph replay, weight+input
+    sets rotating over more than twice the L2.  The library's M dispatch
+    follows this table."""
+    import numpy as np
+    import torch
+
+    from hyper_connection_gated_gb300 import PATH_DECODE, PATH_PREFILL, HcGatedResidual, inputs
+
+    dev = torch.cuda.current_device()
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 << 20)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to("cuda").view(torch.bfloat16)
+
+    w = {k: bf(v) for k, v in inputs.weights().items()}
+    Mmax = max(Ms)
+    a = inputs.activations(Mmax)
+    base = dict(w, R=bf(a["R"]), y=bf(a["y"]), inj=torch.from_numpy(a["inj"]).cuda())
+    nsets = max(3, int(np.ceil(2.0 * l2 / (WEIGHT_BYTES + Mmax * ACT_BYTES_PER_TOKEN))) + 1)
+    sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
+    hbm, tflops, _ = peaks()
+    stream = torch.cuda.Stream()
+    res = {}
+    with HcGatedResidual(max_M=Mmax) as op:
+        for M in Ms:
+            row = {}
+            for name, path in (("decode", PATH_DECODE), ("prefill", PATH_PREFILL)):
+                if path == PATH_DECODE and M > 64:
+                    continue
+                outs = [None] * nsets
+
+                def call(j):
+                    s_ = sets[j]
+                    outs[j] = op.forward(s_["R"][:M], s_["y"][:M], s_["inj"][:M], s_["Wnorm"], s_["Wu"],
+                                         Wd=s_["Wd"], Wi=s_["Wi"], force_path=path, pdl=True,
+                                         out=outs[j])
+                for j in range(nsets):
+                    call(j)
+                op.check()
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=stream):
+                    for j in range(nsets):
+                        call(j)
+                torch.cuda.synchronize()
+                samples = []
+                with torch.cuda.stream(stream):
+                    g.replay()
+                    for _ in range(reps):
+                        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                        e0.record(stream)
+                        g.replay()
+                        e1.record(stream)
+                        e1.synchronize()
+                        samples.append(e0.elapsed_time(e1) * 1e3 / nsets)
+                op.check()
+                row[name] = statistics.median(samples)
+            roof_us, _ = roofline_us(WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN, M * FLOPS_PER_TOKEN, hbm, tflops)
+            row["roofline_us"] = roof_us
+            res[str(M)] = row
+    return res
+
+
 WIDE_MS = (1, 8, 64, 1024, 8192)
 
 
@@ -952,6 +1019,7 @@ def main():
         torch.distributed.init_process_group("nccl")
     line = run_ours(args, rank, world)
     if rank == 0 and not args.no_prefill_sweep:
+        line["crossover_us"] = crossover_sweep()
         line["prefill_sweep_us"] = prefill_sweep()
         line["wide_sweep_us"] = wide_sweep()
         line["entry_points_us"] = entry_sweep()

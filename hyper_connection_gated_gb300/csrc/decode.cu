@@ -1,5 +1,5 @@
 // Decode path of the HC gated residual: one persistent kernel for small token
-// counts (M <= 32), where the time goes into streaming the weights once
+// counts (M <= 64), where the time goes into streaming the weights once
 // (aiter PR #5913, "Technical Details"; the page's skinny decode with split-K
 // partials and a last-stage reduce is the prior art).
 //

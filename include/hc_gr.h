@@ -37,7 +37,7 @@
  * past the call.  bf16 tensors and lora are 16-byte aligned; inj, rrms and
  * inj_next need only 4-byte alignment.  HS and r are multiples of 8.  The
  * prefill kernels additionally need HS and r multiples of 64, r <= 512 and
- * HC <= 8; other shapes run on the decode kernel (M <= 32) or are rejected
+ * HC <= 8; other shapes run on the decode kernel (M <= 64) or are rejected
  * with HC_GR_ERR_UNSUPPORTED.
  *
  * Streams and concurrency: hc_gr_forward* only enqueues work on `stream`
@@ -96,8 +96,9 @@ typedef enum hc_gr_status {
 /* Dispatch between the two kernel families (the page's "Behavior and intent":
  * a skinny decode path for few tokens beside the tiled two-kernel path). */
 typedef enum hc_gr_path {
-  HC_GR_PATH_AUTO = 0,    /* M <= 32: decode kernel, otherwise prefill kernels */
-  HC_GR_PATH_DECODE = 1,  /* weight-streaming persistent kernel, M <= 32 */
+  HC_GR_PATH_AUTO = 0,    /* M <= 56 (the measured crossover): decode kernel,
+                             otherwise prefill kernels */
+  HC_GR_PATH_DECODE = 1,  /* weight-streaming persistent kernel, M <= 64 */
   HC_GR_PATH_PREFILL = 2  /* tensor-core (tcgen05) two-stage kernels */
 } hc_gr_path;
 

@@ -12,7 +12,8 @@ import pytest
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SMS, SMEM_OPTIN = 152, 232448          # GB300: SMs, opt-in shared memory per block (bytes)
 
-# (HC, HS, r, every M in 1..32 must have a decode plan)
+# (HC, HS, r, every M in 1..32 must have a decode plan; larger M up to the
+# kernel's limit may fall back to the prefill kernels)
 SHAPES = [(4, 2560, 320, True), (8, 4096, 512, True), (4, 256, 32, True), (8, 128, 24, True),
           (2, 2560, 320, True), (2, 8192, 320, True), (4, 8192, 320, True), (4, 256, 64, True),
           (1, 40960, 320, False)]
@@ -41,7 +42,8 @@ def test_decode_plan_invariants(replay, HC, HS, r, all_planned):
     assert lines[-1] == "DONE fails=0"
     planned = [ln for ln in lines if " plan G=" in ln]
     if all_planned:
-        assert len(planned) == 32, [ln for ln in lines if "plan=none" in ln]
+        missing = [ln for ln in lines if "plan=none" in ln and int(ln.split()[0][2:]) <= 32]
+        assert not missing, missing
     else:
         # no decode plan: the dispatcher sends these calls to the prefill kernels
         assert not planned

@@ -113,3 +113,35 @@ def test_decode_deterministic_and_batch_invariant(torch_cuda, case32):
                            {k: tl.to_f64(v)[5:6] for k, v in outs[0].items()})
     assert max(rep.values()) <= 0.5, rep
     np.testing.assert_array_equal(tl.to_f64(one["R2"]), tl.to_f64(outs[0]["R2"])[5:6])
+
+
+@pytest.fixture(scope="module")
+def case64():
+    return tl.make_case(64, seed=71)
+
+
+@pytest.mark.parametrize("M", [33, 40, 56, 64])
+def test_decode_beyond_32_tokens(torch_cuda, case64, M):
+    # the decode kernel up to its 64-token limit (exchange blocks of one
+    # token's whole output row from M = 40 on)
+    case = dict(case64, R=case64["R"][:M], y=case64["y"][:M], inj=case64["inj"][:M], M=M)
+    d = tl.device_case(case)
+    with HcGatedResidual(max_M=64) as op:
+        out = op.forward(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"],
+                         force_path=PATH_DECODE, check=True)
+    tl.assert_parity(out, tl.oracle_ref(case), label=f"decode M={M}")
+
+
+@pytest.mark.parametrize("M", [33, 56, 57, 511])
+def test_auto_dispatch_around_the_crossover(torch_cuda, M):
+    # PATH_AUTO takes the decode kernel up to the measured crossover (56
+    # tokens) and the prefill kernels above; both sides of it, and the last
+    # M before the prefill-only sizes, match the oracle
+    from hyper_connection_gated_gb300 import PATH_AUTO
+
+    case = tl.make_case(M, seed=72)
+    d = tl.device_case(case)
+    with HcGatedResidual(max_M=M) as op:
+        out = op.forward(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"],
+                         force_path=PATH_AUTO, check=True)
+    tl.assert_parity(out, tl.oracle_ref(case), label=f"auto M={M}")
