@@ -76,12 +76,12 @@ namespace {
 
 constexpr int NT = 512;              // threads per CTA
 constexpr int NW = NT / 32;
-constexpr int MAX_SLOTS = 8;         // ring slots per weight stream
+constexpr int MAX_SLOTS = 16;        // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
 constexpr int DOWN_ISSUERS = 8;      // threads that may issue the down MMAs (one per row tile)
 constexpr int UP_ISSUERS = 8;        // threads that may issue the gate MMAs (one per Wu chunk)
 constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
-constexpr int HDR = 512;             // mbarriers, TMEM address, flags
+constexpr int HDR = 1024;            // mbarriers, TMEM address, flags
 constexpr int SMEM_BUDGET = 220 * 1024;
 constexpr int SMEM_ALLOC = SMEM_BUDGET + 1024;
 // Dynamic shared memory of a launch is at least this much, so that two CTAs
@@ -174,6 +174,11 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
   if (g.ntd > DOWN_ISSUERS || g.nchunk_u > UP_ISSUERS) return false;
   const int hsc = c.HS / 64;                            // 64-column chunks per stream
   const int sms = std::min(dev.sms, MAX_GRID);
+  // Every feasible slice size is planned; the plan kept is the one whose
+  // larger per-CTA weight share (down: rows x slice, up: channel rows x r) is
+  // smallest, since every CTA streams its share at about the same rate.
+  Geom best;
+  long long best_bytes = -1;
   for (g.nkc = 1; g.nkc <= hsc; ++g.nkc) {
     g.P = (hsc + g.nkc - 1) / g.nkc;
     g.Gd = c.HC * g.P;
@@ -213,29 +218,39 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
       fits = layout_down(g);
     }
     if (!fits) continue;
-    // up: every chunk resident when it fits, else an even ring (its two
-    // issuers take alternate slots)
+    // up: every chunk resident when it fits, else the deepest ring that fits
+    // with one issuing warp per slot (slot q % nsl_u is always issuer
+    // q % ncu's); each issuer accumulates into its own tensor-memory copy.
+    // With every chunk resident and too many copies for the tensor memory,
+    // two issuers take alternate chunks (each chunk's slot is used once).
     bool fits_u = false;
     for (int u = std::min(g.nchunk_u, MAX_SLOTS); u >= 1 && !fits_u; --u) {
-      if (u < g.nchunk_u && (u & 1)) continue;
+      if (u < g.nchunk_u && u > UP_ISSUERS) continue;
       g.nsl_u = u;
-      fits_u = layout_up(c, g);
+      g.ncu = u >= g.nchunk_u ? g.nchunk_u : u;
+      if (u >= g.nchunk_u && g.ncu * g.ntu * g.Nu > 512) g.ncu = std::min(2, g.nchunk_u);
+      fits_u = g.ncu * g.ntu * g.Nu <= 512 && layout_up(c, g);
     }
     if (!fits_u) continue;
-    // down: one accumulator per row tile (one issuing thread each); up: one
-    // accumulator copy per issuing thread -- a thread per Wu chunk when every
-    // chunk has its own slot and the copies fit, else two
-    g.ncu = g.nsl_u >= g.nchunk_u && g.nchunk_u * g.ntu * g.Nu <= 512 ? g.nchunk_u
-                                                                       : std::min(2, g.nchunk_u);
+    // down: one accumulator per row tile (one issuing warp each)
     const int cd = g.ntd * g.Nd, cu = g.ncu * g.ntu * g.Nu;
     if (cd > 512 || cu > 512) continue;
     g.tmem_d = tmem_pow2(cd);
     g.tmem_u = tmem_pow2(cu);
     g.total = std::max(std::max(g.d_total, g.u_total), SMEM_MIN - 1024);
     // a kernel that allocates TMEM runs one CTA per SM
-    if (g.G <= dev.sms) return true;
+    if (g.G > dev.sms) continue;
+    const long long down_b = static_cast<long long>(g.rows_w + (g.merged ? 0 : c.HC)) * g.nkc * 128;
+    const long long up_b = static_cast<long long>(g.rows_u) * c.r * 2;
+    const long long share = std::max(down_b, up_b);
+    if (best_bytes < 0 || share < best_bytes) {
+      best = g;
+      best_bytes = share;
+    }
   }
-  return false;
+  if (best_bytes < 0) return false;
+  g = best;
+  return true;
 }
 
 // Out-of-line slow paths of the bounded waits: one copy of each wait loop
@@ -292,14 +307,15 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   if (tid == 0) HCGR_STAMP(0);
 
   const uint32_t bar0 = smem_u32(smem);
+  // MAX_SLOTS barriers each: full/free of the down ring, full/free of the up ring
   auto full_w = [&](int i) { return bar0 + 8u * i; };
-  auto free_w = [&](int i) { return bar0 + 64u + 8u * i; };
-  auto full_u = [&](int i) { return bar0 + 128u + 8u * i; };
-  auto free_u = [&](int i) { return bar0 + 192u + 8u * i; };
-  const uint32_t barD = bar0 + 256u, barG = bar0 + 264u;
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 272);
-  uint32_t* s_epoch = reinterpret_cast<uint32_t*>(smem + 276);
-  int* s_mma_ok = reinterpret_cast<int*>(smem + 280);
+  auto free_w = [&](int i) { return bar0 + 8u * (MAX_SLOTS + i); };
+  auto full_u = [&](int i) { return bar0 + 8u * (2 * MAX_SLOTS + i); };
+  auto free_u = [&](int i) { return bar0 + 8u * (3 * MAX_SLOTS + i); };
+  const uint32_t barD = bar0 + 8u * 4 * MAX_SLOTS, barG = barD + 8u;
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(smem + 8 * 4 * MAX_SLOTS + 16);
+  uint32_t* s_epoch = s_tmem + 1;
+  int* s_mma_ok = reinterpret_cast<int*>(s_tmem + 2);
 
   // this CTA's work: the down slice, or the up channel range
   const int s = down ? b / g.P : 0;
@@ -359,7 +375,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   };
   if (tid == 0) {
 #pragma unroll 1
-    for (int i = 0; i < 32; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
+    for (int i = 0; i < 4 * MAX_SLOTS; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
     mbar_init(barD, DOWN_ISSUERS);
     mbar_init(barG, UP_ISSUERS);
     fence_mbar_init();
@@ -784,9 +800,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     }
     if (tid == 0) HCGR_STAMP(9);
     // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
-    // channel) of this CTA's range; lane 0 of warp 2k + 1 (k < ncu) issues
-    // chunks k, k + ncu, .. into its own accumulator copy (with a ring, ncu =
-    // 2 and each of its two slots serves one issuer).  Every candidate thread
+    // channel) of this CTA's range; warp 2k + 1 (k < ncu) walks chunks k,
+    // k + ncu, .. (with a ring, always the same slot) into its own
+    // accumulator copy and one elected lane issues.  Every candidate warp
     // commits barG.
     const uint32_t tmem = *s_tmem;
     up_issued = ok && nc > 0;

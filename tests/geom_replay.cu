@@ -62,14 +62,14 @@ int main(int argc, char** argv) {
               g.tmem_u >= g.ncu * g.ntu * g.Nu, M, "tensor-memory columns");
     check(g.ntd <= hcgr::DOWN_ISSUERS && g.nchunk_u <= hcgr::UP_ISSUERS && g.ncu >= 1 &&
               g.ncu <= g.nchunk_u, M, "issuers");
-    // rings: a down ring's slots each serve one row tile (one issuer); an up
-    // ring alternates its slots between two issuers
+    // rings: every slot of a ring serves one issuer (the down ring's slot
+    // count a multiple of its row tiles, the up ring one issuer per slot)
     const int nbox = g.ntd * g.nkc;
     check(g.nsl_w >= 1 && g.nsl_w <= hcgr::MAX_SLOTS && (g.nsl_w >= nbox || g.nsl_w % g.ntd == 0),
           M, "down ring");
     check(g.nsl_u >= 1 && g.nsl_u <= hcgr::MAX_SLOTS &&
               (g.nsl_u >= g.nchunk_u ? g.ncu == g.nchunk_u || g.ncu == 2
-                                     : g.ncu == 2 && g.nsl_u % 2 == 0),
+                                     : g.ncu == g.nsl_u && g.ncu <= hcgr::UP_ISSUERS),
           M, "up ring");
     // down role regions: header arrays, operands, weight slots
     check(g.d_ss1 >= hcgr::HDR && g.d_ssum >= g.d_ss1 + g.Nt * g.nkc * 8 * 4, M, "down header arrays");
