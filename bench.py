@@ -41,9 +41,10 @@ ACT_BYTES_PER_TOKEN = (2 * K_DIM + 2 * HS + 4 * HC + 2 * K_DIM + 4 * HC + 4 * HC
 FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 
 # DRAM bytes (read + write) of one decode_kernel launch per M, from one ncu
-# capture (dram__bytes_read.sum + dram__bytes_write.sum, profiles/
-# decode_kernel_dram_per_M.md).  They hold only for the kernel sources they
-# were taken on: if those changed since, roofline.traffic is null.
+# capture of this benchmark's decode calls (dram__bytes_read.sum +
+# dram__bytes_write.sum; the capture's summary sits under profiles/).  They
+# hold only for the kernel sources they were taken on: if those changed
+# since, roofline.traffic is null and roofline.traffic_source says why.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
     "sources_sha256": "e793798bc6625aef7145c9bb03fb7bec2100522e73f69caf0ac5f2f22d7e0907",
@@ -71,10 +72,14 @@ def decode_sources_sha256() -> str:
 
 
 def decode_traffic_per_launch():
-    """Mean measured DRAM bytes per launch over the sweep, or None if stale."""
+    """Mean measured DRAM bytes per launch over the sweep (None if the stored
+    capture is stale) and a note on where the figure comes from."""
     if decode_sources_sha256() != DECODE_TRAFFIC["sources_sha256"]:
-        return None
-    return sum(DECODE_TRAFFIC["bytes"][M] for M in SWEEP) / len(SWEEP)
+        return None, ("null: the decode kernel's sources changed since the stored ncu capture "
+                      "(sources hash mismatch)")
+    return (sum(DECODE_TRAFFIC["bytes"][M] for M in SWEEP) / len(SWEEP),
+            "stored ncu capture of these kernel sources (dram__bytes_read.sum + "
+            "dram__bytes_write.sum per launch, mean over the sweep); not measured in this run")
 
 
 def max_over_ranks(value: float, world: int, device="cuda") -> float:
@@ -471,6 +476,7 @@ def run_ours(args, rank, world):
 
     hbm, bf16_peak, peak_src = peaks()
     alg_bytes = sum(WEIGHT_BYTES + M * ACT_BYTES_PER_TOKEN for M in SWEEP)
+    traffic, traffic_src = decode_traffic_per_launch()
     kernel_us = sum(per_m[M] for M in SWEEP)
     achieved = alg_bytes / (kernel_us * 1e-6) / 1e9
     clocks = clk.summary()
@@ -496,7 +502,7 @@ def run_ours(args, rank, world):
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": len(SWEEP) * args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": decode_traffic_per_launch(),
+                     "frac": achieved / hbm, "traffic": traffic, "traffic_source": traffic_src,
                      "algorithmic_bytes_per_launch": alg_bytes / len(SWEEP),
                      "kernel": "decode_kernel (per launch, mean over the sweep: weights + activations)",
                      "peak_source": peak_src},
@@ -879,9 +885,13 @@ TRACE_PHASES = {0: "start", 1: "prologue done", 2: "previous kernel done", 3: "C
                 17: "last piece word seen (any thread)", 18: "last thread out of its piece loop",
                 19: "last thread past the shuffle tree", 20: "last thread past its sum store",
                 21: "last thread done with the gate readback", 22: "last thread done with x",
-                23: "last thread's first product readback"}
-DOWN_PHASES = (0, 13, 14, 1, 2, 3, 4, 5, 23, 16, 6, 12)
-UP_PHASES = (0, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 9, 15, 10, 21, 22, 11, 12)
+                23: "last thread's first product readback",
+                24: "issuer 0: first box landed", 25: "issuer 0: first MMAs issued",
+                26: "last thread out of the gather loop", 27: "issuer 0: first chunk landed",
+                28: "issuer 0: first gate MMAs issued", 29: "mix inputs landed",
+                30: "down MMA completion seen", 31: "gate MMA completion seen"}
+DOWN_PHASES = (0, 13, 14, 1, 2, 3, 24, 25, 4, 30, 5, 23, 16, 6, 12)
+UP_PHASES = (0, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 29, 26, 9, 27, 28, 15, 31, 10, 21, 22, 11, 12)
 
 
 def decode_trace(args):
@@ -922,7 +932,7 @@ def decode_trace(args):
     a = inputs.activations(32, shape)
     base = dict(w, R=bf(a["R"]), y=bf(a["y"]), inj=torch.from_numpy(a["inj"]).cuda())
     sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
-    slots = 24
+    slots = 32
     n = 256 * slots
     buf = np.zeros(n, dtype=np.uint64)
     report = {}

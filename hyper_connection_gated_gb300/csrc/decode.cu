@@ -79,6 +79,7 @@ constexpr int NW = NT / 32;
 constexpr int MAX_SLOTS = 16;        // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
 constexpr int DOWN_ISSUERS = 8;      // threads that may issue the down MMAs (one per row tile)
+constexpr uint64_t PF_CHUNK = 16384;   // bytes per L2 prefetch of the weights
 constexpr int UP_ISSUERS = 8;        // threads that may issue the gate MMAs (one per Wu chunk)
 constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int HDR = 1024;            // mbarriers, TMEM address, flags
@@ -268,7 +269,7 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long 
 
 
 #ifdef HCGR_TRACE
-constexpr int TRACE_SLOTS = 24;
+constexpr int TRACE_SLOTS = 32;
 __device__ unsigned long long g_trace[MAX_GRID * TRACE_SLOTS];
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -297,6 +298,44 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   __shared__ unsigned long long s_stamp[TRACE_SLOTS];
   if (tid < TRACE_SLOTS) s_stamp[tid] = 0;
 #endif
+  // Every CTA first asks L2 for its 1/G share of the weights, in contiguous
+  // pieces of up to 16 KB: HBM streams them in long runs (the box copies of
+  // the operand layout read 128-byte pieces of many rows, a pattern HBM
+  // serves at about two thirds of the rate) from the kernel's first
+  // instructions on, and the box copies issued later mostly hit L2.  The
+  // weights never depend on the previous kernel, so this precedes
+  // griddepcontrol.wait.
+  {
+    const uint64_t G = gridDim.x, me = blockIdx.x;
+    const uint64_t rK = static_cast<uint64_t>(c.r) * c.K, hK = static_cast<uint64_t>(c.HC) * c.K;
+    const bool merged_w = c.Wi == c.Wd + rK;
+    // [lo, hi) of this CTA's share of a buffer of n bytes (16-byte bounds)
+    auto share = [&](uint64_t n, uint64_t& lo, uint64_t& hi) {
+      const uint64_t piece = (n / G + 16) & ~15ull;   // > n / G, a multiple of 16
+      lo = min(n, piece * me);
+      hi = min(n, lo + piece);
+    };
+    uint64_t lo0, hi0, lo1, hi1, lo2, hi2;
+    share(2 * (merged_w ? rK + hK : rK), lo0, hi0);
+    share(merged_w ? 0 : 2 * hK, lo1, hi1);
+    share(2 * rK, lo2, hi2);
+    const int n0 = static_cast<int>((hi0 - lo0 + PF_CHUNK - 1) / PF_CHUNK);
+    const int n1 = static_cast<int>((hi1 - lo1 + PF_CHUNK - 1) / PF_CHUNK);
+    const int n2 = static_cast<int>((hi2 - lo2 + PF_CHUNK - 1) / PF_CHUNK);
+#pragma unroll 1
+    for (int i = threadIdx.x; i < n0 + n1 + n2; i += NT) {
+      const char* src;
+      uint64_t a, end;
+      if (i < n0) {
+        src = reinterpret_cast<const char*>(c.Wd); a = lo0 + i * PF_CHUNK; end = hi0;
+      } else if (i < n0 + n1) {
+        src = reinterpret_cast<const char*>(c.Wi); a = lo1 + (i - n0) * PF_CHUNK; end = hi1;
+      } else {
+        src = reinterpret_cast<const char*>(c.Wu); a = lo2 + (i - n0 - n1) * PF_CHUNK; end = hi2;
+      }
+      bulk_prefetch_l2(src + a, static_cast<uint32_t>(end - a < PF_CHUNK ? end - a : PF_CHUNK));
+    }
+  }
   const int b = blockIdx.x;
   const int M = static_cast<int>(c.M), Nt = g.Nt, Nd = g.Nd, Nu = g.Nu;
   const int HC = c.HC, HS = c.HS, K = c.K, r = c.r, n_out = c.n_out;
@@ -489,6 +528,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         okm = __all_sync(0xffffffffu,
                          mbar_test_wait(full_w(slot), ph) || wait_bar(full_w(slot), ph, p.err, p.limit_ns));
         if (!okm) break;
+        if (me == 0 && lane == 0 && i == me) HCGR_STAMP(24);
         tc_fence_after();
         const uint32_t a = wbase + slot * TILE, bq = act + ch * Nd * 128;
         const uint32_t d = tmem + me * Nd;
@@ -497,6 +537,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
           for (int ks = 0; ks < 4; ++ks)
             umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc, (ch || ks) ? 1u : 0u);
           umma_commit(free_w(slot));
+          if (me == 0 && i == me) HCGR_STAMP(25);
         }
         __syncwarp();
       }
@@ -540,6 +581,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     // the products, straight from TMEM (hi + lo halves): warp w reads lanes
     // 32 (w % 4) ..; the four warp groups take alternate (tile, 8-token) items
     ok = __all_sync(0xffffffffu, wait_bar(barD, 0, p.err, p.limit_ns));
+    if (tid == 0) HCGR_STAMP(30);
     tc_fence_after();
     ok = __syncthreads_and(ok && *s_mma_ok != 0);
     if (tid == 0) HCGR_STAMP(5);
@@ -731,6 +773,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     cp_async_wait_all();
 #pragma unroll 1
     for (int i = tid; i < M * HC; i += NT) s_iw[i] = has_y ? combine_weight(s_iw[i], inv_hc) : 0.f;
+    if (tid == 0) HCGR_STAMP(29);
 
     // --- step 5: all-gather of h (into the swizzled operand layout) and
     // rrms: each warp polls its quads together until all of them hold values
@@ -787,6 +830,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
           }
         }
       }
+      HCGR_STAMP_MAX(26);
       // token rows past M, and h columns past r in the last chunk, are zero
 #pragma unroll 1
       for (int i = tid; i < g.nchunk_u * Nu * 8; i += NT) {
@@ -819,6 +863,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
           okm = __all_sync(0xffffffffu,
                            mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns));
           if (!okm) break;
+          if (me == 0 && lane == 0 && q == me) HCGR_STAMP(27);
           tc_fence_after();
           const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
           if (elect_one()) {
@@ -829,6 +874,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
                 umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
                           desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
             umma_commit(free_u(slot));
+            if (me == 0 && q == me) HCGR_STAMP(28);
           }
           __syncwarp();
         }
@@ -848,6 +894,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         }
       }
       bool got = __all_sync(0xffffffffu, wait_bar(barG, 0, p.err, p.limit_ns));
+      if (tid == 0) HCGR_STAMP(31);
       tc_fence_after();
       ok = __syncthreads_and(got && *s_mma_ok != 0);
       if (tid == 0) HCGR_STAMP(10);

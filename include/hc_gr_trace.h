@@ -5,7 +5,7 @@
  * libhc_gr_trace.so, the same sources compiled with HCGR_TRACE defined
  * (hyper_connection_gated_gb300/build.py, build(trace=True)).  In that build
  * thread 0 of every decode CTA records %globaltimer (ns) at fixed points of
- * the kernel into a device array of 24 slots per CTA:
+ * the kernel into a device array of 32 slots per CTA:
  *   0 start, 1 prologue done (weight copies issued, TMEM allocated),
  *   2 previous kernel finished (griddepcontrol.wait returned),
  *   down CTAs: 3 COMBINE done, 4 the first issuer's last weight box landed
@@ -17,7 +17,15 @@
  *   12 end (tensor memory released), 13 the prologue's CTA barrier passed,
  *   14 thread 0's first weight box issued, 15 the first up issuer's gate
  *   MMAs issued, 16 (down) the last reduce-scatter store issued by any
- *   thread, 17 (up) the last word of its first block seen by any thread.
+ *   thread, 17 (up) the last word of its first block seen by any thread,
+ *   18-23 sub-stamps of the reduce (18 piece loop left, 19 shuffle tree
+ *   passed, 20 sum stored; latest thread), of the gate readback (21), of x
+ *   (22) and of the first product readback (23); 24/25 the first down
+ *   issuer's first box landed / its first MMAs issued; 26 (up) the last
+ *   thread out of the all-gather loop; 27/28 the first up issuer's first
+ *   chunk landed / its MMAs issued; 29 (up) the mix inputs landed;
+ *   30 (down) the down MMAs' completion seen; 31 (up) the gate MMAs'
+ *   completion seen.
  * Slots a CTA does not pass read 0 (every read clears the array).
  */
 #ifndef HC_GR_TRACE_H_
@@ -27,7 +35,7 @@
 extern "C" {
 #endif
 
-/* Copies n <= 256 * 24 values ([CTA][24], CTA = blockIdx.x of the last
+/* Copies n <= 256 * 32 values ([CTA][32], CTA = blockIdx.x of the last
  * decode launch) to host memory, then zeroes the device array.  Returns the
  * CUDA status (0 = success). */
 int hc_gr_trace_read(unsigned long long* host, int n);

@@ -37,4 +37,12 @@ def test_code_only_ignores_prose_but_not_code():
 def test_decode_hash_is_stable_and_sixty_four_hex():
     h = bench.decode_sources_sha256()
     assert h == bench.decode_sources_sha256() and len(h) == 64
-    assert bench.decode_traffic_per_launch() is None or bench.decode_traffic_per_launch() > 1e7
+    traffic, source = bench.decode_traffic_per_launch()
+    assert (traffic is None) == source.startswith("null")
+    assert traffic is None or traffic > 1e7
+
+
+def test_stale_traffic_is_null_with_its_reason(monkeypatch):
+    monkeypatch.setitem(bench.DECODE_TRAFFIC, "sources_sha256", "0" * 64)
+    traffic, source = bench.decode_traffic_per_launch()
+    assert traffic is None and "changed" in source
