@@ -362,6 +362,19 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   const int nkv = down ? min(g.nkc, (HS - c0) / 64) : 0;       // chunks of the slice
   const int k0 = s * HS + c0;
   const int nbox = g.ntd * nkv;                                // down weight boxes
+  // The COMBINE inputs of a down CTA's slice (R and y rows of every token,
+  // the Wnorm slice) into L2 as well: L2 is the point of coherence, so a
+  // prefetch before griddepcontrol.wait never hands out data older than a
+  // write the previous kernel makes (it only warms the lines).
+  if (down && nkv > 0 && tid <= 2 * M) {
+    const uint32_t sb = static_cast<uint32_t>(min(64 * g.nkc, HS - c0)) * 2;
+    if (tid < M)
+      bulk_prefetch_l2(c.R + static_cast<int64_t>(tid) * K + k0, sb);
+    else if (tid < 2 * M && has_y)
+      bulk_prefetch_l2(c.y + static_cast<int64_t>(tid - M) * HS + c0, sb);
+    else if (tid == 2 * M)
+      bulk_prefetch_l2(c.Wnorm + s * c.ld_wnorm + c0, sb);
+  }
   const int u_idx = down ? 0 : b - g.Gd;
   const int cp0 = down ? 0 : min(HS, u_idx * g.nc_max);
   const int nc = down ? 0 : min(HS, cp0 + g.nc_max) - cp0;
