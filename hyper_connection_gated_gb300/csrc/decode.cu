@@ -80,7 +80,7 @@ constexpr int MAX_SLOTS = 16;        // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
 constexpr int DOWN_ISSUERS = 8;      // threads that may issue the down MMAs (one per row tile)
 constexpr uint64_t PF_CHUNK = 16384;   // bytes per L2 prefetch of the weights
-constexpr int UP_ISSUERS = 8;        // threads that may issue the gate MMAs (one per Wu chunk)
+constexpr int UP_ISSUERS = 15;       // warps that may issue the gate MMAs (one per copy and row tile)
 constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int HDR = 1024;            // mbarriers, TMEM address, flags
 constexpr int SMEM_BUDGET = 220 * 1024;
@@ -219,18 +219,23 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
       fits = layout_down(g);
     }
     if (!fits) continue;
-    // up: every chunk resident when it fits, else the deepest ring that fits
-    // with one issuing warp per slot (slot q % nsl_u is always issuer
-    // q % ncu's); each issuer accumulates into its own tensor-memory copy.
-    // With every chunk resident and too many copies for the tensor memory,
-    // two issuers take alternate chunks (each chunk's slot is used once).
+    // up: every chunk resident when it fits, else the deepest ring that fits.
+    // The gate products accumulate in ncu tensor-memory copies (copy k takes
+    // chunks k, k + ncu, ..; with a ring, ncu = slots, so a slot always feeds
+    // the same copy), and one warp issues each (copy, row tile) chain, so up
+    // to UP_ISSUERS warps issue side by side.  With every chunk resident, as
+    // many copies as fit the tensor memory and the issuers.
     bool fits_u = false;
     for (int u = std::min(g.nchunk_u, MAX_SLOTS); u >= 1 && !fits_u; --u) {
-      if (u < g.nchunk_u && u > UP_ISSUERS) continue;
+      if (u < g.nchunk_u && u * g.ntu > UP_ISSUERS) continue;
       g.nsl_u = u;
-      g.ncu = u >= g.nchunk_u ? g.nchunk_u : u;
-      if (u >= g.nchunk_u && g.ncu * g.ntu * g.Nu > 512) g.ncu = std::min(2, g.nchunk_u);
-      fits_u = g.ncu * g.ntu * g.Nu <= 512 && layout_up(c, g);
+      if (u >= g.nchunk_u) {
+        g.ncu = std::max(1, std::min(g.nchunk_u, UP_ISSUERS / g.ntu));
+        while (g.ncu > 1 && g.ncu * g.ntu * g.Nu > 512) --g.ncu;
+      } else {
+        g.ncu = u;
+      }
+      fits_u = g.ncu * g.ntu * g.Nu <= 512 && g.ncu * g.ntu <= UP_ISSUERS && layout_up(c, g);
     }
     if (!fits_u) continue;
     // down: one accumulator per row tile (one issuing warp each)
@@ -427,7 +432,9 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   };
   if (tid == 0) {
 #pragma unroll 1
-    for (int i = 0; i < 4 * MAX_SLOTS; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free, down and up
+    for (int i = 0; i < 3 * MAX_SLOTS; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free down, full up
+    // an up slot is free once the MMAs of each row tile (one issuer each) read it
+    for (int i = 0; i < MAX_SLOTS; ++i) mbar_init(free_u(i), g.ntu);
     mbar_init(barD, DOWN_ISSUERS);
     mbar_init(barG, UP_ISSUERS);
     fence_mbar_init();
@@ -857,37 +864,36 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     }
     if (tid == 0) HCGR_STAMP(9);
     // the gates on the tensor cores: D[row][m] = Wu[row] . h[m], rows (stream,
-    // channel) of this CTA's range; warp 2k + 1 (k < ncu) walks chunks k,
-    // k + ncu, .. (with a ring, always the same slot) into its own
-    // accumulator copy and one elected lane issues.  Every candidate warp
-    // commits barG.
+    // channel) of this CTA's range.  Warp 1 + k * ntu + t (k < ncu) walks
+    // chunks k, k + ncu, .. of row tile t (with a ring, always the same slot)
+    // into accumulator copy k and one elected lane issues.  Every candidate
+    // warp (1 .. UP_ISSUERS) commits barG.
     const uint32_t tmem = *s_tmem;
     up_issued = ok && nc > 0;
     if (up_issued) {
-      if ((warp & 1) == 1 && (warp >> 1) < UP_ISSUERS) {
-        const int me = warp >> 1;
+      if (warp >= 1 && warp <= UP_ISSUERS) {
+        const int me = warp - 1, kc = me / g.ntu, tu = me - kc * g.ntu;
         tc_fence_after();
         const uint32_t idesc = idesc_bf16(128, Nu);
+        const uint32_t d = tmem + (kc * g.ntu + tu) * Nu;
         bool okm = true;
 #pragma unroll 1
-        for (int q = me; q < nub && okm && me < g.ncu; q += g.ncu) {
+        for (int q = kc; q < nub && okm && me < g.ncu * g.ntu; q += g.ncu) {
           const int slot = q % g.nsl_u;
           const uint32_t ph = (q / g.nsl_u) & 1;
           okm = __all_sync(0xffffffffu,
                            mbar_test_wait(full_u(slot), ph) || wait_bar(full_u(slot), ph, p.err, p.limit_ns));
           if (!okm) break;
-          if (me == 0 && lane == 0 && q == me) HCGR_STAMP(27);
+          if (me == 0 && lane == 0 && q == kc) HCGR_STAMP(27);
           tc_fence_after();
-          const uint32_t a = ubase + slot * g.slot_u, bq = hbase + q * Nu * 128;
+          const uint32_t a = ubase + slot * g.slot_u + tu * TILE, bq = hbase + q * Nu * 128;
           if (elect_one()) {
 #pragma unroll 1
-            for (int tu = 0; tu < g.ntu; ++tu)
-#pragma unroll 1
-              for (int ks = 0; ks < 4; ++ks)
-                umma_bf16(tmem + (me * g.ntu + tu) * Nu, desc_sw128(a + tu * TILE + ks * 32),
-                          desc_sw128(bq + ks * 32), idesc, (q >= g.ncu || ks) ? 1u : 0u);
+            for (int ks = 0; ks < 4; ++ks)
+              umma_bf16(d, desc_sw128(a + ks * 32), desc_sw128(bq + ks * 32), idesc,
+                        (q >= g.ncu || ks) ? 1u : 0u);
             umma_commit(free_u(slot));
-            if (me == 0 && q == me) HCGR_STAMP(28);
+            if (me == 0 && q == kc) HCGR_STAMP(28);
           }
           __syncwarp();
         }

@@ -62,14 +62,15 @@ int main(int argc, char** argv) {
               g.tmem_u >= g.ncu * g.ntu * g.Nu, M, "tensor-memory columns");
     check(g.ntd <= hcgr::DOWN_ISSUERS && g.nchunk_u <= hcgr::UP_ISSUERS && g.ncu >= 1 &&
               g.ncu <= g.nchunk_u, M, "issuers");
-    // rings: every slot of a ring serves one issuer (the down ring's slot
-    // count a multiple of its row tiles, the up ring one issuer per slot)
+    // rings: every slot of the down ring serves one issuer (its slot count a
+    // multiple of its row tiles); every up slot feeds one accumulator copy,
+    // read by one issuer per row tile
     const int nbox = g.ntd * g.nkc;
     check(g.nsl_w >= 1 && g.nsl_w <= hcgr::MAX_SLOTS && (g.nsl_w >= nbox || g.nsl_w % g.ntd == 0),
           M, "down ring");
     check(g.nsl_u >= 1 && g.nsl_u <= hcgr::MAX_SLOTS &&
-              (g.nsl_u >= g.nchunk_u ? g.ncu == g.nchunk_u || g.ncu == 2
-                                     : g.ncu == g.nsl_u && g.ncu <= hcgr::UP_ISSUERS),
+              g.ncu * g.ntu <= hcgr::UP_ISSUERS &&
+              (g.nsl_u >= g.nchunk_u ? g.ncu >= 1 && g.ncu <= g.nchunk_u : g.ncu == g.nsl_u),
           M, "up ring");
     // down role regions: header arrays, operands, weight slots
     check(g.d_ss1 >= hcgr::HDR && g.d_ssum >= g.d_ss1 + g.Nt * g.nkc * 8 * 4, M, "down header arrays");
