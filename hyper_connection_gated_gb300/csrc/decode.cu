@@ -950,20 +950,30 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
         }
         HCGR_STAMP_MAX(21);
         __syncthreads();
+        // a thread takes a channel pair of one token (nc, nc_max and cp0 are
+        // even): paired shared-memory loads and one 4-byte store of x
+        const int npr = nc / 2;
 #pragma unroll 1
-        for (int i = tid; i < M * nc; i += NT) {
-          const int m = i / nc, cc = i - m * nc, ch = cp0 + cc;
-          float sum = 0.f;
-#pragma unroll 1
+        for (int i = tid; i < M * npr; i += NT) {
+          const int m = i / npr, cc = 2 * (i - m * npr), ch = cp0 + cc;
+          const uint32_t yp = has_y ? *reinterpret_cast<const uint32_t*>(s_x3y + m * g.nc_max + cc) : 0u;
+          float sum0 = 0.f, sum1 = 0.f;
+#pragma unroll 4
           for (int ss = 0; ss < HC; ++ss) {
-            const float rv = bf16_to_f32(s_x3r[(m * HC + ss) * g.nc_max + cc]);
-            const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(bf16_to_f32(s_x3y[m * g.nc_max + cc]),
-                                                                  s_iw[m * HC + ss], rv)))
-                                   : rv;
-            const float xn = r2 * s_rr[m * HC + ss] * (1.0f + bf16_to_f32(s_x3w[ss * g.nc_max + cc]));
-            sum = fmaf(s_g[m * g.rows_u + ss * g.nc_max + cc], xn, sum);
+            const uint32_t rp = *reinterpret_cast<const uint32_t*>(s_x3r + (m * HC + ss) * g.nc_max + cc);
+            const uint32_t wp = *reinterpret_cast<const uint32_t*>(s_x3w + ss * g.nc_max + cc);
+            const float2 gp = *reinterpret_cast<const float2*>(s_g + m * g.rows_u + ss * g.nc_max + cc);
+            const float iw = s_iw[m * HC + ss], rr = s_rr[m * HC + ss];
+            float r0 = lo_bf16(rp), r1 = hi_bf16(rp);
+            if (has_y) {
+              r0 = bf16_to_f32(f32_to_bf16(fmaf(lo_bf16(yp), iw, r0)));
+              r1 = bf16_to_f32(f32_to_bf16(fmaf(hi_bf16(yp), iw, r1)));
+            }
+            sum0 = fmaf(gp.x, r0 * rr * (1.0f + lo_bf16(wp)), sum0);
+            sum1 = fmaf(gp.y, r1 * rr * (1.0f + hi_bf16(wp)), sum1);
           }
-          c.x[static_cast<int64_t>(m) * HS + ch] = f32_to_bf16(sum * inv_hc);
+          *reinterpret_cast<uint32_t*>(c.x + static_cast<int64_t>(m) * HS + ch) =
+              pack2(sum0 * inv_hc, sum1 * inv_hc);
         }
         HCGR_STAMP_MAX(22);
       }

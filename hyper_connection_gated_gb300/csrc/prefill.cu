@@ -956,7 +956,10 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
                            cudaStream_t stream) {
   if (!prefill_supported(c)) return cudaErrorNotSupported;
   // hc_gr_args.pdl: K1 as a programmatic dependent of the previous kernel in
-  // the stream, the reduce of K1 and K2 of the reduce
+  // the stream.  The reduce (of K1) and K2 (of the reduce) are always
+  // programmatic dependents: their predecessors are this call's own kernels,
+  // and each waits for its predecessor's end before it touches memory, so
+  // their prologues and launches overlap the predecessor's tail in either mode.
   const bool pdl = c.pdl != 0;
   if (prefill_ws_bytes(c.M, c.HC, c.HS, c.r) > ws.prefill_bytes) return cudaErrorNotSupported;
   const int M = static_cast<int>(c.M);
@@ -1089,7 +1092,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   case HCV:                                                                                  \
     e = launch_maybe_pdl(batch2 ? k1_reduce_kernel<HCV, (HCV <= 4 ? 2 : 1)>                \
                                 : k1_reduce_kernel<HCV, 1>,                                  \
-                         grid, dim3(RED_THREADS), 0, stream, pdl, (const float*)part,         \
+                         grid, dim3(RED_THREADS), 0, stream, true, (const float*)part,        \
                          (const float*)sumsq, c.rrms, c.lora, c.inj_next, h, c.Wnorm,         \
                          static_cast<int>(c.ld_wnorm), w1, M, S, c.r, np, c.HS, 1.0f / c.HS,  \
                          c.eps);                                                              \
@@ -1154,14 +1157,14 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
     const int grid = std::min(p.n_units, dev.sms);
     cudaError_t e = cudaSuccess;
     switch (c.HC) {
-      case 1: e = launch_k2<1>(p, grid, smem, dev, stream, pdl); break;
-      case 2: e = launch_k2<2>(p, grid, smem, dev, stream, pdl); break;
-      case 3: e = launch_k2<3>(p, grid, smem, dev, stream, pdl); break;
-      case 4: e = launch_k2<4>(p, grid, smem, dev, stream, pdl); break;
-      case 5: e = launch_k2<5>(p, grid, smem, dev, stream, pdl); break;
-      case 6: e = launch_k2<6>(p, grid, smem, dev, stream, pdl); break;
-      case 7: e = launch_k2<7>(p, grid, smem, dev, stream, pdl); break;
-      default: e = launch_k2<8>(p, grid, smem, dev, stream, pdl); break;
+      case 1: e = launch_k2<1>(p, grid, smem, dev, stream, true); break;
+      case 2: e = launch_k2<2>(p, grid, smem, dev, stream, true); break;
+      case 3: e = launch_k2<3>(p, grid, smem, dev, stream, true); break;
+      case 4: e = launch_k2<4>(p, grid, smem, dev, stream, true); break;
+      case 5: e = launch_k2<5>(p, grid, smem, dev, stream, true); break;
+      case 6: e = launch_k2<6>(p, grid, smem, dev, stream, true); break;
+      case 7: e = launch_k2<7>(p, grid, smem, dev, stream, true); break;
+      default: e = launch_k2<8>(p, grid, smem, dev, stream, true); break;
     }
     if (e != cudaSuccess) return e;
   }

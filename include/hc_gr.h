@@ -138,10 +138,13 @@ typedef struct hc_gr_args {
                           that kernel has finished, so that kernel must not
                           write them; activations are read and outputs written
                           only after it has finished.  Prefill: K1's prologue
-                          overlaps the previous kernel, the stream reduce is a
-                          dependent of K1 and K2 of the reduce; each waits for
-                          its predecessor before touching memory.  0: plain
-                          stream order. */
+                          overlaps the previous kernel (K1 touches memory
+                          only after it has finished).  0: plain stream
+                          order for the call's first kernel.  Inside a
+                          prefill call the stream reduce is always a
+                          dependent of K1 and K2 of the reduce, whatever this
+                          field; each waits for its predecessor to finish
+                          before it touches memory. */
   int32_t wnorm_hs;    /* 1: Wnorm has HS entries, one per channel, shared by
                           every stream (xn[s, c] = R2[s, c] rrms[s]
                           (1 + Wnorm[c])); 0: the full-width [K] layout.  A
