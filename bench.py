@@ -889,9 +889,12 @@ TRACE_PHASES = {0: "start", 1: "prologue done", 2: "previous kernel done", 3: "C
                 24: "issuer 0: first box landed", 25: "issuer 0: first MMAs issued",
                 26: "last thread out of the gather loop", 27: "issuer 0: first chunk landed",
                 28: "issuer 0: first gate MMAs issued", 29: "mix inputs landed",
-                30: "down MMA completion seen", 31: "gate MMA completion seen"}
-DOWN_PHASES = (0, 13, 14, 1, 2, 3, 24, 25, 4, 30, 5, 23, 16, 6, 12)
-UP_PHASES = (0, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 29, 26, 9, 27, 28, 15, 31, 10, 21, 22, 11, 12)
+                30: "down MMA completion seen", 31: "gate MMA completion seen",
+                32: "thread 0: before the barrier init", 33: "thread 0: barriers initialised",
+                34: "last thread at the prologue barrier"}
+DOWN_PHASES = (0, 32, 33, 34, 13, 14, 1, 2, 3, 24, 25, 4, 30, 5, 23, 16, 6, 12)
+UP_PHASES = (0, 32, 33, 34, 13, 14, 1, 2, 17, 18, 19, 20, 7, 8, 29, 26, 9, 27, 28, 15, 31, 10, 21, 22,
+             11, 12)
 
 
 def decode_trace(args):
@@ -932,7 +935,7 @@ def decode_trace(args):
     a = inputs.activations(32, shape)
     base = dict(w, R=bf(a["R"]), y=bf(a["y"]), inj=torch.from_numpy(a["inj"]).cuda())
     sets = [{k: v.clone() for k, v in base.items()} for _ in range(nsets)]
-    slots = 32
+    slots = 36
     n = 256 * slots
     buf = np.zeros(n, dtype=np.uint64)
     report = {}

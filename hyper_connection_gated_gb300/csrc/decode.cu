@@ -80,6 +80,8 @@ constexpr int MAX_SLOTS = 16;        // ring slots per weight stream
 constexpr int XU = 8;                // exchange loads a thread keeps in flight
 constexpr int DOWN_ISSUERS = 8;      // threads that may issue the down MMAs (one per row tile)
 constexpr uint64_t PF_CHUNK = 16384;   // bytes per L2 prefetch of the weights
+constexpr int PF_FIRST_THREAD = 128;   // the weight prefetches are issued by threads from here
+constexpr int PF_INPUT_THREAD = 256;   // the COMBINE-input prefetches by threads from here
 constexpr int UP_ISSUERS = 15;       // warps that may issue the gate MMAs (one per copy and row tile)
 constexpr int TILE = 16384;          // 128 rows x 64 bf16, 128-byte swizzle
 constexpr int HDR = 1024;            // mbarriers, TMEM address, flags
@@ -274,7 +276,7 @@ __device__ __noinline__ void drain_bar(uint32_t bar, uint32_t parity, long long 
 
 
 #ifdef HCGR_TRACE
-constexpr int TRACE_SLOTS = 32;
+constexpr int TRACE_SLOTS = 36;
 __device__ unsigned long long g_trace[MAX_GRID * TRACE_SLOTS];
 __device__ __forceinline__ unsigned long long globaltimer_ns() {
   unsigned long long t;
@@ -309,8 +311,11 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // serves at about two thirds of the rate) from the kernel's first
   // instructions on, and the box copies issued later mostly hit L2.  The
   // weights never depend on the previous kernel, so this precedes
-  // griddepcontrol.wait.
-  {
+  // griddepcontrol.wait.  Warps 4.. issue them: the prologue's other jobs
+  // (barrier initialisation in warps 0-2, the call ticket in the last warp)
+  // then run side by side, since a thread's second bulk copy instruction
+  // waits for its first to be taken.
+  if (threadIdx.x >= PF_FIRST_THREAD) {
     const uint64_t G = gridDim.x, me = blockIdx.x;
     const uint64_t rK = static_cast<uint64_t>(c.r) * c.K, hK = static_cast<uint64_t>(c.HC) * c.K;
     const bool merged_w = c.Wi == c.Wd + rK;
@@ -328,7 +333,7 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     const int n1 = static_cast<int>((hi1 - lo1 + PF_CHUNK - 1) / PF_CHUNK);
     const int n2 = static_cast<int>((hi2 - lo2 + PF_CHUNK - 1) / PF_CHUNK);
 #pragma unroll 1
-    for (int i = threadIdx.x; i < n0 + n1 + n2; i += NT) {
+    for (int i = threadIdx.x - PF_FIRST_THREAD; i < n0 + n1 + n2; i += NT - PF_FIRST_THREAD) {
       const char* src;
       uint64_t a, end;
       if (i < n0) {
@@ -371,13 +376,14 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // the Wnorm slice) into L2 as well: L2 is the point of coherence, so a
   // prefetch before griddepcontrol.wait never hands out data older than a
   // write the previous kernel makes (it only warms the lines).
-  if (down && nkv > 0 && tid <= 2 * M) {
+  if (down && nkv > 0 && tid >= PF_INPUT_THREAD && tid - PF_INPUT_THREAD <= 2 * M) {
+    const int j = tid - PF_INPUT_THREAD;
     const uint32_t sb = static_cast<uint32_t>(min(64 * g.nkc, HS - c0)) * 2;
-    if (tid < M)
-      bulk_prefetch_l2(c.R + static_cast<int64_t>(tid) * K + k0, sb);
-    else if (tid < 2 * M && has_y)
-      bulk_prefetch_l2(c.y + static_cast<int64_t>(tid - M) * HS + c0, sb);
-    else if (tid == 2 * M)
+    if (j < M)
+      bulk_prefetch_l2(c.R + static_cast<int64_t>(j) * K + k0, sb);
+    else if (j < 2 * M && has_y)
+      bulk_prefetch_l2(c.y + static_cast<int64_t>(j - M) * HS + c0, sb);
+    else if (j == 2 * M)
       bulk_prefetch_l2(c.Wnorm + s * c.ld_wnorm + c0, sb);
   }
   const int u_idx = down ? 0 : b - g.Gd;
@@ -430,16 +436,25 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
       *s_epoch = static_cast<uint32_t>(ticket_old >> 32);
     }
   };
-  if (tid == 0) {
-#pragma unroll 1
-    for (int i = 0; i < 3 * MAX_SLOTS; ++i) mbar_init(bar0 + 8u * i, 1);   // full/free down, full up
-    // an up slot is free once the MMAs of each row tile (one issuer each) read it
-    for (int i = 0; i < MAX_SLOTS; ++i) mbar_init(free_u(i), g.ntu);
-    mbar_init(barD, DOWN_ISSUERS);
-    mbar_init(barG, UP_ISSUERS);
+  // Barrier initialisation, one barrier per thread of warps 0-2 (one thread
+  // initialising all of them in turn took ~1 µs): full/free of the down
+  // ring and full of the up ring count one arrival; an up slot is free once
+  // the MMAs of each row tile (one issuer each) have read it; barD and barG
+  // take one commit per candidate issuer warp.
+  if (tid == 0) HCGR_STAMP(32);
+  if (tid < 4 * MAX_SLOTS + 2) {
+    const uint32_t count = tid < 3 * MAX_SLOTS ? 1u
+                           : tid < 4 * MAX_SLOTS ? static_cast<uint32_t>(g.ntu)
+                           : tid == 4 * MAX_SLOTS ? static_cast<uint32_t>(DOWN_ISSUERS)
+                                                  : static_cast<uint32_t>(UP_ISSUERS);
+    mbar_init(bar0 + 8u * tid, count);
     fence_mbar_init();
-    *s_mma_ok = 1;
   }
+  if (tid == 0) {
+    *s_mma_ok = 1;
+    HCGR_STAMP(33);
+  }
+  HCGR_STAMP_MAX(34);
   __syncthreads();
   if (tid == 0) HCGR_STAMP(13);
   if (lane == 0) {

@@ -5,7 +5,7 @@
  * libhc_gr_trace.so, the same sources compiled with HCGR_TRACE defined
  * (hyper_connection_gated_gb300/build.py, build(trace=True)).  In that build
  * thread 0 of every decode CTA records %globaltimer (ns) at fixed points of
- * the kernel into a device array of 32 slots per CTA:
+ * the kernel into a device array of 36 slots per CTA:
  *   0 start, 1 prologue done (weight copies issued, TMEM allocated),
  *   2 previous kernel finished (griddepcontrol.wait returned),
  *   down CTAs: 3 COMBINE done, 4 the first issuer's last weight box landed
@@ -25,7 +25,9 @@
  *   thread out of the all-gather loop; 27/28 the first up issuer's first
  *   chunk landed / its MMAs issued; 29 (up) the mix inputs landed;
  *   30 (down) the down MMAs' completion seen; 31 (up) the gate MMAs'
- *   completion seen.
+ *   completion seen; 32/33 thread 0 before / after the barrier
+ *   initialisation; 34 the last thread at the prologue's CTA barrier;
+ *   35 unused.
  * Slots a CTA does not pass read 0 (every read clears the array).
  */
 #ifndef HC_GR_TRACE_H_
@@ -35,7 +37,7 @@
 extern "C" {
 #endif
 
-/* Copies n <= 256 * 32 values ([CTA][32], CTA = blockIdx.x of the last
+/* Copies n <= 256 * 36 values ([CTA][36], CTA = blockIdx.x of the last
  * decode launch) to host memory, then zeroes the device array.  Returns the
  * CUDA status (0 = success). */
 int hc_gr_trace_read(unsigned long long* host, int n);
