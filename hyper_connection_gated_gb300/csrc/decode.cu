@@ -204,9 +204,10 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     g.nquad = g.row / 4;
     if (g.nquad > NT) return false;
     // reducer: R sub-ranges (a power of two, consecutive lanes) of ppr
-    // pieces per stream and quad
+    // pieces per stream and quad; at most 4, so that a lane keeps several
+    // loads in flight and the shuffle tree is at most two levels deep
     g.R = 1;
-    while (2 * g.R <= 32 && 2 * g.R * c.HC * g.nquad <= NT) g.R *= 2;
+    while (2 * g.R <= 4 && 2 * g.R * c.HC * g.nquad <= NT) g.R *= 2;
     g.ppr = (g.P + g.R - 1) / g.R;
     g.L2w = round_up(c.r / 2 + c.HC, 4);     // h pairs, then rrms, then pad words
     // down: every box resident when they fit, else the deepest ring that
