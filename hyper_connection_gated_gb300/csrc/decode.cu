@@ -179,7 +179,8 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
   const int sms = std::min(dev.sms, MAX_GRID);
   // Every feasible slice size is planned; the plan kept is the one whose
   // larger per-CTA weight share (down: rows x slice, up: channel rows x r) is
-  // smallest, since every CTA streams its share at about the same rate.
+  // smallest, since every CTA streams its share at about the same rate (the
+  // up share weighted by 2 from 24 tokens, see below).
   Geom best;
   long long best_bytes = -1;
   for (g.nkc = 1; g.nkc <= hsc; ++g.nkc) {
@@ -249,9 +250,14 @@ bool make_geom(const Call& c, const Device& dev, Geom& g) {
     g.total = std::max(std::max(g.d_total, g.u_total), SMEM_MIN - 1024);
     // a kernel that allocates TMEM runs one CTA per SM
     if (g.G > dev.sms) continue;
+    // From about 24 tokens the up role's per-token work (the gather, the gate
+    // readback and the gated mean, all proportional to its channel range)
+    // outweighs the down role's extra MMAs, so the up share counts double:
+    // measured at the default shape, 56 down / 96 up CTAs take 1.2 us less
+    // than 80 / 72 at M = 32 and up to 1.1 us more at M <= 8.
     const long long down_b = static_cast<long long>(g.rows_w + (g.merged ? 0 : c.HC)) * g.nkc * 128;
     const long long up_b = static_cast<long long>(g.rows_u) * c.r * 2;
-    const long long share = std::max(down_b, up_b);
+    const long long share = std::max(down_b, (M >= 24 ? 2 : 1) * up_b);
     if (best_bytes < 0 || share < best_bytes) {
       best = g;
       best_bytes = share;

@@ -253,12 +253,14 @@ int hc_gr_forward_ex(hc_gr_handle h, const hc_gr_args* a, struct CUstream_st* st
   DeviceGuard guard(h->dev.id);
   // M-based dispatch (the page's split between a skinny decode path and the
   // tiled kernels, "Behavior and intent"): the weight-streaming decode kernel
-  // up to the measured crossover DECODE_AUTO_MAX_M, the tensor-core prefill
-  // kernels above it (and for shapes the decode kernel's plan cannot hold).
+  // up to the measured crossover (M <= DECODE_MAX_M and M * K <=
+  // DECODE_AUTO_MAX_MK), the tensor-core prefill kernels above it (and for
+  // shapes the decode kernel's plan cannot hold).
   cudaError_t e;
   if (a->force_path == HC_GR_PATH_DECODE) {
     e = hcgr::launch_decode(c, h->ws, h->dev, s);
-  } else if (a->force_path == HC_GR_PATH_PREFILL || M > hcgr::DECODE_AUTO_MAX_M) {
+  } else if (a->force_path == HC_GR_PATH_PREFILL || M > hcgr::DECODE_MAX_M ||
+             M * c.K > hcgr::DECODE_AUTO_MAX_MK) {
     e = hcgr::launch_prefill(c, h->ws, h->dev, s);
   } else {
     e = hcgr::launch_decode(c, h->ws, h->dev, s);

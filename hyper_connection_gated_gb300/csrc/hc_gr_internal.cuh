@@ -79,13 +79,16 @@ inline cudaError_t smem_limit_once(const void* func, int bytes, int device,
 
 // Decode path (M <= DECODE_MAX_M): one persistent kernel.
 constexpr int DECODE_MAX_M = 64;
-// The M dispatch's threshold: the decode kernel for M <= DECODE_AUTO_MAX_M,
-// the prefill kernels above.  Measured on the GB300 at HC=4, HS=2560, r=320
-// (graph replay, weights from HBM, programmatic dependent launches): decode
-// 16.5 / 18.6 / 22.6 / 23.8 / 25.9 / 27.0 us at M = 24 / 32 / 40 / 48 / 56 /
-// 64 against prefill 25.9 / 26.2 / 26.2 / 26.2 / 26.3 / 26.4 us, so the paths
-// cross between 56 and 64 tokens.
-constexpr int DECODE_AUTO_MAX_M = 56;
+// The M dispatch's threshold: the decode kernel while M <= DECODE_MAX_M and
+// M * K <= DECODE_AUTO_MAX_MK, the prefill kernels above.  Measured on the
+// GB300 (graph replay, weights from HBM, programmatic dependent launches):
+// at HC=4, HS=2560, r=320 (K = 10240) decode takes 14.9 / 16.5 / 19.0 / 21.1 /
+// 22.5 / 23.3 us at M = 24 / 32 / 40 / 48 / 56 / 64 against 25.9 - 26.2 us for
+// prefill, so decode wins up to its 64-token limit; at HC=8, HS=4096, r=512
+// (K = 32768) decode takes 39.2 / 51.4 us at M = 16 / 24 against 50.0 / 50.4
+// us, so the paths cross near 20 tokens.  Both crossovers sit at about the
+// same M * K: the decode kernel's per-token work grows with the width K.
+constexpr int64_t DECODE_AUTO_MAX_MK = 64LL * 10240;
 constexpr int MAX_GRID = 256;            // largest prefill grid the scratch is sized for
 constexpr int CTL_BYTES = MAX_GRID * 8 + 256;   // ticket at 0, status word at MAX_GRID * 8
 // Exchange words the decode kernel needs for one call (0: shape unsupported).

@@ -96,8 +96,10 @@ typedef enum hc_gr_status {
 /* Dispatch between the two kernel families (the page's "Behavior and intent":
  * a skinny decode path for few tokens beside the tiled two-kernel path). */
 typedef enum hc_gr_path {
-  HC_GR_PATH_AUTO = 0,    /* M <= 56 (the measured crossover): decode kernel,
-                             otherwise prefill kernels */
+  HC_GR_PATH_AUTO = 0,    /* M <= 64 and M * HC * HS <= 64 * 10240 (the
+                             measured crossover: 64 tokens at HC=4, HS=2560;
+                             20 at HC=8, HS=4096): decode kernel, otherwise
+                             (or where its plan does not fit) prefill */
   HC_GR_PATH_DECODE = 1,  /* weight-streaming persistent kernel, M <= 64 */
   HC_GR_PATH_PREFILL = 2  /* tensor-core (tcgen05) two-stage kernels */
 } hc_gr_path;

@@ -132,16 +132,19 @@ def test_decode_beyond_32_tokens(torch_cuda, case64, M):
     tl.assert_parity(out, tl.oracle_ref(case), label=f"decode M={M}")
 
 
-@pytest.mark.parametrize("M", [33, 56, 57, 511])
-def test_auto_dispatch_around_the_crossover(torch_cuda, M):
-    # PATH_AUTO takes the decode kernel up to the measured crossover (56
-    # tokens) and the prefill kernels above; both sides of it, and the last
-    # M before the prefill-only sizes, match the oracle
+@pytest.mark.parametrize("M,wide", [(33, False), (64, False), (65, False), (511, False),
+                                    (20, True), (21, True)])
+def test_auto_dispatch_around_the_crossover(torch_cuda, M, wide):
+    # PATH_AUTO takes the decode kernel up to the measured crossover (M * K up
+    # to 64 tokens at K = 10240: 64 tokens at the default shape, 20 at the
+    # wide one) and the prefill kernels above; both sides of it, at both
+    # shapes, match the oracle
     from hyper_connection_gated_gb300 import PATH_AUTO
 
-    case = tl.make_case(M, seed=72)
+    shape = inputs.WIDE if wide else inputs.DEFAULT
+    case = tl.make_case(M, seed=72, shape=shape)
     d = tl.device_case(case)
-    with HcGatedResidual(max_M=M) as op:
+    with HcGatedResidual(max_M=M, HC=shape.HC, HS=shape.HS, r=shape.r) as op:
         out = op.forward(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"],
                          force_path=PATH_AUTO, check=True)
     tl.assert_parity(out, tl.oracle_ref(case), label=f"auto M={M}")
