@@ -321,8 +321,12 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
   // griddepcontrol.wait.  Warps 4.. issue them: the prologue's other jobs
   // (barrier initialisation in warps 0-2, the call ticket in the last warp)
   // then run side by side, since a thread's second bulk copy instruction
-  // waits for its first to be taken.
-  if (threadIdx.x >= PF_FIRST_THREAD) {
+  // waits for its first to be taken.  Only when every CTA holds its whole
+  // share in shared memory: with rings (weights larger than the SMs' shared
+  // memory) the early stream of all the weights competes with the boxes the
+  // rings need first, and measured slower.
+  const bool resident = g.nsl_w >= g.ntd * g.nkc && g.nsl_u >= g.nchunk_u;
+  if (resident && threadIdx.x >= PF_FIRST_THREAD) {
     const uint64_t G = gridDim.x, me = blockIdx.x;
     const uint64_t rK = static_cast<uint64_t>(c.r) * c.K, hK = static_cast<uint64_t>(c.HC) * c.K;
     const bool merged_w = c.Wi == c.Wd + rK;
