@@ -47,8 +47,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # since, roofline.traffic is null and roofline.traffic_source says why.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "e793798bc6625aef7145c9bb03fb7bec2100522e73f69caf0ac5f2f22d7e0907",
-    "bytes": {2: 13339392, 4: 13391616, 8: 13496320, 16: 13699328, 32: 14127104},
+    "sources_sha256": "7e2d38f35bb8b547e82a588074b5f45839f8510ea6a71eeaf5d721ab823a18fb",
+    "bytes": {2: 13620480, 4: 13918379, 8: 14421931, 16: 15513429, 32: 16540160},
 }
 
 
