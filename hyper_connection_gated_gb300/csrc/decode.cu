@@ -501,46 +501,73 @@ __global__ void __launch_bounds__(NT, 1) decode_kernel(const __grid_constant__ P
     // swizzled layout (16-byte unit u of row m of a chunk at (u ^ (m & 7)) *
     // 16; hi in rows m, lo in rows Nt + m)
     const int nu = g.nkc * 8;                                  // 16-byte units per row
+    const int nitem = Nt * nu;
+    // a thread takes two items per pass and issues all their loads before it
+    // uses any, so that a CTA with more items than threads waits through one
+    // round of input loads, not two
 #pragma unroll 1
-    for (int it = tid; it < Nt * nu; it += NT) {
-      const int m = it / nu, un = it - m * nu;
-      const int ch = un >> 3, uu = un & 7;
-      uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
-      float ss = 0.f;
-      if (m < M && ch < nkv) {
-        const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
-        float rv[8], yv[8] = {}, wv[8], a[8];
-        float iw = 0.f;
-        unpack8(__ldg(reinterpret_cast<const uint4*>(c.R + kk)), rv);
-        if (has_y) {
-          iw = combine_weight(c.inj[m * c.ld_inj + s], inv_hc);
-          unpack8(__ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8)), yv);
-        }
-        unpack8(__ldg(reinterpret_cast<const uint4*>(c.Wnorm + s * c.ld_wnorm + c0 + un * 8)), wv);
-        uint32_t pr[4], ph[4], pl[4];
+    for (int it0 = tid; it0 < nitem; it0 += 2 * NT) {
+      uint4 rq[2], yq[2], wq[2];
+      float injv[2] = {0.f, 0.f};
+      bool val[2];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(yv[i], iw, rv[i]))) : rv[i];
-          ss = fmaf(r2, r2, ss);
-          rv[i] = r2;
-          a[i] = c.fold ? r2 : r2 * (1.0f + wv[i]);
+      for (int e = 0; e < 2; ++e) {
+        const int it = it0 + e * NT;
+        const int m = it / nu, un = it - m * nu;
+        val[e] = it < nitem && m < M && (un >> 3) < nkv;
+        rq[e] = yq[e] = wq[e] = make_uint4(0, 0, 0, 0);
+        if (val[e]) {
+          rq[e] = __ldg(reinterpret_cast<const uint4*>(c.R + static_cast<int64_t>(m) * K + k0 + un * 8));
+          if (has_y) {
+            injv[e] = c.inj[m * c.ld_inj + s];
+            yq[e] = __ldg(reinterpret_cast<const uint4*>(c.y + static_cast<int64_t>(m) * HS + c0 + un * 8));
+          }
+          wq[e] = __ldg(reinterpret_cast<const uint4*>(c.Wnorm + s * c.ld_wnorm + c0 + un * 8));
         }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          pr[i] = pack2(rv[2 * i], rv[2 * i + 1]);
-          const float h0 = bf16_to_f32(f32_to_bf16(a[2 * i]));
-          const float h1 = bf16_to_f32(f32_to_bf16(a[2 * i + 1]));
-          ph[i] = pack2(h0, h1);
-          pl[i] = pack2(a[2 * i] - h0, a[2 * i + 1] - h1);
-        }
-        if (c.R2) *reinterpret_cast<uint4*>(c.R2 + kk) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
-        hv = make_uint4(ph[0], ph[1], ph[2], ph[3]);
-        lv = make_uint4(pl[0], pl[1], pl[2], pl[3]);
       }
-      const int sw = ch * Nd * 128 + m * 128 + ((uu ^ (m & 7)) << 4);
-      *reinterpret_cast<uint4*>(smem + g.d_act + sw) = hv;
-      *reinterpret_cast<uint4*>(smem + g.d_act + sw + Nt * 128) = lv;
-      s_ss1[m * nu + un] = ss;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int it = it0 + e * NT;
+        if (it >= nitem) break;
+        const int m = it / nu, un = it - m * nu;
+        const int ch = un >> 3, uu = un & 7;
+        uint4 hv = make_uint4(0, 0, 0, 0), lv = make_uint4(0, 0, 0, 0);
+        float ss = 0.f;
+        if (val[e]) {
+          const int64_t kk = static_cast<int64_t>(m) * K + k0 + un * 8;
+          float rv[8], yv[8] = {}, wv[8], a[8];
+          float iw = 0.f;
+          unpack8(rq[e], rv);
+          if (has_y) {
+            iw = combine_weight(injv[e], inv_hc);
+            unpack8(yq[e], yv);
+          }
+          unpack8(wq[e], wv);
+          uint32_t pr[4], ph[4], pl[4];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const float r2 = has_y ? bf16_to_f32(f32_to_bf16(fmaf(yv[i], iw, rv[i]))) : rv[i];
+            ss = fmaf(r2, r2, ss);
+            rv[i] = r2;
+            a[i] = c.fold ? r2 : r2 * (1.0f + wv[i]);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            pr[i] = pack2(rv[2 * i], rv[2 * i + 1]);
+            const float h0 = bf16_to_f32(f32_to_bf16(a[2 * i]));
+            const float h1 = bf16_to_f32(f32_to_bf16(a[2 * i + 1]));
+            ph[i] = pack2(h0, h1);
+            pl[i] = pack2(a[2 * i] - h0, a[2 * i + 1] - h1);
+          }
+          if (c.R2) *reinterpret_cast<uint4*>(c.R2 + kk) = make_uint4(pr[0], pr[1], pr[2], pr[3]);
+          hv = make_uint4(ph[0], ph[1], ph[2], ph[3]);
+          lv = make_uint4(pl[0], pl[1], pl[2], pl[3]);
+        }
+        const int sw = ch * Nd * 128 + m * 128 + ((uu ^ (m & 7)) << 4);
+        *reinterpret_cast<uint4*>(smem + g.d_act + sw) = hv;
+        *reinterpret_cast<uint4*>(smem + g.d_act + sw + Nt * 128) = lv;
+        s_ss1[m * nu + un] = ss;
+      }
     }
     fence_proxy_async_smem();   // the operand rows are read by the tensor cores
     take_ticket();

@@ -74,8 +74,10 @@ def test_decode_strided_inj(torch_cuda, case32):
     tl.assert_parity(out, tl.oracle_ref(case), label="strided inj")
 
 
-@pytest.mark.parametrize("M", [1, 8])
+@pytest.mark.parametrize("M", [1, 8, 24, 32])
 def test_decode_wide_variant(torch_cuda, M):
+    # M = 1, 8: the two-role plan with rings on both roles; from 24 tokens the
+    # planner moves to more up CTAs (only a forced decode reaches those plans)
     case = tl.make_case(M, inputs.WIDE)
     d = tl.device_case(case)
     with HcGatedResidual(max_M=32, HC=8, HS=4096, r=512) as op:
