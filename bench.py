@@ -47,8 +47,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # since, roofline.traffic is null and roofline.traffic_source says why.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "7e2d38f35bb8b547e82a588074b5f45839f8510ea6a71eeaf5d721ab823a18fb",
-    "bytes": {2: 13620480, 4: 13918379, 8: 14421931, 16: 15513429, 32: 16540160},
+    "sources_sha256": "0e773a3c70d1bd38f2365eb4bcb9828e23498b57f6a395069ddd5a91e6df9e29",
+    "bytes": {2: 13625685, 4: 13923840, 8: 14427477, 16: 15518976, 32: 16553131},
 }
 
 
