@@ -47,8 +47,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # since, roofline.traffic is null and roofline.traffic_source says why.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "0e773a3c70d1bd38f2365eb4bcb9828e23498b57f6a395069ddd5a91e6df9e29",
-    "bytes": {2: 13625685, 4: 13923840, 8: 14427477, 16: 15518976, 32: 16553131},
+    "sources_sha256": "3494ce2db83f400b10ba3099c388ec183bbf052edff4753dd21c37cee675adbd",
+    "bytes": {2: 13580885, 4: 13864277, 8: 14429355, 16: 15526229, 32: 16545536},
 }
 
 

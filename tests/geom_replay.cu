@@ -90,7 +90,8 @@ int main(int argc, char** argv) {
     check(g.rows_u == HC * g.nc_max && g.ntu * 128 >= g.rows_u && g.slot_u >= g.rows_u * 128, M,
           "up rows");
     // exchanges
-    check(g.Qn % 4 == 0 && g.Jm * g.Qn >= n_out && (M * g.Jm <= g.Gu || g.Jm == 1), M,
+    check(g.Qn % 4 == 0 && g.Jm * g.Qn >= n_out && (M * g.Jm <= g.Gu || g.Jm == 1) &&
+              g.Qn >= std::min(hcgr::QN_MIN, (n_out + 3) / 4 * 4) && g.Qn < n_out + 4, M,
           "reduce-scatter blocks");
     check(g.row == g.Qn + 4 && g.nquad * 4 == g.row && g.nquad <= hcgr::NT, M, "block rows");
     // (items beyond NT loop; sub-ranges of one (stream, quad) stay in one warp)
