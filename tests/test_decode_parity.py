@@ -150,3 +150,20 @@ def test_auto_dispatch_around_the_crossover(torch_cuda, M, wide):
         out = op.forward(d["R"], d["y"], d["inj"], d["Wnorm"], d["Wu"], Wd=d["Wd"], Wi=d["Wi"],
                          force_path=PATH_AUTO, check=True)
     tl.assert_parity(out, tl.oracle_ref(case), label=f"auto M={M}")
+
+
+def test_decode_token_counts_alternate_on_one_handle(torch_cuda, case32, ref32):
+    # consecutive calls of one handle with different plans (block sizes,
+    # role splits) and both launch modes: each call leaves the reduce-scatter
+    # words empty and the all-gather copy of the next parity ready
+    torch = torch_cuda
+    d = tl.device_case(case32)
+    seq = [(1, False), (2, True), (8, True), (1, True), (1, True), (32, False), (2, False),
+           (2, True), (4, True), (1, False), (3, True), (2, True)]
+    with HcGatedResidual(max_M=32) as op:
+        outs = [op.forward(d["R"][:M], d["y"][:M], d["inj"][:M], d["Wnorm"], d["Wu"], Wd=d["Wd"],
+                           Wi=d["Wi"], force_path=PATH_DECODE, pdl=pdl) for M, pdl in seq]
+        op.check()
+        torch.cuda.synchronize()
+    for (M, pdl), out in zip(seq, outs):
+        tl.assert_parity(out, {k: v[:M] for k, v in ref32.items()}, label=f"M={M} pdl={pdl}")

@@ -59,8 +59,8 @@ def test_noalloc_matches_oracle_and_forward_on_two_calls(torch_cuda):
     stream = torch.cuda.current_stream()
     with HcGatedResidual(max_M=8) as op:
         # two calls in a row with a caller lora, then two with lora = NULL,
-        # all sharing the one scratch array
-        for M, with_lora in ((4, True), (8, True), (8, False), (3, False)):
+        # then the smallest token counts, all sharing the one scratch array
+        for M, with_lora in ((4, True), (8, True), (8, False), (3, False), (1, True), (2, False)):
             a = {k: v[:M] if k in ("R", "y", "inj") else v for k, v in d.items()}
             sub = dict(case, R=case["R"][:M], y=case["y"][:M], inj=case["inj"][:M], M=M)
             fwd = op.forward(a["R"], a["y"], a["inj"], a["Wnorm"], a["Wu"], Wd=a["Wd"], Wi=a["Wi"],
