@@ -47,8 +47,8 @@ FLOPS_PER_TOKEN = 2 * K_DIM * (R_LOW + HC + R_LOW)
 # since, roofline.traffic is null and roofline.traffic_source says why.
 DECODE_SOURCES = ("decode.cu", "hc_gr_internal.cuh", "tmap.h")
 DECODE_TRAFFIC = {
-    "sources_sha256": "3494ce2db83f400b10ba3099c388ec183bbf052edff4753dd21c37cee675adbd",
-    "bytes": {2: 13580885, 4: 13864277, 8: 14429355, 16: 15526229, 32: 16545536},
+    "sources_sha256": "cbdcd3472c86401ed797328aa1a5267fa4ec1f9d62f8a7b2f181069494d3bd4f",
+    "bytes": {2: 13579691, 4: 13862656, 8: 14428501, 16: 15519147, 32: 16545536},
 }
 
 

@@ -402,59 +402,6 @@ __device__ __forceinline__ bool all_set(const uint4& v) {
 __device__ __forceinline__ uint32_t xword(float v) {
   return v != v ? 0x7fc00000u : __float_as_uint(v);
 }
-// Spin (bounded) until four consecutive exchange words all hold values.
-// For words that one reader polls (each waiter its own words); words many
-// readers share are better published through a counter (wait_count).  Gives
-// up when the status word reports an error elsewhere or after the time limit
-// (then it reports the timeout itself).
-__device__ __forceinline__ bool xwait4(const uint32_t* p, uint4& v, int* err, long long limit) {
-  v = ld_relaxed_v4(p);
-  if (all_set(v)) return true;
-  const long long t0 = clock64();
-  uint32_t it = 0;
-  while (true) {
-    v = ld_relaxed_v4(p);
-    if (all_set(v)) return true;
-    if ((++it & 15u) == 0) {
-      if (*((volatile int*)err) != DEV_OK) return false;
-      if (clock64() - t0 > limit) {
-        atomicCAS(err, DEV_OK, DEV_TIMEOUT);
-        return false;
-      }
-    }
-  }
-}
-
-// Counters of exchanges whose words many readers share (32-bit, in the
-// control block after the call ticket, so every reset of the ticket clears
-// them): each producer CTA makes its words visible, then adds 1 with release
-// semantics; one thread of each reader CTA waits (acquire) until the count is
-// complete, sleeping briefly between reads, and then its CTA reads the words
-// once.  Many threads spinning on words that every CTA reads crowd the L2
-// slices those words live in.
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-__device__ __forceinline__ bool wait_count(const unsigned* p, unsigned target, int* err,
-                                           long long limit) {
-  if (ld_acquire_u32(p) >= target) return true;
-  const long long t0 = clock64();
-  while (true) {
-    __nanosleep(64);
-    if (ld_acquire_u32(p) >= target) return true;
-    if (*((volatile int*)err) != DEV_OK) return false;
-    if (clock64() - t0 > limit) {
-      atomicCAS(err, DEV_OK, DEV_TIMEOUT);
-      return false;
-    }
-  }
-}
-
 // Writes that an earlier grid made with ordinary stores, ordered before this
 // thread's later async-proxy (TMA) reads of global memory.
 __device__ __forceinline__ void fence_proxy_async_global() {

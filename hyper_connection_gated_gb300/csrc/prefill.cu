@@ -622,9 +622,12 @@ constexpr int K2_MAX_ST = 8;     // stage ring slots
 constexpr int K2_MAX_R2 = 16;    // R2 stream slots
 constexpr uint32_t K2_BAR_BYTES = 512;
 
+// Channels per unit: 64 up to HC = 4, 32 above (MMA N = HC * NCU <= 256).
+// At HC = 4 the host halves the block (N = 128) when even the halved units
+// fit one round over the SMs (one 128-token tile).
 __host__ __device__ constexpr int k2_ncu(int hc) { return hc <= 4 ? 64 : 32; }
-__host__ __device__ constexpr uint32_t k2_tmem_cols(int hc) {
-  return 2 * hc * k2_ncu(hc) <= 128 ? 128u : (2 * hc * k2_ncu(hc) <= 256 ? 256u : 512u);
+__host__ __device__ constexpr uint32_t k2_tmem_cols(int hc, int ncu) {
+  return 2 * hc * ncu <= 128 ? 128u : (2 * hc * ncu <= 256 ? 256u : 512u);
 }
 
 struct K2Params {
@@ -652,16 +655,16 @@ __device__ __forceinline__ uint32_t swz_off(int row, int chunk) {
   else return row * 32 + ((chunk ^ ((row >> 2) & 1)) << 4);
 }
 
-template <int HCT>
+template <int HCT, int NCUT>
 __global__ void __launch_bounds__(K2_THREADS, 1) k2_kernel(const __grid_constant__ K2Params p) {
   extern __shared__ unsigned char smem_raw[];
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int HC = HCT;
-  constexpr int NCU = k2_ncu(HCT);
+  constexpr int NCU = NCUT;
   constexpr int N = HC * NCU;
   constexpr uint32_t BOXB = BM * NCU * 2;        // one stream's R2 box
-  constexpr uint32_t TMEM_COLS = k2_tmem_cols(HCT);
+  constexpr uint32_t TMEM_COLS = k2_tmem_cols(HCT, NCUT);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int HS = p.HS, nkb = p.nkb, nst = p.nst, nr2 = p.nr2;
   const uint32_t sbase = smem_u32(smem);
@@ -908,14 +911,14 @@ cudaError_t launch_k1(const K1Params& p, int grid, size_t smem, const Device& de
   return launch_maybe_pdl(k1_kernel<HCT, INJ_MMA>, dim3(grid), dim3(K1_THREADS), smem, stream, pdl, p);
 }
 
-template <int HCT>
+template <int HCT, int NCUT = k2_ncu(HCT)>
 cudaError_t launch_k2(const K2Params& p, int grid, size_t smem, const Device& dev,
                       cudaStream_t stream, bool pdl) {
   static std::atomic<unsigned long long> attr{0};
-  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k2_kernel<HCT>), dev.smem_optin,
-                                  dev.id, attr);
+  cudaError_t e = smem_limit_once(reinterpret_cast<const void*>(k2_kernel<HCT, NCUT>),
+                                  dev.smem_optin, dev.id, attr);
   if (e != cudaSuccess) return e;
-  return launch_maybe_pdl(k2_kernel<HCT>, dim3(grid), dim3(K2_THREADS), smem, stream, pdl, p);
+  return launch_maybe_pdl(k2_kernel<HCT, NCUT>, dim3(grid), dim3(K2_THREADS), smem, stream, pdl, p);
 }
 
 bool prefill_supported(const Call& c) {
@@ -923,6 +926,18 @@ bool prefill_supported(const Call& c) {
 }
 static_assert(k2_ncu(4) * 4 == 256 && k2_ncu(8) * 8 == 256 && k2_ncu(1) * 8 <= 512,
               "K2 MMA N = 256 for HC = 4 and 8; 2N tensor-memory columns fit");
+
+// K2's channel block at HC = 4: 32 instead of 64 when the halved units still
+// fit one round over the SMs, so that the same work spreads over twice the
+// CTAs.  Measured on the GB300 at HS = 2560: 1.1 us less at M = 128 (40 or
+// 80 units); where halving adds rounds it costs more than it saves (+0.5 us
+// at M = 512, +5 at 2048, +12 at 4096: a unit's cost is far from
+// proportional to its channels).
+int k2_block(int HC, int n_mt, int HS, int sms) {
+  const int ncu = k2_ncu(HC);
+  if (HC != 4 || HS % 32 != 0) return ncu;
+  return static_cast<int64_t>(n_mt) * (HS / 32) <= sms ? 32 : ncu;
+}
 
 
 // K chunks per stream: enough (tile, stream, chunk) CTAs to cover the SMs
@@ -1107,7 +1122,7 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   // ---------------- K2
   {
     K2Params p;
-    const int ncu = k2_ncu(c.HC);
+    const int ncu = k2_block(c.HC, n_mt, c.HS, dev.sms);
     const int N = c.HC * ncu;
     const uint64_t dh[2] = {static_cast<uint64_t>(c.r), static_cast<uint64_t>(M)};
     const uint64_t sh[1] = {static_cast<uint64_t>(c.r) * 2};
@@ -1160,7 +1175,8 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
       case 1: e = launch_k2<1>(p, grid, smem, dev, stream, true); break;
       case 2: e = launch_k2<2>(p, grid, smem, dev, stream, true); break;
       case 3: e = launch_k2<3>(p, grid, smem, dev, stream, true); break;
-      case 4: e = launch_k2<4>(p, grid, smem, dev, stream, true); break;
+      case 4: e = ncu == 32 ? launch_k2<4, 32>(p, grid, smem, dev, stream, true)
+                            : launch_k2<4>(p, grid, smem, dev, stream, true); break;
       case 5: e = launch_k2<5>(p, grid, smem, dev, stream, true); break;
       case 6: e = launch_k2<6>(p, grid, smem, dev, stream, true); break;
       case 7: e = launch_k2<7>(p, grid, smem, dev, stream, true); break;
