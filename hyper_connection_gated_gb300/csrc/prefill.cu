@@ -486,14 +486,12 @@ __global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
   constexpr int NCOL = RED_COLS / 8;
   const int ns = HC * S;
   const int64_t tb = static_cast<int64_t>(tile) * ns;
-  float4 q[HC];
+  float4 rs[HC];
   float4 pv[NCOL][HC];
-  // with one K chunk per stream (the usual case) every load issues before
-  // any is used; with K chunks, the chunks' loads issue CB at a time (their
-  // sums are still added in chunk order).  CB = 2 halves the chain of
-  // dependent loads a thread waits through, at half the resident blocks, so
-  // the host picks it only when the grid fits one wave either way.
   if (S == 1) {
+    // one K chunk per stream (the usual case): every load issues before any
+    // is used
+    float4 q[HC];
 #pragma unroll
     for (int ss = 0; ss < HC; ++ss)
       q[ss] = __ldcg(reinterpret_cast<const float4*>(sumsq + (tb + ss) * BM + r4));
@@ -504,53 +502,61 @@ __global__ void __launch_bounds__(RED_THREADS, CB > 1 || HC > 4 ? 2 : 4)
       for (int ss = 0; ss < HC; ++ss)
         pv[j][ss] = __ldcg(reinterpret_cast<const float4*>(part + ((tb + ss) * np + n) * BM + r4));
     }
+#pragma unroll
+    for (int ss = 0; ss < HC; ++ss)
+      rs[ss] = make_float4(rsqrt_nr(fmaf(q[ss].x, inv_hs, eps)), rsqrt_nr(fmaf(q[ss].y, inv_hs, eps)),
+                           rsqrt_nr(fmaf(q[ss].z, inv_hs, eps)), rsqrt_nr(fmaf(q[ss].w, inv_hs, eps)));
   } else {
+    // K chunks: the chunks' loads issue CB at a time (their sums are still
+    // added in chunk order).  Warp w < HC also sums stream w's partial sums
+    // of squares for its lanes' rows and shares the stream's rrms through
+    // shared memory, so a thread's batch holds its column's products and at
+    // most one stream's squares instead of every stream's: fewer dependent
+    // batches for the same registers.  CB > 1 halves the resident blocks, so
+    // the host picks it only when the grid fits one wave either way.
+    __shared__ float4 s_rs[HC][32];
+    float4 qw = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-  for (int ss = 0; ss < HC; ++ss) q[ss] = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < NCOL; ++j)
 #pragma unroll
-  for (int j = 0; j < NCOL; ++j)
-#pragma unroll
-    for (int ss = 0; ss < HC; ++ss) pv[j][ss] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int ss = 0; ss < HC; ++ss) pv[j][ss] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 1
-  for (int c0 = 0; c0 < S; c0 += CB) {
-    float4 qc[CB][HC], vc[CB][NCOL][HC];
+    for (int c0 = 0; c0 < S; c0 += CB) {
+      float4 qc[CB], vc[CB][NCOL][HC];
 #pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      const int c = min(c0 + u, S - 1);
+      for (int u = 0; u < CB; ++u) {
+        const int c = min(c0 + u, S - 1);
+        qc[u] = cw < HC ? __ldcg(reinterpret_cast<const float4*>(sumsq + (tb + cw * S + c) * BM + r4))
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int ss = 0; ss < HC; ++ss)
-        qc[u][ss] = __ldcg(reinterpret_cast<const float4*>(sumsq + (tb + ss * S + c) * BM + r4));
+        for (int j = 0; j < NCOL; ++j) {
+          const int n = min(n0 + cw + 8 * j, np - 1);
 #pragma unroll
-      for (int j = 0; j < NCOL; ++j) {
-        const int n = min(n0 + cw + 8 * j, np - 1);
-#pragma unroll
-        for (int ss = 0; ss < HC; ++ss)
-          vc[u][j][ss] = __ldcg(reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4));
-      }
-    }
-#pragma unroll
-    for (int u = 0; u < CB; ++u) {
-      if (c0 + u < S) {
-#pragma unroll
-        for (int ss = 0; ss < HC; ++ss) {
-          q[ss].x += qc[u][ss].x; q[ss].y += qc[u][ss].y; q[ss].z += qc[u][ss].z; q[ss].w += qc[u][ss].w;
+          for (int ss = 0; ss < HC; ++ss)
+            vc[u][j][ss] = __ldcg(reinterpret_cast<const float4*>(part + ((tb + ss * S + c) * np + n) * BM + r4));
         }
+      }
 #pragma unroll
-        for (int j = 0; j < NCOL; ++j)
+      for (int u = 0; u < CB; ++u) {
+        if (c0 + u < S) {
+          qw.x += qc[u].x; qw.y += qc[u].y; qw.z += qc[u].z; qw.w += qc[u].w;
 #pragma unroll
-          for (int ss = 0; ss < HC; ++ss) {
-            pv[j][ss].x += vc[u][j][ss].x; pv[j][ss].y += vc[u][j][ss].y;
-            pv[j][ss].z += vc[u][j][ss].z; pv[j][ss].w += vc[u][j][ss].w;
-          }
+          for (int j = 0; j < NCOL; ++j)
+#pragma unroll
+            for (int ss = 0; ss < HC; ++ss) {
+              pv[j][ss].x += vc[u][j][ss].x; pv[j][ss].y += vc[u][j][ss].y;
+              pv[j][ss].z += vc[u][j][ss].z; pv[j][ss].w += vc[u][j][ss].w;
+            }
+        }
       }
     }
-  }
-  }
-  float4 rs[HC];
+    if (cw < HC)
+      s_rs[cw][tid & 31] = make_float4(rsqrt_nr(fmaf(qw.x, inv_hs, eps)), rsqrt_nr(fmaf(qw.y, inv_hs, eps)),
+                                       rsqrt_nr(fmaf(qw.z, inv_hs, eps)), rsqrt_nr(fmaf(qw.w, inv_hs, eps)));
+    __syncthreads();
 #pragma unroll
-  for (int ss = 0; ss < HC; ++ss)
-    rs[ss] = make_float4(rsqrt_nr(fmaf(q[ss].x, inv_hs, eps)), rsqrt_nr(fmaf(q[ss].y, inv_hs, eps)),
-                         rsqrt_nr(fmaf(q[ss].z, inv_hs, eps)), rsqrt_nr(fmaf(q[ss].w, inv_hs, eps)));
+    for (int ss = 0; ss < HC; ++ss) rs[ss] = s_rs[ss][tid & 31];
+  }
   if (blockIdx.x == 0 && cw == 0) {
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -1101,11 +1107,11 @@ cudaError_t launch_prefill(const Call& c, const Workspace& ws, const Device& dev
   // ---------------- reduce
   {
     const dim3 grid((np + RED_COLS - 1) / RED_COLS, n_mt);
-    const bool batch2 = S > 1 && static_cast<int64_t>(grid.x) * grid.y <= 2 * dev.sms;
+    const bool batched = S > 1 && static_cast<int64_t>(grid.x) * grid.y <= 2 * dev.sms;
     cudaError_t e = cudaSuccess;
 #define HCGR_RED(HCV)                                                                        \
   case HCV:                                                                                  \
-    e = launch_maybe_pdl(batch2 ? k1_reduce_kernel<HCV, (HCV <= 4 ? 2 : 1)>                \
+    e = launch_maybe_pdl(batched ? k1_reduce_kernel<HCV, (HCV <= 4 ? 3 : 2)>               \
                                 : k1_reduce_kernel<HCV, 1>,                                  \
                          grid, dim3(RED_THREADS), 0, stream, true, (const float*)part,        \
                          (const float*)sumsq, c.rrms, c.lora, c.inj_next, h, c.Wnorm,         \
