@@ -82,12 +82,13 @@ constexpr int DECODE_MAX_M = 64;
 // The M dispatch's threshold: the decode kernel while M <= DECODE_MAX_M and
 // M * K <= DECODE_AUTO_MAX_MK, the prefill kernels above.  Measured on the
 // GB300 (graph replay, weights from HBM, programmatic dependent launches):
-// at HC=4, HS=2560, r=320 (K = 10240) decode takes 14.6 / 16.1 / 18.7 / 21.0 /
-// 22.3 / 23.2 us at M = 24 / 32 / 40 / 48 / 56 / 64 against 25.6 - 26.2 us for
+// at HC=4, HS=2560, r=320 (K = 10240) decode takes 14.6 / 16.0 / 19.1 / 21.3 /
+// 22.4 / 23.3 us at M = 24 / 32 / 40 / 48 / 56 / 64 against 23.1 - 23.6 us for
 // prefill, so decode wins up to its 64-token limit; at HC=8, HS=4096, r=512
-// (K = 32768) decode takes 39.2 / 51.4 us at M = 16 / 24 against 50.0 / 50.4
-// us, so the paths cross near 20 tokens.  Both crossovers sit at about the
-// same M * K: the decode kernel's per-token work grows with the width K.
+// (K = 32768) decode takes 38.3 / 41.9 / 49.9 us at M = 16 / 20 / 24 against
+// 43.7 / 43.8 / 44.1 us, so the paths cross between 20 and 24 tokens.  Both
+// crossovers sit at about the same M * K: the decode kernel's per-token work
+// grows with the width K.
 constexpr int64_t DECODE_AUTO_MAX_MK = 64LL * 10240;
 constexpr int MAX_GRID = 256;            // largest prefill grid the scratch is sized for
 constexpr int CTL_BYTES = MAX_GRID * 8 + 256;   // ticket at 0, status word at MAX_GRID * 8
