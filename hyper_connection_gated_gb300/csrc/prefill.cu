@@ -457,8 +457,9 @@ __global__ void __launch_bounds__(K1_THREADS, 1) k1_kernel(const __grid_constant
 // x RED_COLS columns: it reads the column-major partials in float4s, 512
 // contiguous bytes per warp, column and stream, and transposes through shared
 // memory to write the row-major outputs in 32-byte row runs.  Eight columns
-// a block keep a thread at one column (64 registers at HC <= 4: four blocks
-// an SM), so more loads are in flight per SM than with 16.
+// a block keep a thread at one column (at HC <= 4 under 64 registers with one
+// K chunk per batch: four blocks an SM), so more loads are in flight per SM
+// than with 16.
 constexpr int RED_THREADS = 256;
 constexpr int RED_COLS = 8;           // columns per block (a block covers a whole 128-row tile)
 
